@@ -55,7 +55,8 @@ READINGS = {
     "lr_scale": "lr * muon_lr_scale * 0.2 * sqrt(max(rows, cols)) of the full matrix",
     "muon_weight_decay": "decoupled p *= 1 - lr*wd with the base lr, wd 0.1",
     "adamw": "PyTorch AdamW: decoupled decay first, eps outside sqrt of bias-corrected v",
-    "clip": "coef = min(1, max_norm/(total+1e-6)) over both groups' gradients, before either update",
+    "clip": "coef = min(1, max_norm/(total+1e-6)) over both groups' gradients, before either update; "
+            "a NaN norm gives a NaN coefficient, an infinite norm gives 0",
     "schedule": "HF cosine_with_min_lr, num_cycles 0.5, lr = base*(min + (1-min)*0.5*(1+cos(pi*p)))",
 }
 
@@ -110,9 +111,17 @@ def global_grad_norm(grads: Sequence[np.ndarray]) -> float:
 
 
 def clip_coefficient(total: float, max_norm: float, eps: float = 1e-6) -> float:
-    """Factor applied to every gradient: min(1, max_norm / (total + eps))."""
+    """Factor applied to every gradient: min(1, max_norm / (total + eps)).
+
+    The article gives no rule for a non-finite norm. Reading: no step is
+    skipped; a NaN norm gives a NaN factor (every update becomes NaN, as
+    multiplying the gradients by the unclamped ratio would), and an infinite
+    norm gives the factor 0.
+    """
     if max_norm <= 0.0:
         return 1.0
+    if math.isnan(total):
+        return float("nan")
     return min(1.0, max_norm / (total + eps))
 
 

@@ -289,6 +289,13 @@ def test_clip_hand_values():
     assert oracle.clip_coefficient(5.0, 0.0) == 1.0  # max_norm <= 0 disables
 
 
+def test_clip_non_finite():
+    assert math.isnan(oracle.clip_coefficient(float("nan"), 1.0))
+    assert oracle.clip_coefficient(float("inf"), 1.0) == 0.0
+    assert math.isnan(oracle.global_grad_norm([np.array([1.0, np.nan])]))
+    assert oracle.global_grad_norm([np.array([np.inf, 1.0])]) == float("inf")
+
+
 # ---------------------------------------------------------------------------
 # Schedule
 # ---------------------------------------------------------------------------
