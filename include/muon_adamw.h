@@ -1,0 +1,247 @@
+/*
+ * muon_adamw.h -- C ABI of a single-GPU hybrid Muon + AdamW optimizer step
+ * for GB300 (sm_103a).
+ *
+ * The method is the MuonAdamW hybrid optimizer of the OpenDM VLA training
+ * stack, as described in the article "VLA训练栈深度揭秘：OpenDM的Muon+AdamW优化器、
+ * FSDP分布式训练与混合精度策略" (gsyq.cn/news/451971), section 核心揭秘一:
+ *
+ *   - routing (参数如何分流): 2-D parameters whose path holds action_expert
+ *     and sits under layers, ending in .weight, and that are not embeddings,
+ *     lm_head or norms, go to Muon; every other trainable parameter goes to
+ *     AdamW; the optim switch "adamw" sends everything to AdamW;
+ *   - Muon (Muon 的工作原理, 关键超参默认值): Nesterov momentum 0.95, then
+ *     five Newton-Schulz iterations that approximate the orthogonal factor
+ *     of the update on its short side, then the step
+ *     lr * muon_lr_scale * 0.2 * sqrt(max(rows, cols));
+ *   - the training-stack defaults table (训练栈默认参数速查表): gradient
+ *     clipping at max_grad_norm 1.0 and the cosine_with_min_lr schedule with
+ *     min_lr_rate 0.1.
+ *
+ * Conventions for every call:
+ *   - Return value: MA_OK or an error status. No C++ exception crosses this
+ *     boundary. On error a message is kept per thread and read with
+ *     muon_adamw_last_error().
+ *   - Device pointers are CUDA device addresses in the current device's
+ *     primary context (e.g. torch tensors' data_ptr()). Host pointers are
+ *     marked "host".
+ *   - Tensors are dense and row-major (PyTorch [out, in] for matrices).
+ *   - The caller owns parameters, gradients and bf16 shadows; they must stay
+ *     allocated at the same address until muon_adamw_destroy(). The library
+ *     owns its optimizer state and workspaces (allocated at the first step,
+ *     freed by destroy) and never frees caller memory.
+ *   - All device work is queued on the stream given to muon_adamw_create();
+ *     calls return before the GPU finishes unless stated otherwise.
+ *   - A handle is not thread-safe: serialise calls on one handle.
+ */
+#ifndef MUON_ADAMW_H
+#define MUON_ADAMW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MA_API __attribute__((visibility("default")))
+#else
+#define MA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct muon_adamw muon_adamw_t; /* opaque handle, owned by the library */
+
+typedef enum {
+  MA_OK = 0,
+  MA_ERR_ARG = 1,          /* null pointer, bad enum, out-of-range value */
+  MA_ERR_SHAPE = 2,        /* ndim/shape not usable for the assigned group */
+  MA_ERR_DTYPE = 3,        /* gradient dtype not F32/BF16 */
+  MA_ERR_ALIGN = 4,        /* pointer not aligned to its element size */
+  MA_ERR_STATE = 5,        /* call not valid now (e.g. register after the first step) */
+  MA_ERR_OOM = 6,          /* device allocation failed */
+  MA_ERR_CUDA = 7,         /* a CUDA runtime/driver call failed */
+  MA_ERR_DEVICE_CHECK = 8, /* a kernel's own check failed (bounded wait ran out) */
+  MA_ERR_UNSUPPORTED = 9   /* device is not sm_103 / feature not built */
+} ma_status;
+
+typedef enum { MA_MODE_MUON_ADAMW = 0, MA_MODE_ADAMW_ONLY = 1 } ma_mode;      /* optim switch */
+typedef enum { MA_BF16_MIXED = 0, MA_FP32_MIXED = 1 } ma_precision;           /* precision_policy */
+typedef enum { MA_GROUP_AUTO = 0, MA_GROUP_MUON = 1, MA_GROUP_ADAMW = 2, MA_GROUP_FROZEN = 3 } ma_group;
+typedef enum { MA_DT_F32 = 0, MA_DT_BF16 = 1 } ma_dtype;
+typedef enum { MA_NS_TCGEN05 = 0, MA_NS_SIMT = 1 } ma_ns_kernel;
+
+/* Optimizer configuration. Fill with muon_adamw_config_init(), then edit.
+ * Defaults (article section in brackets):
+ *   mode MA_MODE_MUON_ADAMW; precision MA_BF16_MIXED [核心揭秘三: bf16_mixed is
+ *   the default policy; under it the library also writes a bf16 copy of each
+ *   updated parameter when a shadow pointer is registered];
+ *   muon_momentum 0.95, muon_nesterov 1, ns_steps 5, moonlight_coef 0.2
+ *   [关键超参默认值]; muon_lr_scale 1.0 (named there without a value);
+ *   ns_a/ns_b/ns_c 3.4445/-4.7750/2.0315 and ns_eps 1e-7 (the standard Muon
+ *   quintic; not printed on the page); muon_weight_decay 0.1 (decoupled,
+ *   base lr); adam_beta1 0.9, adam_beta2 0.999, adam_eps 1e-8,
+ *   adam_weight_decay 0.1; max_grad_norm 1.0 [训练栈默认参数速查表]
+ *   (<= 0 disables clipping); clip_eps 1e-6;
+ *   ns_kernel MA_NS_TCGEN05 (MA_NS_SIMT selects a slow CUDA-core GEMM used
+ *   to cross-check the tensor-core kernel). */
+typedef struct {
+  int32_t mode;
+  int32_t precision;
+  float muon_momentum;
+  int32_t muon_nesterov;
+  int32_t ns_steps;
+  float ns_a, ns_b, ns_c;
+  float ns_eps;
+  float moonlight_coef;
+  float muon_lr_scale;
+  float muon_weight_decay;
+  float adam_beta1, adam_beta2, adam_eps, adam_weight_decay;
+  float max_grad_norm;
+  float clip_eps;
+  int32_t ns_kernel;
+  int32_t reserved[7];
+} muon_adamw_config;
+
+/* Per-kernel timing collected while profiling is on (see muon_adamw_set_profiling).
+ * Index = ma_kernel_kind. ms = summed CUDA-event time of that kernel's launches
+ * (events recorded on the stream the kernel runs on); units = algorithmic
+ * work of those launches: bytes for HBM-bound kernels, flops for the NS GEMMs
+ * (symmetric count: A = XX^T and A*A count the lower triangle only). */
+typedef enum {
+  MA_K_GRAD_NORM = 0,   /* sum of squares of all gradients */
+  MA_K_CLIP = 1,        /* norm finalise + clip coefficient */
+  MA_K_MOMENTUM = 2,    /* Muon Nesterov momentum + canonical bf16 pack */
+  MA_K_NS_PREP = 3,     /* per-matrix Frobenius scale */
+  MA_K_NS_GRAM = 4,     /* A = X X^T (iteration 1 scaled by 1/||G||^2) */
+  MA_K_NS_POLY = 5,     /* B = b A + c A A */
+  MA_K_NS_UPDATE = 6,   /* X <- a X + B X (last iteration applies the step) */
+  MA_K_ADAMW = 7,       /* fused multi-tensor AdamW */
+  MA_K_COUNT = 8
+} ma_kernel_kind;
+
+typedef struct {
+  int64_t launches[MA_K_COUNT];
+  double ms[MA_K_COUNT];
+  double units[MA_K_COUNT];
+  int64_t steps;
+} ma_profile;
+
+/* Sizes of the frozen step plan (valid after the first step). */
+typedef struct {
+  int32_t n_params, n_muon, n_adamw, n_frozen;
+  int32_t n_buckets;          /* groups of Muon matrices of equal padded canonical shape */
+  int64_t muon_elems, adamw_elems, grad_elems;
+  int64_t state_bytes, workspace_bytes;
+  double ns_flops_per_step;   /* symmetric algorithmic count */
+  double ns_dense_flops_per_step;
+  double stream_bytes_per_step; /* algorithmic HBM bytes of the streaming kernels */
+} ma_plan_info;
+
+/* Fill *cfg with the defaults listed above. cfg must not be NULL. */
+MA_API void muon_adamw_config_init(muon_adamw_config* cfg);
+
+/* Routing predicate of 参数如何分流, as a pure host function: returns 1 when a
+ * parameter called `name` (UTF-8, NUL-terminated) with `ndim` dimensions goes
+ * to Muon, 0 otherwise (also for name == NULL). The match is: ndim == 2;
+ * `name` contains "action_expert"; one dot-separated component equals
+ * "layers"; `name` ends with ".weight"; the lower-cased name contains none of
+ * "embed", "lm_head", "norm". */
+MA_API int muon_adamw_is_muon_param(const char* name, int ndim);
+
+/* Multiplier of the base lr for the cosine_with_min_lr schedule
+ * (训练栈默认参数速查表): linear warmup over `warmup` steps, then
+ * min_lr_rate + (1 - min_lr_rate) * 0.5 * (1 + cos(pi * progress)),
+ * progress = (step - warmup) / (total - warmup). Pure host function. */
+MA_API double muon_adamw_cosine_with_min_lr(int64_t step, int64_t total, int64_t warmup, double min_lr_rate);
+
+/* Create an optimizer. cfg: host, copied. cuda_stream: a cudaStream_t (NULL =
+ * legacy default stream) on the current device; all work of this handle is
+ * ordered on it (a second, library-owned stream runs AdamW concurrently and
+ * is joined back before each step returns). *out receives the handle.
+ * Errors: MA_ERR_ARG (NULL out/cfg, invalid config values), MA_ERR_UNSUPPORTED
+ * (current device is not compute capability 10.3), MA_ERR_CUDA. */
+MA_API ma_status muon_adamw_create(const muon_adamw_config* cfg, void* cuda_stream, muon_adamw_t** out);
+
+/* Register one parameter, before the first step.
+ *   name        host UTF-8 string (copied), used for routing;
+ *   ndim, shape host array of ndim int64 sizes (ndim 0..8, sizes >= 0);
+ *   param_fp32  device fp32 master weights, numel elements (updated in place;
+ *               may be NULL only for MA_GROUP_FROZEN);
+ *   grad        device gradient, numel elements of grad_dtype (MA_DT_BF16 or
+ *               MA_DT_F32); read each step, never written; NULL only when frozen;
+ *   param_bf16_shadow  device bf16 copy written after each update when the
+ *               precision is MA_BF16_MIXED, or NULL for none;
+ *   group_override  MA_GROUP_AUTO applies the routing predicate (and the
+ *               mode); MUON/ADAMW/FROZEN force the group (MUON needs ndim 2);
+ *   assigned    host out (may be NULL): the group used;
+ *   index_out   host out (may be NULL): registration index (0, 1, ...).
+ * Errors: MA_ERR_ARG, MA_ERR_SHAPE, MA_ERR_DTYPE, MA_ERR_ALIGN (pointer not
+ * aligned to its element size), MA_ERR_STATE (after the first step). */
+MA_API ma_status muon_adamw_register_param(muon_adamw_t* h, const char* name, int ndim, const int64_t* shape,
+                                    float* param_fp32, const void* grad, int grad_dtype,
+                                    void* param_bf16_shadow, int group_override, int* assigned,
+                                    int* index_out);
+
+/* One optimizer step with base learning rate `lr` (the caller applies its
+ * schedule, stepped once per optimizer step). The first call freezes the
+ * plan and allocates state and workspaces. Queues on the handle's stream:
+ * global grad norm and clip coefficient; Muon momentum, Newton-Schulz and
+ * update; AdamW. grad_norm_out: host out (NULL = fully asynchronous); when
+ * given, the call synchronises the stream and stores the pre-clip global
+ * gradient norm, and also reports a failed in-kernel check as
+ * MA_ERR_DEVICE_CHECK. Non-finite gradients are not skipped: they propagate
+ * into the parameters and the norm. Errors: MA_ERR_ARG (lr not finite),
+ * MA_ERR_OOM, MA_ERR_CUDA, MA_ERR_DEVICE_CHECK. */
+MA_API ma_status muon_adamw_step(muon_adamw_t* h, float lr, float* grad_norm_out);
+
+/* Wait for the handle's stream and read the kernels' error flag.
+ * MA_ERR_DEVICE_CHECK if a bounded in-kernel wait ran out. */
+MA_API ma_status muon_adamw_sync(muon_adamw_t* h);
+
+/* Copy optimizer state of parameter `index` to host memory `dst_host`
+ * (numel fp32 values). which = 0: Muon momentum buffer or AdamW first
+ * moment; which = 1: AdamW second moment. Synchronises the stream.
+ * Errors: MA_ERR_ARG (bad index/which, NULL dst), MA_ERR_STATE (before the
+ * first step, or a frozen parameter). */
+MA_API ma_status muon_adamw_get_state(muon_adamw_t* h, int index, int which, float* dst_host);
+
+/* Replace the same state from host memory `src_host` (numel fp32 values),
+ * for resuming from a checkpoint; also valid before the first step (the
+ * plan is then frozen by this call). Synchronises the stream. */
+MA_API ma_status muon_adamw_set_state(muon_adamw_t* h, int index, int which, const float* src_host);
+
+/* Step counter t used for bias correction (number of completed steps), and
+ * setter for resuming (t >= 0). */
+MA_API ma_status muon_adamw_get_step(muon_adamw_t* h, int64_t* t_out);
+MA_API ma_status muon_adamw_set_step(muon_adamw_t* h, int64_t t);
+
+/* Last step's global gradient norm and clip coefficient (synchronises). */
+MA_API ma_status muon_adamw_last_norm(muon_adamw_t* h, float* total_out, float* coef_out);
+
+/* Plan sizes (after the first step; MA_ERR_STATE before). */
+MA_API ma_status muon_adamw_plan_info(muon_adamw_t* h, ma_plan_info* out);
+
+/* Per-kernel CUDA-event timing. enable = 1 records an event pair around every
+ * kernel launch of subsequent steps (on the launching stream); 0 stops.
+ * get_profile synchronises, folds the recorded events into *out (host) and
+ * keeps accumulating; reset clears the totals. */
+MA_API ma_status muon_adamw_set_profiling(muon_adamw_t* h, int enable);
+MA_API ma_status muon_adamw_get_profile(muon_adamw_t* h, ma_profile* out);
+MA_API ma_status muon_adamw_reset_profile(muon_adamw_t* h);
+
+/* Free the library's state and workspaces (after waiting for the stream)
+ * and the handle. Caller memory is not touched. h == NULL is MA_ERR_ARG. */
+MA_API ma_status muon_adamw_destroy(muon_adamw_t* h);
+
+/* Message of the last error on this thread ("" if none). Never NULL. */
+MA_API const char* muon_adamw_last_error(void);
+
+/* Library version string, e.g. "0.1.0 sm_103a". */
+MA_API const char* muon_adamw_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_ADAMW_H */

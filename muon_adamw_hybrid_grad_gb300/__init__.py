@@ -1,0 +1,366 @@
+"""Python binding of the GB300 hybrid Muon + AdamW optimizer library.
+
+Argument marshalling only: every step of the optimizer runs in the CUDA
+kernels of ``lib/libmuon_adamw_gb300.so`` behind the C ABI declared in
+``include/muon_adamw.h``. The functions below carry the C names; the
+``MuonAdamW`` class is a convenience wrapper that takes torch tensors and
+passes their device pointers and the current CUDA stream.
+
+There is no fallback: if the shared library has not been built, every call
+raises ``LibraryNotBuilt`` (run ``muon_adamw_hybrid_grad_gb300.build.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+from . import build as _build
+
+# ---- enums (mirror include/muon_adamw.h) ----
+MA_OK = 0
+MA_ERR_ARG = 1
+MA_ERR_SHAPE = 2
+MA_ERR_DTYPE = 3
+MA_ERR_ALIGN = 4
+MA_ERR_STATE = 5
+MA_ERR_OOM = 6
+MA_ERR_CUDA = 7
+MA_ERR_DEVICE_CHECK = 8
+MA_ERR_UNSUPPORTED = 9
+STATUS_NAMES = {0: "MA_OK", 1: "MA_ERR_ARG", 2: "MA_ERR_SHAPE", 3: "MA_ERR_DTYPE", 4: "MA_ERR_ALIGN",
+                5: "MA_ERR_STATE", 6: "MA_ERR_OOM", 7: "MA_ERR_CUDA", 8: "MA_ERR_DEVICE_CHECK",
+                9: "MA_ERR_UNSUPPORTED"}
+
+MA_MODE_MUON_ADAMW = 0
+MA_MODE_ADAMW_ONLY = 1
+MA_BF16_MIXED = 0
+MA_FP32_MIXED = 1
+MA_GROUP_AUTO = 0
+MA_GROUP_MUON = 1
+MA_GROUP_ADAMW = 2
+MA_GROUP_FROZEN = 3
+MA_DT_F32 = 0
+MA_DT_BF16 = 1
+MA_NS_TCGEN05 = 0
+MA_NS_SIMT = 1
+
+KERNEL_KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "adamw")
+MA_K_COUNT = len(KERNEL_KINDS)
+GROUP_NAMES = {MA_GROUP_MUON: "muon", MA_GROUP_ADAMW: "adamw", MA_GROUP_FROZEN: "frozen"}
+
+
+class MuonAdamWConfig(ctypes.Structure):
+    _fields_ = [
+        ("mode", ctypes.c_int32),
+        ("precision", ctypes.c_int32),
+        ("muon_momentum", ctypes.c_float),
+        ("muon_nesterov", ctypes.c_int32),
+        ("ns_steps", ctypes.c_int32),
+        ("ns_a", ctypes.c_float),
+        ("ns_b", ctypes.c_float),
+        ("ns_c", ctypes.c_float),
+        ("ns_eps", ctypes.c_float),
+        ("moonlight_coef", ctypes.c_float),
+        ("muon_lr_scale", ctypes.c_float),
+        ("muon_weight_decay", ctypes.c_float),
+        ("adam_beta1", ctypes.c_float),
+        ("adam_beta2", ctypes.c_float),
+        ("adam_eps", ctypes.c_float),
+        ("adam_weight_decay", ctypes.c_float),
+        ("max_grad_norm", ctypes.c_float),
+        ("clip_eps", ctypes.c_float),
+        ("ns_kernel", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 7),
+    ]
+
+
+class Profile(ctypes.Structure):
+    _fields_ = [
+        ("launches", ctypes.c_int64 * MA_K_COUNT),
+        ("ms", ctypes.c_double * MA_K_COUNT),
+        ("units", ctypes.c_double * MA_K_COUNT),
+        ("steps", ctypes.c_int64),
+    ]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("n_params", ctypes.c_int32),
+        ("n_muon", ctypes.c_int32),
+        ("n_adamw", ctypes.c_int32),
+        ("n_frozen", ctypes.c_int32),
+        ("n_buckets", ctypes.c_int32),
+        ("muon_elems", ctypes.c_int64),
+        ("adamw_elems", ctypes.c_int64),
+        ("grad_elems", ctypes.c_int64),
+        ("state_bytes", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_int64),
+        ("ns_flops_per_step", ctypes.c_double),
+        ("ns_dense_flops_per_step", ctypes.c_double),
+        ("stream_bytes_per_step", ctypes.c_double),
+    ]
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class MuonAdamWError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+# Exported symbols and their ctypes signatures: (restype, argtypes).
+_P = ctypes.c_void_p
+_SIGNATURES = {
+    "muon_adamw_config_init": (None, [ctypes.POINTER(MuonAdamWConfig)]),
+    "muon_adamw_is_muon_param": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_int]),
+    "muon_adamw_cosine_with_min_lr": (ctypes.c_double, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                        ctypes.c_double]),
+    "muon_adamw_create": (ctypes.c_int, [ctypes.POINTER(MuonAdamWConfig), _P, ctypes.POINTER(_P)]),
+    "muon_adamw_register_param": (ctypes.c_int, [_P, ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
+                                                 _P, _P, ctypes.c_int, _P, ctypes.c_int,
+                                                 ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+    "muon_adamw_step": (ctypes.c_int, [_P, ctypes.c_float, ctypes.POINTER(ctypes.c_float)]),
+    "muon_adamw_sync": (ctypes.c_int, [_P]),
+    "muon_adamw_get_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),
+    "muon_adamw_set_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),
+    "muon_adamw_get_step": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int64)]),
+    "muon_adamw_set_step": (ctypes.c_int, [_P, ctypes.c_int64]),
+    "muon_adamw_last_norm": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
+    "muon_adamw_plan_info": (ctypes.c_int, [_P, ctypes.POINTER(PlanInfo)]),
+    "muon_adamw_set_profiling": (ctypes.c_int, [_P, ctypes.c_int]),
+    "muon_adamw_get_profile": (ctypes.c_int, [_P, ctypes.POINTER(Profile)]),
+    "muon_adamw_reset_profile": (ctypes.c_int, [_P]),
+    "muon_adamw_destroy": (ctypes.c_int, [_P]),
+    "muon_adamw_last_error": (ctypes.c_char_p, []),
+    "muon_adamw_version": (ctypes.c_char_p, []),
+}
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the shared library (once). Raises LibraryNotBuilt if it is missing."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise LibraryNotBuilt(f"{path} is missing: build it with muon_adamw_hybrid_grad_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != MA_OK:
+        msg = load_library().muon_adamw_last_error().decode("utf-8", "replace")
+        raise MuonAdamWError(status, msg)
+
+
+# ---- C-named functions ----
+
+def muon_adamw_config_init() -> MuonAdamWConfig:
+    cfg = MuonAdamWConfig()
+    load_library().muon_adamw_config_init(ctypes.byref(cfg))
+    return cfg
+
+
+def muon_adamw_is_muon_param(name: str, ndim: int) -> bool:
+    return bool(load_library().muon_adamw_is_muon_param(name.encode("utf-8"), int(ndim)))
+
+
+def muon_adamw_cosine_with_min_lr(step: int, total: int, warmup: int, min_lr_rate: float) -> float:
+    return float(load_library().muon_adamw_cosine_with_min_lr(int(step), int(total), int(warmup), float(min_lr_rate)))
+
+
+def muon_adamw_create(cfg: MuonAdamWConfig, cuda_stream: int = 0) -> int:
+    h = _P()
+    _check(load_library().muon_adamw_create(ctypes.byref(cfg), _P(cuda_stream or None), ctypes.byref(h)))
+    return h.value
+
+
+def muon_adamw_register_param(h: int, name: str, shape: Sequence[int], param_ptr: int, grad_ptr: int,
+                              grad_dtype: int, shadow_ptr: int = 0, group: int = MA_GROUP_AUTO):
+    """Returns (index, assigned_group)."""
+    arr = (ctypes.c_int64 * max(1, len(shape)))(*[int(d) for d in shape])
+    assigned = ctypes.c_int(-1)
+    index = ctypes.c_int(-1)
+    _check(load_library().muon_adamw_register_param(
+        _P(h), name.encode("utf-8"), len(shape), arr, _P(param_ptr or None), _P(grad_ptr or None),
+        int(grad_dtype), _P(shadow_ptr or None), int(group), ctypes.byref(assigned), ctypes.byref(index)))
+    return index.value, assigned.value
+
+
+def muon_adamw_step(h: int, lr: float, want_norm: bool = False) -> Optional[float]:
+    if want_norm:
+        out = ctypes.c_float()
+        _check(load_library().muon_adamw_step(_P(h), float(lr), ctypes.byref(out)))
+        return float(out.value)
+    _check(load_library().muon_adamw_step(_P(h), float(lr), None))
+    return None
+
+
+def muon_adamw_sync(h: int) -> None:
+    _check(load_library().muon_adamw_sync(_P(h)))
+
+
+def muon_adamw_get_state(h: int, index: int, which: int, dst_ptr: int) -> None:
+    _check(load_library().muon_adamw_get_state(_P(h), int(index), int(which), _P(dst_ptr)))
+
+
+def muon_adamw_set_state(h: int, index: int, which: int, src_ptr: int) -> None:
+    _check(load_library().muon_adamw_set_state(_P(h), int(index), int(which), _P(src_ptr)))
+
+
+def muon_adamw_get_step(h: int) -> int:
+    t = ctypes.c_int64()
+    _check(load_library().muon_adamw_get_step(_P(h), ctypes.byref(t)))
+    return t.value
+
+
+def muon_adamw_set_step(h: int, t: int) -> None:
+    _check(load_library().muon_adamw_set_step(_P(h), int(t)))
+
+
+def muon_adamw_last_norm(h: int):
+    total = ctypes.c_float()
+    coef = ctypes.c_float()
+    _check(load_library().muon_adamw_last_norm(_P(h), ctypes.byref(total), ctypes.byref(coef)))
+    return float(total.value), float(coef.value)
+
+
+def muon_adamw_plan_info(h: int) -> PlanInfo:
+    info = PlanInfo()
+    _check(load_library().muon_adamw_plan_info(_P(h), ctypes.byref(info)))
+    return info
+
+
+def muon_adamw_set_profiling(h: int, enable: bool) -> None:
+    _check(load_library().muon_adamw_set_profiling(_P(h), 1 if enable else 0))
+
+
+def muon_adamw_get_profile(h: int) -> Profile:
+    prof = Profile()
+    _check(load_library().muon_adamw_get_profile(_P(h), ctypes.byref(prof)))
+    return prof
+
+
+def muon_adamw_reset_profile(h: int) -> None:
+    _check(load_library().muon_adamw_reset_profile(_P(h)))
+
+
+def muon_adamw_destroy(h: int) -> None:
+    _check(load_library().muon_adamw_destroy(_P(h)))
+
+
+def muon_adamw_last_error() -> str:
+    return load_library().muon_adamw_last_error().decode("utf-8", "replace")
+
+
+def muon_adamw_version() -> str:
+    return load_library().muon_adamw_version().decode()
+
+
+# ---- convenience wrapper over torch tensors ----
+
+class MuonAdamW:
+    """Owns one optimizer handle; parameters and gradients are torch tensors.
+
+    ``params``: list of (name, fp32 CUDA parameter, CUDA gradient (bf16 or
+    fp32), optional bf16 shadow or None, optional group override or None).
+    Tensors must stay alive and keep their storage until ``close()``.
+    """
+
+    def __init__(self, params, *, stream=None, **config):
+        import torch
+
+        cfg = muon_adamw_config_init()
+        for k, v in config.items():
+            if k == "reserved":
+                for i, x in enumerate(v):
+                    cfg.reserved[i] = int(x)
+                continue
+            if not hasattr(cfg, k):
+                raise TypeError(f"unknown config field {k!r}")
+            setattr(cfg, k, v)
+        self.cfg = cfg
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        self.handle = muon_adamw_create(cfg, self.stream.cuda_stream)
+        self._keep = []
+        self.indices = []
+        self.groups = []
+        try:
+            for entry in params:
+                name, p, g = entry[0], entry[1], entry[2]
+                shadow = entry[3] if len(entry) > 3 else None
+                group = entry[4] if len(entry) > 4 and entry[4] is not None else MA_GROUP_AUTO
+                if p is not None and (p.dtype != torch.float32 or not p.is_contiguous()):
+                    raise TypeError(f"{name}: parameter must be a contiguous fp32 tensor")
+                if g is not None:
+                    if g.dtype not in (torch.bfloat16, torch.float32) or not g.is_contiguous():
+                        raise TypeError(f"{name}: gradient must be a contiguous bf16 or fp32 tensor")
+                    if p is not None and g.shape != p.shape:
+                        raise ValueError(f"{name}: gradient shape {tuple(g.shape)} != parameter {tuple(p.shape)}")
+                if shadow is not None and (shadow.dtype != torch.bfloat16 or not shadow.is_contiguous()):
+                    raise TypeError(f"{name}: shadow must be a contiguous bf16 tensor")
+                shape = tuple(p.shape) if p is not None else tuple(g.shape) if g is not None else ()
+                gdt = MA_DT_BF16 if (g is None or g.dtype == torch.bfloat16) else MA_DT_F32
+                idx, grp = muon_adamw_register_param(
+                    self.handle, name, shape, p.data_ptr() if p is not None else 0,
+                    g.data_ptr() if g is not None else 0, gdt,
+                    shadow.data_ptr() if shadow is not None else 0, group)
+                self._keep.append((p, g, shadow))
+                self.indices.append(idx)
+                self.groups.append(GROUP_NAMES.get(grp, grp))
+        except Exception:
+            self.close()
+            raise
+
+    def step(self, lr: float, want_norm: bool = False):
+        return muon_adamw_step(self.handle, lr, want_norm)
+
+    def state(self, index: int, which: int = 0):
+        import torch
+
+        p = self._keep[index][0]
+        out = torch.empty(p.shape, dtype=torch.float32)
+        muon_adamw_get_state(self.handle, index, which, out.data_ptr())
+        return out
+
+    def set_state(self, index: int, which: int, value) -> None:
+        import torch
+
+        src = value.detach().to(device="cpu", dtype=torch.float32).contiguous()
+        muon_adamw_set_state(self.handle, index, which, src.data_ptr())
+
+    def profile(self) -> dict:
+        prof = muon_adamw_get_profile(self.handle)
+        return {k: {"launches": int(prof.launches[i]), "ms": float(prof.ms[i]), "units": float(prof.units[i])}
+                for i, k in enumerate(KERNEL_KINDS)} | {"steps": int(prof.steps)}
+
+    def plan_info(self) -> dict:
+        info = muon_adamw_plan_info(self.handle)
+        return {f: getattr(info, f) for f, _ in PlanInfo._fields_}
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            muon_adamw_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,899 @@
+// Host runtime of the hybrid Muon + AdamW optimizer and its C ABI.
+//
+// OpenDM VLA training-stack article (gsyq.cn/news/451971), 核心揭秘一:
+//   - 参数如何分流: routing of parameters to Muon or AdamW (is_muon_param);
+//     the parameter list is frozen before the first step (the article records
+//     shapes before wrapping, which this library mirrors by freezing the plan
+//     at the first step);
+//   - 关键超参默认值: momentum 0.95 (Nesterov), 5 Newton-Schulz steps, lr scale
+//     0.2 * sqrt(max(shape));
+//   - 训练栈默认参数速查表: max_grad_norm 1.0, cosine_with_min_lr (min 0.1).
+// Everything on the device runs in the kernels of stream_kernels.cu, ns_tc.cu
+// (and the ns_simt.cu cross-check); this file plans, allocates and launches.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <map>
+#include <new>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "../../include/muon_adamw.h"
+#include "internal.h"
+
+using namespace ma;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+ma_status fail(ma_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+ma_status ok() {
+  g_last_error.clear();
+  return MA_OK;
+}
+
+#define CUDA_TRY(expr)                                                                        \
+  do {                                                                                        \
+    cudaError_t e_ = (expr);                                                                  \
+    if (e_ != cudaSuccess) {                                                                  \
+      return fail(e_ == cudaErrorMemoryAllocation ? MA_ERR_OOM : MA_ERR_CUDA, "%s: %s (%s:%d)", \
+                  #expr, cudaGetErrorString(e_), __FILE__, __LINE__);                         \
+    }                                                                                         \
+  } while (0)
+
+bool contains(const std::string& s, const char* sub) { return s.find(sub) != std::string::npos; }
+
+bool route_is_muon(const char* name, int ndim) {
+  if (!name || ndim != 2) return false;
+  const std::string n(name);
+  if (!contains(n, "action_expert")) return false;
+  bool under_layers = false;
+  size_t start = 0;
+  while (start <= n.size()) {
+    size_t dot = n.find('.', start);
+    if (dot == std::string::npos) dot = n.size();
+    if (n.compare(start, dot - start, "layers") == 0 && dot - start == 6) under_layers = true;
+    start = dot + 1;
+  }
+  if (!under_layers) return false;
+  static const char kSuffix[] = ".weight";
+  if (n.size() < sizeof(kSuffix) - 1 || n.compare(n.size() - (sizeof(kSuffix) - 1), std::string::npos, kSuffix) != 0)
+    return false;
+  std::string low(n);
+  for (char& ch : low)
+    if (ch >= 'A' && ch <= 'Z') ch = (char)(ch - 'A' + 'a');
+  if (contains(low, "embed") || contains(low, "lm_head") || contains(low, "norm")) return false;
+  return true;
+}
+
+int64_t pad_up(int64_t x, int64_t g) { return (x + g - 1) / g * g; }
+
+struct Param {
+  std::string name;
+  std::vector<int64_t> shape;
+  int64_t numel = 0;
+  float* p = nullptr;
+  const void* g = nullptr;
+  int gdtype = MA_DT_BF16;
+  uint16_t* shadow = nullptr;
+  int group = MA_GROUP_ADAMW;
+  float* st0 = nullptr;  // Muon buf or AdamW m
+  float* st1 = nullptr;  // AdamW v
+};
+
+struct Bucket {
+  int S = 0, L = 0;
+  std::vector<int> params;  // param indices in slot order
+  int mat0 = 0;             // first index in the MuonMat table
+  uint16_t *X0 = nullptr, *X1 = nullptr, *A = nullptr, *B = nullptr;
+};
+
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+  double units;
+};
+
+}  // namespace
+
+struct muon_adamw {
+  muon_adamw_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  cudaStream_t s0 = nullptr;  // caller's stream
+  cudaStream_t s1 = nullptr;  // AdamW stream (library-owned)
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  std::vector<Param> params;
+  bool planned = false;
+  int64_t t = 0;
+
+  // arena
+  void* arena = nullptr;
+  size_t arena_bytes = 0;
+  size_t state_bytes = 0, workspace_bytes = 0;
+
+  // device tables
+  GradChunk* d_norm_chunks = nullptr;
+  int n_norm_chunks = 0;
+  int norm_grid = 0;
+  float* d_norm_partials = nullptr;
+  AdamChunk* d_adam_chunks = nullptr;
+  int n_adam_chunks = 0;
+  int adam_grid = 0;
+  MuonMat* d_mats = nullptr;
+  int n_mats = 0;
+  MomTile* d_tiles = nullptr;
+  int n_tiles = 0;
+  int mom_grid = 0;
+  float* d_tile_partials = nullptr;
+  float* d_rscale = nullptr;
+  StepScalars* d_scalars = nullptr;
+  int* d_err = nullptr;
+
+  std::vector<Bucket> buckets;
+  std::vector<int> muon_params, adam_params;
+  // per iteration, per kind: launches (tcgen05) or problems (SIMT)
+  std::vector<std::vector<TcLaunch>> tc[3];
+  std::vector<std::vector<NsProblem>> simt[3];
+  double unit_gram = 0, unit_poly = 0, unit_update = 0;  // symmetric flops per iteration (all buckets)
+  double dense_flops = 0;
+  double bytes_norm = 0, bytes_mom = 0, bytes_adam = 0;
+  int64_t muon_elems = 0, adam_elems = 0, grad_elems = 0;
+
+  // profiling
+  bool profiling = false;
+  std::vector<ProfRec> prof_pending;
+  std::vector<cudaEvent_t> ev_pool;
+  ma_profile prof{};
+};
+
+namespace {
+
+cudaEvent_t take_event(muon_adamw* h) {
+  if (!h->ev_pool.empty()) {
+    cudaEvent_t e = h->ev_pool.back();
+    h->ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Launch helper: records a profiling event pair around `fn` when enabled.
+template <class F>
+void timed(muon_adamw* h, int kind, cudaStream_t st, double units, F&& fn) {
+  if (!h->profiling) {
+    fn();
+    return;
+  }
+  ProfRec r{kind, take_event(h), take_event(h), units};
+  if (r.a) cudaEventRecord(r.a, st);
+  fn();
+  if (r.b) cudaEventRecord(r.b, st);
+  if (r.a && r.b) h->prof_pending.push_back(r);
+}
+
+ma_status fold_profile(muon_adamw* h) {
+  for (const ProfRec& r : h->prof_pending) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventElapsedTime(&ms, r.a, r.b);
+    if (e != cudaSuccess) return fail(MA_ERR_CUDA, "cudaEventElapsedTime: %s", cudaGetErrorString(e));
+    h->prof.launches[r.kind] += 1;
+    h->prof.ms[r.kind] += ms;
+    h->prof.units[r.kind] += r.units;
+    h->ev_pool.push_back(r.a);
+    h->ev_pool.push_back(r.b);
+  }
+  h->prof_pending.clear();
+  return MA_OK;
+}
+
+ma_status check_device_flag(muon_adamw* h) {
+  if (!h->d_err) return MA_OK;
+  int err = 0;
+  CUDA_TRY(cudaMemcpy(&err, h->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (err != 0) {
+    cudaMemset(h->d_err, 0, sizeof(int));
+    return fail(MA_ERR_DEVICE_CHECK, "a kernel's bounded wait ran out (code 0x%x); its step was not completed", err);
+  }
+  return MA_OK;
+}
+
+ma_status build_plan(muon_adamw* h) {
+  const muon_adamw_config& c = h->cfg;
+  if (h->arena) {  // a previous attempt failed part-way
+    cudaFree(h->arena);
+    h->arena = nullptr;
+  }
+  // --- classify ---
+  h->muon_params.clear();
+  h->adam_params.clear();
+  for (int i = 0; i < (int)h->params.size(); ++i) {
+    const Param& p = h->params[i];
+    if (p.group == MA_GROUP_MUON && p.numel > 0) h->muon_params.push_back(i);
+    if (p.group == MA_GROUP_ADAMW && p.numel > 0) h->adam_params.push_back(i);
+  }
+  // --- buckets (by padded canonical shape, first-seen order) ---
+  std::map<std::pair<int, int>, int> bidx;
+  h->buckets.clear();
+  for (int pi : h->muon_params) {
+    const Param& p = h->params[pi];
+    const int64_t m = p.shape[0], n = p.shape[1];
+    const int S = (int)pad_up(std::min(m, n), kPad), L = (int)pad_up(std::max(m, n), kPad);
+    auto key = std::make_pair(S, L);
+    auto it = bidx.find(key);
+    if (it == bidx.end()) {
+      bidx[key] = (int)h->buckets.size();
+      Bucket b;
+      b.S = S;
+      b.L = L;
+      h->buckets.push_back(b);
+      it = bidx.find(key);
+    }
+    h->buckets[it->second].params.push_back(pi);
+  }
+  // --- sizes ---
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  size_t off = 0;
+  std::vector<size_t> st0_off(h->params.size(), 0), st1_off(h->params.size(), 0);
+  for (int pi : h->muon_params) {
+    st0_off[pi] = off;
+    off += al(h->params[pi].numel * sizeof(float));
+  }
+  for (int pi : h->adam_params) {
+    st0_off[pi] = off;
+    off += al(h->params[pi].numel * sizeof(float));
+    st1_off[pi] = off;
+    off += al(h->params[pi].numel * sizeof(float));
+  }
+  h->state_bytes = off;
+  std::vector<size_t> ws_off(h->buckets.size() * 4);
+  for (size_t b = 0; b < h->buckets.size(); ++b) {
+    const Bucket& B = h->buckets[b];
+    const size_t nb = B.params.size();
+    const size_t xs = al(nb * (size_t)B.S * B.L * 2), as = al(nb * (size_t)B.S * B.S * 2);
+    ws_off[4 * b + 0] = off;
+    off += xs;
+    ws_off[4 * b + 1] = off;
+    off += xs;
+    ws_off[4 * b + 2] = off;
+    off += as;
+    ws_off[4 * b + 3] = off;
+    off += as;
+  }
+  h->workspace_bytes = off - h->state_bytes;
+
+  // --- counts of the device tables ---
+  auto chunks_of = [](int64_t n) { return (size_t)((n + kChunk - 1) / kChunk); };
+  size_t n_norm = 0, n_adam = 0, n_tiles = 0, n_mats = 0;
+  for (const Param& p : h->params)
+    if (p.group != MA_GROUP_FROZEN && p.numel > 0) n_norm += chunks_of(p.numel);
+  for (int pi : h->adam_params) n_adam += chunks_of(h->params[pi].numel);
+  for (int pi : h->muon_params) {
+    const Param& p = h->params[pi];
+    n_tiles += (size_t)((p.shape[0] + kMomTile - 1) / kMomTile) * (size_t)((p.shape[1] + kMomTile - 1) / kMomTile);
+    ++n_mats;
+  }
+  h->norm_grid = (int)std::max<size_t>(1, std::min<size_t>(n_norm, (size_t)4 * h->num_sms));
+  h->adam_grid = (int)std::max<size_t>(1, std::min<size_t>(n_adam, (size_t)8 * h->num_sms));
+  h->mom_grid = (int)std::max<size_t>(1, std::min<size_t>(n_tiles, (size_t)8 * h->num_sms));
+  const size_t off_norm_chunks = off;
+  off += al(n_norm * sizeof(GradChunk));
+  const size_t off_norm_part = off;
+  off += al(h->norm_grid * sizeof(float));
+  const size_t off_adam_chunks = off;
+  off += al(n_adam * sizeof(AdamChunk));
+  const size_t off_mats = off;
+  off += al(n_mats * sizeof(MuonMat));
+  const size_t off_tiles = off;
+  off += al(n_tiles * sizeof(MomTile));
+  const size_t off_tile_part = off;
+  off += al(n_tiles * sizeof(float));
+  const size_t off_rscale = off;
+  off += al(n_mats * sizeof(float));
+  const size_t off_scalars = off;
+  off += al(sizeof(StepScalars));
+  const size_t off_err = off;
+  off += al(sizeof(int));
+  h->arena_bytes = off;
+
+  // --- allocate and zero (state starts at zero; workspace padding stays zero) ---
+  CUDA_TRY(cudaMalloc(&h->arena, h->arena_bytes));
+  CUDA_TRY(cudaMemsetAsync(h->arena, 0, h->arena_bytes, h->s0));
+  char* base = static_cast<char*>(h->arena);
+  for (int pi : h->muon_params) h->params[pi].st0 = reinterpret_cast<float*>(base + st0_off[pi]);
+  for (int pi : h->adam_params) {
+    h->params[pi].st0 = reinterpret_cast<float*>(base + st0_off[pi]);
+    h->params[pi].st1 = reinterpret_cast<float*>(base + st1_off[pi]);
+  }
+  for (size_t b = 0; b < h->buckets.size(); ++b) {
+    Bucket& B = h->buckets[b];
+    B.X0 = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 0]);
+    B.X1 = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 1]);
+    B.A = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 2]);
+    B.B = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 3]);
+  }
+  h->d_norm_chunks = reinterpret_cast<GradChunk*>(base + off_norm_chunks);
+  h->n_norm_chunks = (int)n_norm;
+  h->d_norm_partials = reinterpret_cast<float*>(base + off_norm_part);
+  h->d_adam_chunks = reinterpret_cast<AdamChunk*>(base + off_adam_chunks);
+  h->n_adam_chunks = (int)n_adam;
+  h->d_mats = reinterpret_cast<MuonMat*>(base + off_mats);
+  h->d_tiles = reinterpret_cast<MomTile*>(base + off_tiles);
+  h->d_tile_partials = reinterpret_cast<float*>(base + off_tile_part);
+  h->d_rscale = reinterpret_cast<float*>(base + off_rscale);
+  h->d_scalars = reinterpret_cast<StepScalars*>(base + off_scalars);
+  h->d_err = reinterpret_cast<int*>(base + off_err);
+
+  // --- host tables with device pointers ---
+  std::vector<GradChunk> norm_chunks;
+  std::vector<AdamChunk> adam_chunks;
+  std::vector<MuonMat> mats;
+  std::vector<MomTile> tiles;
+  norm_chunks.reserve(n_norm);
+  adam_chunks.reserve(n_adam);
+  tiles.reserve(n_tiles);
+  h->grad_elems = h->muon_elems = h->adam_elems = 0;
+  h->bytes_norm = h->bytes_mom = h->bytes_adam = 0;
+  for (size_t i = 0; i < h->params.size(); ++i) {
+    const Param& p = h->params[i];
+    if (p.group == MA_GROUP_FROZEN || p.numel == 0) continue;
+    const size_t es = p.gdtype == MA_DT_BF16 ? 2 : 4;
+    h->grad_elems += p.numel;
+    h->bytes_norm += (double)p.numel * es;
+    for (int64_t o = 0; o < p.numel; o += kChunk) {
+      GradChunk gc;
+      gc.g = static_cast<const char*>(p.g) + o * es;
+      gc.n = std::min<int64_t>(kChunk, p.numel - o);
+      gc.dtype = p.gdtype == MA_DT_BF16 ? DT_BF16 : DT_F32;
+      gc.vec = (reinterpret_cast<uintptr_t>(gc.g) % 16) == 0;
+      norm_chunks.push_back(gc);
+    }
+  }
+  for (int pi : h->adam_params) {
+    const Param& p = h->params[pi];
+    const size_t es = p.gdtype == MA_DT_BF16 ? 2 : 4;
+    h->adam_elems += p.numel;
+    h->bytes_adam += (double)p.numel * (es + 24 + (p.shadow ? 2 : 0));
+    for (int64_t o = 0; o < p.numel; o += kChunk) {
+      AdamChunk a;
+      a.p = p.p + o;
+      a.g = static_cast<const char*>(p.g) + o * es;
+      a.m = p.st0 + o;
+      a.v = p.st1 + o;
+      a.shadow = p.shadow ? p.shadow + o : nullptr;
+      a.n = std::min<int64_t>(kChunk, p.numel - o);
+      a.gdtype = p.gdtype == MA_DT_BF16 ? DT_BF16 : DT_F32;
+      const uintptr_t pa = reinterpret_cast<uintptr_t>(a.p), ga = reinterpret_cast<uintptr_t>(a.g),
+                      sa = reinterpret_cast<uintptr_t>(a.shadow);
+      a.vec = (pa % 16 == 0) && (ga % (a.gdtype == DT_BF16 ? 8 : 16) == 0) && (sa % 8 == 0);
+      adam_chunks.push_back(a);
+    }
+  }
+  int mat_index = 0;
+  h->unit_gram = h->unit_poly = h->unit_update = h->dense_flops = 0;
+  for (size_t b = 0; b < h->buckets.size(); ++b) {
+    Bucket& B = h->buckets[b];
+    B.mat0 = mat_index;
+    for (size_t slot = 0; slot < B.params.size(); ++slot) {
+      const Param& p = h->params[B.params[slot]];
+      const size_t es = p.gdtype == MA_DT_BF16 ? 2 : 4;
+      MuonMat M{};
+      M.p = p.p;
+      M.g = p.g;
+      M.buf = p.st0;
+      M.shadow = p.shadow;
+      M.x0 = B.X0 + slot * (size_t)B.S * B.L;
+      M.m = (int)p.shape[0];
+      M.n = (int)p.shape[1];
+      M.s = std::min(M.m, M.n);
+      M.l = std::max(M.m, M.n);
+      M.S = B.S;
+      M.L = B.L;
+      M.transposed = M.m > M.n;
+      M.gdtype = p.gdtype == MA_DT_BF16 ? DT_BF16 : DT_F32;
+      M.vec = (M.n % 8 == 0) && (reinterpret_cast<uintptr_t>(p.g) % 16 == 0);
+      M.lr_mult = (float)((double)c.muon_lr_scale * c.moonlight_coef * sqrt((double)M.l));
+      M.tile_begin = (int)tiles.size();
+      for (int r0 = 0; r0 < M.m; r0 += kMomTile)
+        for (int c0 = 0; c0 < M.n; c0 += kMomTile) tiles.push_back(MomTile{mat_index, r0, c0, 0});
+      M.tile_end = (int)tiles.size();
+      mats.push_back(M);
+      ++mat_index;
+      const double s = M.s, l = M.l;
+      h->muon_elems += p.numel;
+      h->bytes_mom += (double)p.numel * (es + 8 + 2);
+      h->unit_gram += s * (s + 1) * l;
+      h->unit_poly += s * (s + 1) * s;
+      h->unit_update += 2 * s * s * l;
+      h->dense_flops += (double)c.ns_steps * (4 * s * s * l + 2 * s * s * s);
+    }
+  }
+  h->n_mats = mat_index;
+  h->n_tiles = (int)tiles.size();
+  if (!norm_chunks.empty())
+    CUDA_TRY(cudaMemcpyAsync(h->d_norm_chunks, norm_chunks.data(), norm_chunks.size() * sizeof(GradChunk),
+                             cudaMemcpyHostToDevice, h->s0));
+  if (!adam_chunks.empty())
+    CUDA_TRY(cudaMemcpyAsync(h->d_adam_chunks, adam_chunks.data(), adam_chunks.size() * sizeof(AdamChunk),
+                             cudaMemcpyHostToDevice, h->s0));
+  if (!mats.empty())
+    CUDA_TRY(cudaMemcpyAsync(h->d_mats, mats.data(), mats.size() * sizeof(MuonMat), cudaMemcpyHostToDevice, h->s0));
+  if (!tiles.empty())
+    CUDA_TRY(cudaMemcpyAsync(h->d_tiles, tiles.data(), tiles.size() * sizeof(MomTile), cudaMemcpyHostToDevice, h->s0));
+  CUDA_TRY(cudaStreamSynchronize(h->s0));
+
+  // --- Newton-Schulz launch descriptions ---
+  const int steps = c.ns_steps;
+  for (int k = 0; k < 3; ++k) {
+    h->tc[k].assign(steps, {});
+    h->simt[k].assign(steps, {});
+  }
+  for (int it = 0; it < steps; ++it) {
+    for (int kind = 0; kind < 3; ++kind) {
+      std::vector<NsProblem> probs;
+      for (Bucket& B : h->buckets) {
+        uint16_t* Xcur = (it % 2 == 0) ? B.X0 : B.X1;
+        uint16_t* Xnext = (it % 2 == 0) ? B.X1 : B.X0;
+        NsProblem p{};
+        p.kind = kind;
+        p.S = B.S;
+        p.L = B.L;
+        p.nmat = (int)B.params.size();
+        p.mats = h->d_mats + B.mat0;
+        p.rscale = h->d_rscale + B.mat0;
+        p.first = it == 0;
+        p.last = it == steps - 1;
+        if (kind == NS_GRAM) {
+          p.P = Xcur;
+          p.Q = Xcur;
+          p.aux = nullptr;
+          p.out = B.A;
+          p.M = B.S;
+          p.N = B.S;
+          p.K = B.L;
+        } else if (kind == NS_POLY) {
+          p.P = B.A;
+          p.Q = B.A;
+          p.aux = B.A;
+          p.out = B.B;
+          p.M = B.S;
+          p.N = B.S;
+          p.K = B.S;
+        } else {
+          p.P = B.B;
+          p.Q = Xcur;
+          p.aux = Xcur;
+          p.out = Xnext;
+          p.M = B.S;
+          p.N = B.L;
+          p.K = B.S;
+        }
+        probs.push_back(p);
+      }
+      h->simt[kind][it] = probs;
+      if (c.ns_kernel == MA_NS_TCGEN05) {
+        for (size_t b0 = 0; b0 < probs.size(); b0 += kTcMaxProblems) {
+          TcLaunch L;
+          memset(&L, 0, sizeof L);
+          int tiles_total = 0;
+          for (size_t q = 0; q < (size_t)kTcMaxProblems && b0 + q < probs.size(); ++q) {
+            TcProblem& tp = L.prob[q];
+            tp.p = probs[b0 + q];
+            char eb[256];
+            if (!tc_encode_problem(tp, eb, sizeof eb)) return fail(MA_ERR_CUDA, "%s", eb);
+            tp.tile_begin = tiles_total;
+            tiles_total += tp.tiles_per_mat * tp.p.nmat;
+            L.nprob = (int)q + 1;
+          }
+          L.total_tiles = tiles_total;
+          L.err = h->d_err;
+          L.mn_swap = (c.reserved[0] & 1) ? 1 : 0;
+          h->tc[kind][it].push_back(L);
+        }
+      }
+    }
+  }
+  if (c.ns_kernel == MA_NS_TCGEN05 && !h->buckets.empty()) CUDA_TRY(ns_tc_prepare());
+  h->planned = true;
+  return MA_OK;
+}
+
+void set_epi(NsEpiArgs& e, const muon_adamw_config& c, float lr) {
+  e.a = c.ns_a;
+  e.b = c.ns_b;
+  e.c = c.ns_c;
+  e.decay = (float)(1.0 - (double)lr * c.muon_weight_decay);
+  e.lr = lr;
+}
+
+ma_status valid_config(const muon_adamw_config* c) {
+  if (c->mode != MA_MODE_MUON_ADAMW && c->mode != MA_MODE_ADAMW_ONLY) return fail(MA_ERR_ARG, "bad mode %d", c->mode);
+  if (c->precision != MA_BF16_MIXED && c->precision != MA_FP32_MIXED)
+    return fail(MA_ERR_ARG, "bad precision %d", c->precision);
+  if (c->ns_steps < 1 || c->ns_steps > 64) return fail(MA_ERR_ARG, "ns_steps must be in [1, 64]");
+  if (c->ns_kernel != MA_NS_TCGEN05 && c->ns_kernel != MA_NS_SIMT) return fail(MA_ERR_ARG, "bad ns_kernel");
+  if (!(c->adam_beta1 >= 0.f && c->adam_beta1 < 1.f) || !(c->adam_beta2 >= 0.f && c->adam_beta2 < 1.f))
+    return fail(MA_ERR_ARG, "betas must lie in [0, 1)");
+  if (!(c->adam_eps >= 0.f) || !(c->ns_eps >= 0.f) || !(c->clip_eps >= 0.f)) return fail(MA_ERR_ARG, "eps < 0");
+  if (!isfinite(c->muon_momentum) || !isfinite(c->max_grad_norm) || !isfinite(c->muon_lr_scale) ||
+      !isfinite(c->moonlight_coef) || !isfinite(c->ns_a) || !isfinite(c->ns_b) || !isfinite(c->ns_c))
+    return fail(MA_ERR_ARG, "non-finite config value");
+  return MA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void muon_adamw_config_init(muon_adamw_config* cfg) {
+  if (!cfg) return;
+  memset(cfg, 0, sizeof *cfg);
+  cfg->mode = MA_MODE_MUON_ADAMW;
+  cfg->precision = MA_BF16_MIXED;
+  cfg->muon_momentum = 0.95f;
+  cfg->muon_nesterov = 1;
+  cfg->ns_steps = 5;
+  cfg->ns_a = 3.4445f;
+  cfg->ns_b = -4.7750f;
+  cfg->ns_c = 2.0315f;
+  cfg->ns_eps = 1e-7f;
+  cfg->moonlight_coef = 0.2f;
+  cfg->muon_lr_scale = 1.0f;
+  cfg->muon_weight_decay = 0.1f;
+  cfg->adam_beta1 = 0.9f;
+  cfg->adam_beta2 = 0.999f;
+  cfg->adam_eps = 1e-8f;
+  cfg->adam_weight_decay = 0.1f;
+  cfg->max_grad_norm = 1.0f;
+  cfg->clip_eps = 1e-6f;
+  cfg->ns_kernel = MA_NS_TCGEN05;
+}
+
+int muon_adamw_is_muon_param(const char* name, int ndim) { return route_is_muon(name, ndim) ? 1 : 0; }
+
+double muon_adamw_cosine_with_min_lr(int64_t step, int64_t total, int64_t warmup, double min_lr_rate) {
+  if (step < warmup) return (double)step / (double)std::max<int64_t>(1, warmup);
+  const double progress = (double)(step - warmup) / (double)std::max<int64_t>(1, total - warmup);
+  const double cosine = 0.5 * (1.0 + cos(M_PI * progress));
+  const double f = cosine * (1.0 - min_lr_rate) + min_lr_rate;
+  return f > 0.0 ? f : 0.0;
+}
+
+const char* muon_adamw_last_error(void) { return g_last_error.c_str(); }
+
+const char* muon_adamw_version(void) { return "0.1.0 sm_103a"; }
+
+ma_status muon_adamw_create(const muon_adamw_config* cfg, void* cuda_stream, muon_adamw_t** out) {
+  if (!cfg || !out) return fail(MA_ERR_ARG, "cfg and out must not be NULL");
+  *out = nullptr;
+  ma_status st = valid_config(cfg);
+  if (st != MA_OK) return st;
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  CUDA_TRY(cudaGetDeviceProperties(&prop, dev));
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(MA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev, prop.major,
+                prop.minor);
+  muon_adamw* h = new (std::nothrow) muon_adamw();
+  if (!h) return fail(MA_ERR_OOM, "host allocation failed");
+  h->cfg = *cfg;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  h->s0 = static_cast<cudaStream_t>(cuda_stream);
+  cudaError_t e = cudaStreamCreateWithFlags(&h->s1, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    muon_adamw_destroy(h);
+    return fail(MA_ERR_CUDA, "stream/event creation failed: %s", cudaGetErrorString(e));
+  }
+  *out = h;
+  return ok();
+}
+
+ma_status muon_adamw_register_param(muon_adamw_t* h, const char* name, int ndim, const int64_t* shape,
+                                    float* param_fp32, const void* grad, int grad_dtype, void* param_bf16_shadow,
+                                    int group_override, int* assigned, int* index_out) {
+  if (!h || !name) return fail(MA_ERR_ARG, "handle and name must not be NULL");
+  if (h->planned) return fail(MA_ERR_STATE, "register_param after the first step (plan is frozen)");
+  if (ndim < 0 || ndim > 8) return fail(MA_ERR_SHAPE, "ndim %d outside [0, 8]", ndim);
+  if (ndim > 0 && !shape) return fail(MA_ERR_ARG, "shape must not be NULL for ndim > 0");
+  Param p;
+  p.name = name;
+  p.numel = 1;
+  for (int d = 0; d < ndim; ++d) {
+    if (shape[d] < 0) return fail(MA_ERR_SHAPE, "negative size in dim %d", d);
+    if (shape[d] > ((int64_t)1 << 40)) return fail(MA_ERR_SHAPE, "size too large in dim %d", d);
+    p.shape.push_back(shape[d]);
+    p.numel *= shape[d];
+  }
+  int group;
+  switch (group_override) {
+    case MA_GROUP_AUTO:
+      group = (h->cfg.mode == MA_MODE_MUON_ADAMW && route_is_muon(name, ndim)) ? MA_GROUP_MUON : MA_GROUP_ADAMW;
+      break;
+    case MA_GROUP_MUON:
+    case MA_GROUP_ADAMW:
+    case MA_GROUP_FROZEN:
+      group = group_override;
+      break;
+    default:
+      return fail(MA_ERR_ARG, "bad group override %d", group_override);
+  }
+  if (group == MA_GROUP_MUON) {
+    if (ndim != 2) return fail(MA_ERR_SHAPE, "Muon parameters must be 2-D (got ndim %d)", ndim);
+    if (p.shape[0] >= ((int64_t)1 << 30) || p.shape[1] >= ((int64_t)1 << 30))
+      return fail(MA_ERR_SHAPE, "Muon matrix dimension too large");
+  }
+  if (group != MA_GROUP_FROZEN) {
+    if (!param_fp32 || !grad) return fail(MA_ERR_ARG, "param and grad must not be NULL for trainable '%s'", name);
+    if (grad_dtype != MA_DT_F32 && grad_dtype != MA_DT_BF16) return fail(MA_ERR_DTYPE, "bad grad dtype %d", grad_dtype);
+    if (reinterpret_cast<uintptr_t>(param_fp32) % 4) return fail(MA_ERR_ALIGN, "param not 4-byte aligned");
+    if (reinterpret_cast<uintptr_t>(grad) % (grad_dtype == MA_DT_BF16 ? 2 : 4))
+      return fail(MA_ERR_ALIGN, "grad not aligned to its element size");
+    if (reinterpret_cast<uintptr_t>(param_bf16_shadow) % 2) return fail(MA_ERR_ALIGN, "shadow not 2-byte aligned");
+  }
+  p.p = param_fp32;
+  p.g = grad;
+  p.gdtype = grad_dtype;
+  p.shadow = (h->cfg.precision == MA_BF16_MIXED) ? static_cast<uint16_t*>(param_bf16_shadow) : nullptr;
+  p.group = group;
+  h->params.push_back(p);
+  if (assigned) *assigned = group;
+  if (index_out) *index_out = (int)h->params.size() - 1;
+  return ok();
+}
+
+ma_status muon_adamw_step(muon_adamw_t* h, float lr, float* grad_norm_out) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  if (!isfinite(lr)) return fail(MA_ERR_ARG, "lr is not finite");
+  CUDA_TRY(cudaSetDevice(h->device));
+  if (!h->planned) {
+    ma_status st = build_plan(h);
+    if (st != MA_OK) return st;
+  }
+  const muon_adamw_config& c = h->cfg;
+  h->t += 1;
+  const double t = (double)h->t;
+
+  if (h->n_norm_chunks > 0) {
+    timed(h, MA_K_GRAD_NORM, h->s0, h->bytes_norm,
+          [&] { launch_grad_sumsq(h->d_norm_chunks, h->n_norm_chunks, h->d_norm_partials, h->norm_grid, h->s0); });
+  } else {
+    CUDA_TRY(cudaMemsetAsync(h->d_norm_partials, 0, sizeof(float), h->s0));
+  }
+  timed(h, MA_K_CLIP, h->s0, (double)h->norm_grid * 4, [&] {
+    launch_clip_finalize(h->d_norm_partials, h->n_norm_chunks > 0 ? h->norm_grid : 1, c.max_grad_norm, c.clip_eps,
+                         h->d_scalars, h->s0);
+  });
+
+  const bool have_adam = h->n_adam_chunks > 0;
+  if (have_adam) {
+    CUDA_TRY(cudaEventRecord(h->ev_fork, h->s0));
+    CUDA_TRY(cudaStreamWaitEvent(h->s1, h->ev_fork, 0));
+    AdamArgs a;
+    a.beta1 = c.adam_beta1;
+    a.beta2 = c.adam_beta2;
+    a.omb1 = (float)(1.0 - (double)c.adam_beta1);
+    a.omb2 = (float)(1.0 - (double)c.adam_beta2);
+    a.eps = c.adam_eps;
+    a.decay = (float)(1.0 - (double)lr * c.adam_weight_decay);
+    const double bc1 = 1.0 - pow((double)c.adam_beta1, t), bc2 = 1.0 - pow((double)c.adam_beta2, t);
+    a.step_size = (float)((double)lr / bc1);
+    a.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
+    timed(h, MA_K_ADAMW, h->s1, h->bytes_adam,
+          [&] { launch_adamw(h->d_adam_chunks, h->n_adam_chunks, h->d_scalars, a, h->adam_grid, h->s1); });
+  }
+
+  if (h->n_mats > 0) {
+    MomArgs ma_{c.muon_momentum, c.muon_nesterov};
+    timed(h, MA_K_MOMENTUM, h->s0, h->bytes_mom, [&] {
+      launch_muon_momentum(h->d_tiles, h->n_tiles, h->d_mats, h->d_scalars, ma_, h->d_tile_partials, h->mom_grid,
+                           h->s0);
+    });
+    timed(h, MA_K_NS_PREP, h->s0, (double)h->n_tiles * 4,
+          [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, c.ns_eps, h->d_rscale, h->s0); });
+    NsEpiArgs epi;
+    set_epi(epi, c, lr);
+    const double units[3] = {h->unit_gram, h->unit_poly, h->unit_update};
+    for (int it = 0; it < c.ns_steps; ++it) {
+      for (int kind = 0; kind < 3; ++kind) {
+        if (c.ns_kernel == MA_NS_TCGEN05) {
+          for (TcLaunch& L : h->tc[kind][it]) {
+            L.epi = epi;
+            timed(h, MA_K_NS_GRAM + kind, h->s0, units[kind] / h->tc[kind][it].size(),
+                  [&] { launch_ns_tc(L, h->num_sms, h->s0); });
+          }
+        } else {
+          timed(h, MA_K_NS_GRAM + kind, h->s0, units[kind], [&] {
+            for (const NsProblem& p : h->simt[kind][it]) launch_ns_simt(p, epi, h->s0);
+          });
+        }
+      }
+    }
+  }
+  if (have_adam) {
+    CUDA_TRY(cudaEventRecord(h->ev_join, h->s1));
+    CUDA_TRY(cudaStreamWaitEvent(h->s0, h->ev_join, 0));
+  }
+  CUDA_TRY(cudaGetLastError());
+  if (h->profiling) h->prof.steps += 1;
+  if (grad_norm_out) {
+    StepScalars sc;
+    CUDA_TRY(cudaMemcpyAsync(&sc, h->d_scalars, sizeof sc, cudaMemcpyDeviceToHost, h->s0));
+    CUDA_TRY(cudaStreamSynchronize(h->s0));
+    *grad_norm_out = sc.total;
+    ma_status st = check_device_flag(h);
+    if (st != MA_OK) return st;
+  }
+  return ok();
+}
+
+ma_status muon_adamw_sync(muon_adamw_t* h) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  CUDA_TRY(cudaSetDevice(h->device));
+  CUDA_TRY(cudaStreamSynchronize(h->s0));
+  ma_status st = check_device_flag(h);
+  if (st != MA_OK) return st;
+  return ok();
+}
+
+static ma_status state_ptr(muon_adamw_t* h, int index, int which, float** ptr, int64_t* n) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  if (index < 0 || index >= (int)h->params.size()) return fail(MA_ERR_ARG, "bad parameter index %d", index);
+  const Param& p = h->params[index];
+  if (p.group == MA_GROUP_FROZEN) return fail(MA_ERR_STATE, "parameter %d is frozen: no state", index);
+  if (which == 0) {
+    *ptr = p.st0;
+  } else if (which == 1) {
+    if (p.group != MA_GROUP_ADAMW) return fail(MA_ERR_ARG, "which=1 (second moment) exists only for AdamW");
+    *ptr = p.st1;
+  } else {
+    return fail(MA_ERR_ARG, "bad which %d", which);
+  }
+  *n = p.numel;
+  return MA_OK;
+}
+
+ma_status muon_adamw_get_state(muon_adamw_t* h, int index, int which, float* dst_host) {
+  if (!dst_host) return fail(MA_ERR_ARG, "dst must not be NULL");
+  if (h && !h->planned) return fail(MA_ERR_STATE, "no state before the first step");
+  float* src = nullptr;
+  int64_t n = 0;
+  ma_status st = state_ptr(h, index, which, &src, &n);
+  if (st != MA_OK) return st;
+  CUDA_TRY(cudaSetDevice(h->device));
+  CUDA_TRY(cudaStreamSynchronize(h->s0));
+  if (n > 0) CUDA_TRY(cudaMemcpy(dst_host, src, n * sizeof(float), cudaMemcpyDeviceToHost));
+  return ok();
+}
+
+ma_status muon_adamw_set_state(muon_adamw_t* h, int index, int which, const float* src_host) {
+  if (!h || !src_host) return fail(MA_ERR_ARG, "handle and src must not be NULL");
+  CUDA_TRY(cudaSetDevice(h->device));
+  if (!h->planned) {
+    ma_status st = build_plan(h);
+    if (st != MA_OK) return st;
+  }
+  float* dst = nullptr;
+  int64_t n = 0;
+  ma_status st = state_ptr(h, index, which, &dst, &n);
+  if (st != MA_OK) return st;
+  CUDA_TRY(cudaStreamSynchronize(h->s0));
+  if (n > 0) CUDA_TRY(cudaMemcpy(dst, src_host, n * sizeof(float), cudaMemcpyHostToDevice));
+  return ok();
+}
+
+ma_status muon_adamw_get_step(muon_adamw_t* h, int64_t* t_out) {
+  if (!h || !t_out) return fail(MA_ERR_ARG, "NULL argument");
+  *t_out = h->t;
+  return ok();
+}
+
+ma_status muon_adamw_set_step(muon_adamw_t* h, int64_t t) {
+  if (!h || t < 0) return fail(MA_ERR_ARG, "NULL handle or negative step");
+  h->t = t;
+  return ok();
+}
+
+ma_status muon_adamw_last_norm(muon_adamw_t* h, float* total_out, float* coef_out) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  if (!h->planned) return fail(MA_ERR_STATE, "no step taken yet");
+  CUDA_TRY(cudaSetDevice(h->device));
+  StepScalars sc;
+  CUDA_TRY(cudaMemcpyAsync(&sc, h->d_scalars, sizeof sc, cudaMemcpyDeviceToHost, h->s0));
+  CUDA_TRY(cudaStreamSynchronize(h->s0));
+  if (total_out) *total_out = sc.total;
+  if (coef_out) *coef_out = sc.coef;
+  return ok();
+}
+
+ma_status muon_adamw_plan_info(muon_adamw_t* h, ma_plan_info* out) {
+  if (!h || !out) return fail(MA_ERR_ARG, "NULL argument");
+  if (!h->planned) return fail(MA_ERR_STATE, "plan is built by the first step");
+  memset(out, 0, sizeof *out);
+  out->n_params = (int)h->params.size();
+  for (const Param& p : h->params) {
+    if (p.group == MA_GROUP_MUON) out->n_muon++;
+    if (p.group == MA_GROUP_ADAMW) out->n_adamw++;
+    if (p.group == MA_GROUP_FROZEN) out->n_frozen++;
+  }
+  out->n_buckets = (int)h->buckets.size();
+  out->muon_elems = h->muon_elems;
+  out->adamw_elems = h->adam_elems;
+  out->grad_elems = h->grad_elems;
+  out->state_bytes = (int64_t)h->state_bytes;
+  out->workspace_bytes = (int64_t)h->workspace_bytes;
+  out->ns_flops_per_step = h->cfg.ns_steps * (h->unit_gram + h->unit_poly + h->unit_update);
+  out->ns_dense_flops_per_step = h->dense_flops;
+  out->stream_bytes_per_step = h->bytes_norm + h->bytes_mom + h->bytes_adam;
+  return ok();
+}
+
+ma_status muon_adamw_set_profiling(muon_adamw_t* h, int enable) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  h->profiling = enable != 0;
+  return ok();
+}
+
+ma_status muon_adamw_get_profile(muon_adamw_t* h, ma_profile* out) {
+  if (!h || !out) return fail(MA_ERR_ARG, "NULL argument");
+  CUDA_TRY(cudaSetDevice(h->device));
+  CUDA_TRY(cudaStreamSynchronize(h->s0));
+  CUDA_TRY(cudaStreamSynchronize(h->s1));
+  ma_status st = fold_profile(h);
+  if (st != MA_OK) return st;
+  *out = h->prof;
+  return ok();
+}
+
+ma_status muon_adamw_reset_profile(muon_adamw_t* h) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  CUDA_TRY(cudaSetDevice(h->device));
+  CUDA_TRY(cudaStreamSynchronize(h->s0));
+  CUDA_TRY(cudaStreamSynchronize(h->s1));
+  ma_status st = fold_profile(h);
+  if (st != MA_OK) return st;
+  memset(&h->prof, 0, sizeof h->prof);
+  return ok();
+}
+
+ma_status muon_adamw_destroy(muon_adamw_t* h) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  cudaSetDevice(h->device);
+  if (h->s0 || h->s1) {
+    cudaStreamSynchronize(h->s0);
+    if (h->s1) cudaStreamSynchronize(h->s1);
+  }
+  for (const ProfRec& r : h->prof_pending) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
+  if (h->arena) cudaFree(h->arena);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->s1) cudaStreamDestroy(h->s1);
+  delete h;
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,149 @@
+// Internal types shared by the host runtime (capi.cu) and the kernels.
+// Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ma {
+
+// Elements per multi-tensor chunk of the gradient-norm and AdamW streams.
+constexpr int64_t kChunk = 1 << 16;
+// Edge of the square tiles the Muon momentum kernel walks.
+constexpr int kMomTile = 64;
+// Padding granule of the canonical Newton-Schulz workspaces (rows and cols).
+constexpr int kPad = 128;
+
+enum GradDtype : int32_t { DT_F32 = 0, DT_BF16 = 1 };
+
+struct GradChunk {      // one slice of one gradient
+  const void* g;
+  int64_t n;
+  int32_t dtype;
+  int32_t vec;          // 1 if g is 16-byte aligned (vector loads allowed)
+};
+
+struct AdamChunk {      // one slice of one AdamW parameter
+  float* p;
+  const void* g;
+  float* m;
+  float* v;
+  uint16_t* shadow;     // bf16 copy or nullptr
+  int64_t n;
+  int32_t gdtype;
+  int32_t vec;          // 1 if every pointer allows 4-wide vector access
+};
+
+struct MuonMat {        // one Muon matrix (device-visible metadata)
+  float* p;             // fp32 master [m][n]
+  const void* g;        // gradient [m][n]
+  float* buf;           // momentum [m][n]
+  uint16_t* shadow;     // bf16 [m][n] or nullptr
+  uint16_t* x0;         // canonical bf16 X of this matrix, [S][L], row stride L
+  int32_t m, n;         // parameter shape
+  int32_t s, l;         // canonical shape: s = min(m,n), l = max(m,n)
+  int32_t S, L;         // padded canonical shape (multiples of kPad)
+  int32_t transposed;   // 1 if m > n (X = update^T)
+  int32_t gdtype;
+  int32_t vec;          // rows of g/buf allow 16-byte vector access
+  int32_t tile_begin;   // momentum tiles [tile_begin, tile_end) in the tile list
+  int32_t tile_end;
+  float lr_mult;        // muon_lr_scale * moonlight * sqrt(max(m, n))
+};
+
+struct MomTile {
+  int32_t mat;
+  int32_t r0, c0;       // tile origin in the parameter (row, col)
+  int32_t pad;
+};
+
+struct StepScalars {    // written on the device each step
+  float total;          // global gradient norm
+  float coef;           // clip coefficient
+  float pad0, pad1;
+};
+
+struct AdamArgs {
+  float beta1, beta2, omb1, omb2, eps;
+  float decay;          // 1 - lr * wd
+  float step_size;      // lr / (1 - beta1^t)
+  float inv_sqrt_bc2;   // 1 / sqrt(1 - beta2^t)
+};
+
+struct MomArgs {
+  float mu;
+  int32_t nesterov;
+};
+
+enum NsKind : int32_t { NS_GRAM = 0, NS_POLY = 1, NS_UPDATE = 2 };
+
+struct NsEpiArgs {
+  float a, b, c;
+  float decay;          // 1 - lr * muon_wd
+  float lr;
+};
+
+// One grouped GEMM problem: all same-shape matrices of one bucket.
+//   GRAM:   out[S][S] = X X^T          (P = Q = X, K = L)      symmetric
+//   POLY:   out[S][S] = b A + c A A    (P = Q = A, K = S)      symmetric
+//   UPDATE: out[S][L] = a X + B X      (P = B, Q = X MN-major, K = S)
+struct NsProblem {
+  const uint16_t* P;
+  const uint16_t* Q;
+  const uint16_t* aux;  // POLY: A; UPDATE: X
+  uint16_t* out;
+  const MuonMat* mats;  // this bucket's matrices
+  const float* rscale;  // per matrix 1 / (||update||_F + eps), same indexing
+  int32_t kind;
+  int32_t S, L;
+  int32_t M, N, K;
+  int32_t nmat;
+  int32_t first, last;  // first / last Newton-Schulz iteration
+};
+
+// ---- launchers (stream_kernels.cu) ----
+void launch_grad_sumsq(const GradChunk* chunks, int nchunks, float* partials, int grid, cudaStream_t st);
+void launch_clip_finalize(const float* partials, int n, float max_norm, float clip_eps, StepScalars* out,
+                          cudaStream_t st);
+void launch_muon_momentum(const MomTile* tiles, int ntiles, const MuonMat* mats, const StepScalars* sc,
+                          MomArgs args, float* tile_partials, int grid, cudaStream_t st);
+void launch_ns_prep(const MuonMat* mats, int nmat, const float* tile_partials, float eps, float* rscale,
+                    cudaStream_t st);
+void launch_adamw(const AdamChunk* chunks, int nchunks, const StepScalars* sc, AdamArgs args, int grid,
+                  cudaStream_t st);
+
+// ---- Newton-Schulz GEMMs ----
+// CUDA-core cross-check kernel (ns_simt.cu)
+void launch_ns_simt(const NsProblem& prob, NsEpiArgs epi, cudaStream_t st);
+
+// tcgen05 / TMEM / TMA kernel (ns_tc.cu)
+constexpr int kTcMaxProblems = 4;
+struct TcProblem {
+  CUtensorMap tmP;      // K-major loads of P, box {64, 128}
+  CUtensorMap tmQ;      // GRAM/POLY: K-major box {64, 128}; UPDATE: MN-major box {64, 64}
+  NsProblem p;
+  int32_t bn;           // N tile: 128 or 256
+  int32_t tiles_m;      // M / 128
+  int32_t tiles_n;      // N / bn
+  int32_t tiles_per_mat;
+  int32_t tile_begin;   // first global tile index of this problem
+  int32_t pad[3];
+};
+struct TcLaunch {
+  TcProblem prob[kTcMaxProblems];
+  int32_t nprob;
+  int32_t total_tiles;
+  NsEpiArgs epi;
+  int* err;             // device error flag
+  int32_t mn_swap;      // cross-check knob: exchange LBO/SBO of the MN-major descriptor
+  int32_t pad;
+};
+// Encode the tensor maps of `tp` (host; uses the driver entry point).
+bool tc_encode_problem(TcProblem& tp, char* errbuf, size_t errlen);
+cudaError_t ns_tc_prepare();  // sets the kernel's dynamic shared-memory limit (current device)
+void launch_ns_tc(const TcLaunch& L, int grid, cudaStream_t st);
+size_t ns_tc_smem_bytes();
+int ns_tc_num_tiles_sym(int tiles_m, int bn);  // lower-triangle tile count per matrix
+
+}  // namespace ma

@@ -1,0 +1,488 @@
+// Newton-Schulz grouped GEMMs on the 5th-generation tensor cores (sm_103a).
+//
+// Newton-Schulz orthogonalisation as described in the OpenDM article
+// (核心揭秘一 / Muon 的工作原理): A = X X^T, B = b A + c A A, X <- a X + B X,
+// five times, on the short side. Each launch covers one of the three
+// products for every Muon matrix of up to four shape buckets.
+//
+// Structure (one persistent CTA per SM, 192 threads):
+//   warp 0     TMA producer: 128x64 tiles of the left operand and bn x 64
+//              tiles of the right operand into a 4-stage shared-memory ring
+//              (128-byte swizzle), completion tracked by mbarrier tx counts;
+//   warp 1     allocates 512 TMEM columns; one lane issues
+//              tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32,
+//              M = 128, N = bn, K = 16) and commits stage releases and
+//              accumulator-ready signals to mbarriers;
+//   warps 2-5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane
+//              quarter each), the fused polynomial epilogue, bf16 stores.
+// Two accumulators (2 x 256 columns) let the epilogue of one tile overlap
+// the main loop of the next. X X^T and A A are symmetric: only output tiles
+// that touch the lower triangle are computed and the epilogue mirrors them.
+//
+// Every mbarrier wait is bounded (kWaitLimitNs of wall time). On expiry the
+// CTA records an error code in the device flag, the other roles stop at
+// their next wait, in-flight copies and MMAs are drained (again bounded)
+// and TMEM is released before the CTA exits.
+#include <cuda.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "internal.h"
+#include "ns_epilogue.cuh"
+
+namespace ma {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int BN_MAX = 256;
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;      // 16 KB
+constexpr int B_STAGE = BN_MAX * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int EPI_WARPS = 4;
+constexpr int THREADS = 64 + EPI_WARPS * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+// error codes written to the device flag
+constexpr int kErrWaitProducer = 0x101;
+constexpr int kErrWaitMma = 0x102;
+constexpr int kErrWaitEpilogue = 0x103;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase of parity `parity` of `bar` has completed. Returns
+// false if the CTA is aborting or the wait ran past the limit (then the
+// abort flag and the device error code are set).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                       int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicCAS(err, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle, descriptor version 1.
+//   K-major: rows of 64 bf16 (128 B); 8-row groups 1024 B apart (SBO).
+//   MN-major: rows = K index, 64 MN-elements per 128 B row; 8-row groups
+//   1024 B apart (SBO); 64-element MN panels `panel_bytes` apart (LBO).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulate, bf16 A and B,
+// A K-major, B K-major or MN-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_bf16(int n, bool b_mn_major) {
+  uint32_t d = 0;
+  d |= 1u << 4;   // D format: f32
+  d |= 1u << 7;   // A format: bf16
+  d |= 1u << 10;  // B format: bf16
+  if (b_mn_major) d |= 1u << 16;
+  d |= (uint32_t)(n >> 3) << 17;
+  d |= (uint32_t)(BM >> 4) << 24;
+  return d;
+}
+
+struct TileCoord {
+  int prob, mat, ti, tj;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const TcLaunch& L, int g) {
+  TileCoord c{0, 0, 0, 0};
+  int pi = 0;
+  while (pi + 1 < L.nprob && g >= L.prob[pi + 1].tile_begin) ++pi;
+  const TcProblem& P = L.prob[pi];
+  const int local = g - P.tile_begin;
+  c.prob = pi;
+  c.mat = local / P.tiles_per_mat;
+  int t = local - c.mat * P.tiles_per_mat;
+  if (P.p.kind == NS_UPDATE) {
+    c.ti = t / P.tiles_n;
+    c.tj = t - c.ti * P.tiles_n;
+  } else {
+    // row block ti holds the tiles whose columns start at or before its last row
+    int ti = 0;
+    for (;;) {
+      const int cnt = (ti * BM + BM - 1) / P.bn + 1;
+      if (t < cnt) break;
+      t -= cnt;
+      ++ti;
+    }
+    c.ti = ti;
+    c.tj = t;
+  }
+  return c;
+}
+
+__global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant__ TcLaunch L) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * STAGE_BYTES);
+  // bars[0..S): full, [S..2S): empty, [2S..2S+2): tmem full, [2S+2..2S+4): tmem empty, [2S+4]: drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + STAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * STAGES);
+  const uint32_t tempty0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, EPI_WARPS * 32);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      for (int p = 0; p < L.nprob; ++p) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L.prob[p].tmP)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L.prob[p].tmQ)) : "memory");
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int g = blockIdx.x; g < L.total_tiles && ok; g += gridDim.x) {
+        const TileCoord c = decode_tile(L, g);
+        const TcProblem& P = L.prob[c.prob];
+        const int kblocks = P.p.K / BK;
+        const int rowP = c.mat * P.p.M + c.ti * BM;
+        const bool sym = P.p.kind != NS_UPDATE;
+        const uint32_t tx = (uint32_t)(A_STAGE + P.bn * BK * 2);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, L.err, kErrWaitProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_expect_tx(fb, tx);
+          const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_STAGE;
+          tma_load_2d(sa, &P.tmP, kb * BK, rowP, fb);
+          if (sym) {
+            const int rowQ = c.mat * P.p.N + c.tj * P.bn;
+            for (int h = 0; h < P.bn / BM; ++h) tma_load_2d(sb + h * (BM * BK * 2), &P.tmQ, kb * BK, rowQ + h * BM, fb);
+          } else {
+            const int rowQ = c.mat * P.p.K + kb * BK;
+            for (int q = 0; q < P.bn / 64; ++q) tma_load_2d(sb + q * (64 * BK * 2), &P.tmQ, c.tj * P.bn + q * 64, rowQ, fb);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: wait for the copies of the most recent ring lap to land.
+      const int pending = issued < STAGES ? issued : STAGES;
+      int s = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < pending; ++i) {
+        if (--s < 0) {
+          s = STAGES - 1;
+          ph ^= 1u;
+        }
+        // full[s] completes phase `ph` when that copy lands; a dedicated
+        // bound keeps this loop finite even when the CTA is aborting.
+        const uint64_t t0 = global_timer();
+        while (!mbar_try_wait(full0 + 8 * s, ph)) {
+          if (global_timer() - t0 > kWaitLimitNs) {
+            atomicCAS(L.err, 0, kErrWaitProducer);
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int g = blockIdx.x; g < L.total_tiles && ok; g += gridDim.x) {
+        const TileCoord c = decode_tile(L, g);
+        const TcProblem& P = L.prob[c.prob];
+        const int kblocks = P.p.K / BK;
+        const bool sym = P.p.kind != NS_UPDATE;
+        const uint32_t idesc = idesc_bf16(P.bn, !sym);
+        const uint32_t lbo_mn = L.mn_swap ? 1024u : 64u * BK * 2u;
+        const uint32_t sbo_mn = L.mn_swap ? 64u * BK * 2u : 1024u;
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, L.err, kErrWaitMma)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN_MAX);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, L.err, kErrWaitMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sdesc(sa + kk * 32, 16, 1024);
+            const uint64_t bd = sym ? sdesc(sb + kk * 32, 16, 1024) : sdesc(sb + kk * 16 * 128, lbo_mn, sbo_mn);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty0 + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // Drain: every MMA issued above completes before TMEM is released.
+      umma_commit(drain);
+      const uint64_t t0 = global_timer();
+      while (!mbar_try_wait(drain, 0)) {
+        if (global_timer() - t0 > kWaitLimitNs) {
+          atomicCAS(L.err, 0, kErrWaitMma);
+          break;
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. 32*quarter+31
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int g = blockIdx.x; g < L.total_tiles; g += gridDim.x) {
+      const TileCoord c = decode_tile(L, g);
+      const TcProblem& P = L.prob[c.prob];
+      // every lane waits; the vote keeps the warp converged for tcgen05.ld
+      const bool got = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, L.err, kErrWaitEpilogue);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const int i = c.ti * BM + row;
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN_MAX);
+      for (int c0 = 0; c0 < P.bn; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
+        tmem_ld_wait();
+        const int j0 = c.tj * P.bn + c0;
+#pragma unroll 4
+        for (int e = 0; e < 32; ++e) ns_epilogue_element(P.p, L.epi, c.mat, i, j0 + e, __uint_as_float(r[e]));
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// ---- host side ----
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+               char* errbuf, size_t errlen) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) {
+    snprintf(errbuf, errlen, "cuTensorMapEncodeTiled entry point not available");
+    return false;
+  }
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(errbuf, errlen, "cuTensorMapEncodeTiled failed (%d) for %llux%llu box %ux%u", (int)r,
+             (unsigned long long)rows, (unsigned long long)cols, box_rows, box_cols);
+    return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+int ns_tc_num_tiles_sym(int tiles_m, int bn) {
+  int n = 0;
+  for (int ti = 0; ti < tiles_m; ++ti) n += (ti * BM + BM - 1) / bn + 1;
+  return n;
+}
+
+bool tc_encode_problem(TcProblem& tp, char* errbuf, size_t errlen) {
+  const NsProblem& p = tp.p;
+  if (p.M % BM || p.K % BK || p.N % 128) {
+    snprintf(errbuf, errlen, "tcgen05 GEMM needs M%%128 == 0, K%%64 == 0, N%%128 == 0 (M=%d N=%d K=%d)", p.M, p.N,
+             p.K);
+    return false;
+  }
+  tp.bn = (p.N % 256 == 0) ? 256 : 128;
+  tp.tiles_m = p.M / BM;
+  tp.tiles_n = p.N / tp.bn;
+  tp.tiles_per_mat = p.kind == NS_UPDATE ? tp.tiles_m * tp.tiles_n : ns_tc_num_tiles_sym(tp.tiles_m, tp.bn);
+  const uint64_t nm = (uint64_t)p.nmat;
+  // Left operand: [nmat * M] rows x K cols, K-major tiles of 128 x 64.
+  if (!encode_2d(&tp.tmP, p.P, (uint64_t)p.K, nm * p.M, BK, BM, errbuf, errlen)) return false;
+  if (p.kind == NS_UPDATE) {
+    // Right operand X: [nmat * K] rows x N cols, MN-major tiles of 64 (K) x 64 (N).
+    if (!encode_2d(&tp.tmQ, p.Q, (uint64_t)p.N, nm * p.K, 64, BK, errbuf, errlen)) return false;
+  } else {
+    // Right operand = rows of the same matrix: [nmat * N] rows x K cols.
+    if (!encode_2d(&tp.tmQ, p.Q, (uint64_t)p.K, nm * p.N, BK, BM, errbuf, errlen)) return false;
+  }
+  return true;
+}
+
+size_t ns_tc_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t ns_tc_prepare() {
+  return cudaFuncSetAttribute(ns_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+}
+
+void launch_ns_tc(const TcLaunch& L, int grid, cudaStream_t st) {
+  if (grid > L.total_tiles) grid = L.total_tiles;
+  if (grid <= 0) return;
+  ns_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(L);
+}
+
+}  // namespace ma

@@ -1,0 +1,185 @@
+"""Run the CUDA optimizer and the fp64 oracle side by side on the same inputs.
+
+Inputs come from ``workloads`` (seeded, synthetic). The GPU side goes
+through the C ABI (via the ctypes binding); the oracle side is ``oracle``.
+Nothing computed by the CUDA path is ever fed to the oracle.
+
+Tolerances (derived from the arithmetic; see the assertions below):
+  * global norm: relative 1e-5 (fp32 partial sums, Kahan-compensated);
+  * AdamW p, m, v and Muon momentum: 1e-6 relative to the magnitude of the
+    terms each recurrence adds (|x| plus the absolute terms), which is the
+    fp32 rounding bound of those few operations with headroom; a plain
+    |x_gpu - x_orc| <= 1e-6 |x_orc| cannot hold where the terms cancel;
+  * the orthogonalised update O (bf16 Newton-Schulz): relative Frobenius
+    error <= 2e-2 per matrix. O is recovered from the fp32 parameter update:
+    O = (p_before * decay - p_after) / (lr * lr_mult), with decay and
+    lr_mult rounded to fp32 as the kernel uses them.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+import oracle
+import workloads
+
+O_TOL = 2e-2
+STATE_TOL = 1e-6
+NORM_TOL = 1e-5
+
+
+def _f32(x: float) -> float:
+    return float(np.float32(x))
+
+
+class GpuSide:
+    """GPU tensors of a workload registered with one optimizer handle."""
+
+    def __init__(self, w: workloads.Workload, masters: List[np.ndarray], *, config: Optional[dict] = None):
+        import torch
+
+        import muon_adamw_hybrid_grad_gb300 as mx
+
+        self.torch = torch
+        self.mx = mx
+        self.w = w
+        dev = torch.device("cuda")
+        gdt = torch.bfloat16 if w.grad_dtype == "bf16" else torch.float32
+        cfg = dict(config or {})
+        cfg.setdefault("precision", mx.MA_BF16_MIXED if w.policy == "bf16_mixed" else mx.MA_FP32_MIXED)
+        self.P, self.G, self.S = [], [], []
+        entries = []
+        for i, t in enumerate(w.tensors):
+            p = torch.from_numpy(masters[i]).to(dev) if masters[i] is not None else None
+            g = None if t.frozen else torch.zeros(t.shape, dtype=gdt, device=dev)
+            s = (torch.zeros(t.shape, dtype=torch.bfloat16, device=dev)
+                 if (w.policy == "bf16_mixed" and not t.frozen) else None)
+            if p is None:
+                p = torch.zeros(t.shape, dtype=torch.float32, device=dev)
+            self.P.append(p)
+            self.G.append(g)
+            self.S.append(s)
+            entries.append((t.name, p, g, s, mx.MA_GROUP_FROZEN if t.frozen else None))
+        self.opt = mx.MuonAdamW(entries, **cfg)
+
+    def load_grads(self, grads: Sequence[Optional[np.ndarray]]) -> None:
+        for g_dev, g in zip(self.G, grads):
+            if g_dev is not None:
+                g_dev.copy_(self.torch.from_numpy(np.ascontiguousarray(g)).to(g_dev.dtype))
+
+    def step(self, lr: float) -> float:
+        return self.opt.step(lr, want_norm=True)
+
+    def param(self, i: int) -> np.ndarray:
+        return self.P[i].cpu().numpy()
+
+    def close(self):
+        self.opt.close()
+
+
+def compare_state(name: str, got: np.ndarray, want: np.ndarray, scale: np.ndarray, tol: float = STATE_TOL):
+    err = np.abs(got.astype(np.float64) - want)
+    bound = tol * scale + 1e-30
+    bad = err > bound
+    if bad.any():
+        k = int(np.argmax(err - bound))
+        raise AssertionError(
+            f"{name}: {int(bad.sum())} of {bad.size} elements out of tolerance; worst at flat index {k}: "
+            f"got {got.flat[k]!r} want {want.flat[k]!r} scale {scale.flat[k]!r}")
+
+
+def relative_frobenius(got: np.ndarray, want: np.ndarray) -> float:
+    den = np.linalg.norm(want)
+    return float(np.linalg.norm(got - want) / den) if den > 0 else float(np.linalg.norm(got))
+
+
+def run_parity(w: workloads.Workload, *, steps: Optional[int] = None, config: Optional[dict] = None,
+               oracle_overrides: Optional[dict] = None, muon_sample: Optional[Sequence[int]] = None,
+               grad_scale: float = 1.0, lr: Optional[float] = None, check_states: bool = True,
+               optim: str = "muon_adamw") -> Dict[str, object]:
+    """Run ``steps`` optimizer steps on both sides and assert parity.
+
+    ``muon_sample``: Muon parameter indices whose Newton-Schulz output is
+    checked (all when None). Every AdamW/momentum element is checked when
+    ``check_states`` is set.
+    """
+    steps = steps or w.steps
+    lr = w.lr if lr is None else lr
+    masters = workloads.master_weights(w)
+    gpu = GpuSide(w, masters, config=config)
+    try:
+        cfg = gpu.opt.cfg
+        names = [t.name for t in w.tensors]
+        shapes = [t.shape for t in w.tensors]
+        frozen = [t.frozen for t in w.tensors]
+        ov = dict(oracle_overrides or {})
+        orc = oracle.HybridOracle(names, shapes, frozen, optim=optim, **ov)
+        groups = orc.groups
+        assert groups == gpu.opt.groups, "routing differs between the C ABI and the oracle"
+        muon_idx = [i for i, g in enumerate(groups) if g == "muon"]
+        adam_idx = [i for i, g in enumerate(groups) if g == "adamw"]
+        sample = muon_idx if muon_sample is None else list(muon_sample)
+        orc_p = [m.astype(np.float64) for m in masters]
+        worst_o = 0.0
+        sum_abs_g: Dict[int, np.ndarray] = {}
+        beta1, beta2 = orc.cfg["adam_betas"]
+        mu = orc.cfg["muon_momentum"]
+        for step in range(1, steps + 1):
+            grads = workloads.gradients(w, step, scale=grad_scale)
+            gpu.load_grads(grads)
+            before = {i: gpu.param(i) for i in sample}
+            adam_before = {i: orc_p[i].copy() for i in adam_idx} if check_states else {}
+            total_gpu = gpu.step(lr)
+            res = orc.step(orc_p, grads, lr, muon_indices=sample)
+            # --- norm ---
+            assert math.isclose(total_gpu, res["total"], rel_tol=NORM_TOL, abs_tol=1e-30), \
+                f"step {step}: norm {total_gpu} vs {res['total']}"
+            coef = res["coef"]
+            # --- Muon: momentum (all elements) and O (sampled) ---
+            decay = _f32(1.0 - _f32(lr) * _f32(cfg.muon_weight_decay))
+            for i in muon_idx:
+                ghat = np.abs(coef * grads[i].astype(np.float64))
+                sum_abs_g[i] = sum_abs_g.get(i, 0.0) + ghat
+                if check_states:
+                    buf = gpu.opt.state(i, 0).numpy()
+                    compare_state(f"step {step} buf[{names[i]}]", buf, orc.buf[i],
+                                  np.abs(orc.buf[i]) + sum_abs_g[i])
+            for i in sample:
+                m_, n_ = shapes[i]
+                lr_mult = _f32(_f32(cfg.muon_lr_scale) * _f32(cfg.moonlight_coef) * math.sqrt(max(m_, n_)))
+                after = gpu.param(i).astype(np.float64)
+                O_gpu = (before[i].astype(np.float64) * decay - after) / (_f32(lr) * lr_mult)
+                err = relative_frobenius(O_gpu, res["O"][i])
+                worst_o = max(worst_o, err)
+                assert err <= O_TOL, f"step {step} {names[i]} {shapes[i]}: O rel. Frobenius error {err:.3e}"
+                if gpu.S[i] is not None:
+                    sh = gpu.S[i].float().cpu().numpy()
+                    want = workloads.bf16_round(after.astype(np.float32))
+                    assert np.array_equal(sh, want), f"{names[i]}: bf16 shadow != bf16(p)"
+            # --- AdamW ---
+            if check_states:
+                t = res["t"]
+                for i in adam_idx:
+                    ghat = np.abs(coef * grads[i].astype(np.float64))
+                    m_gpu = gpu.opt.state(i, 0).numpy()
+                    v_gpu = gpu.opt.state(i, 1).numpy()
+                    compare_state(f"step {step} m[{names[i]}]", m_gpu, orc.m[i], np.abs(orc.m[i]) + ghat)
+                    compare_state(f"step {step} v[{names[i]}]", v_gpu, orc.v[i], np.abs(orc.v[i]) + ghat * ghat)
+                    p_gpu = gpu.param(i)
+                    upd = lr * t * 10.0
+                    compare_state(f"step {step} p[{names[i]}]", p_gpu, orc_p[i],
+                                  np.abs(adam_before[i]) + np.abs(orc_p[i]) + upd)
+                    if gpu.S[i] is not None:
+                        sh = gpu.S[i].float().cpu().numpy()
+                        assert np.array_equal(sh, workloads.bf16_round(p_gpu)), f"{names[i]}: shadow"
+                    # keep the oracle on the same footing as the GPU for the
+                    # next step's parameters (p is compared, not inherited)
+            # frozen params are never written
+            for i, fz in enumerate(frozen):
+                if fz:
+                    assert np.array_equal(gpu.param(i), masters[i]), f"frozen {names[i]} was modified"
+        return {"worst_o": worst_o, "steps": steps, "groups": groups}
+    finally:
+        gpu.close()
