@@ -1,0 +1,425 @@
+"""Benchmark of the hybrid Muon + AdamW optimizer step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One "step" is one full optimizer step of the workload (global grad norm and
+clip, Muon momentum, five Newton-Schulz iterations and update, AdamW) with
+all inputs resident in HBM. Default workload: h1024 (action expert, hidden
+1024, MLP 4096, 16 layers: 112 Muon matrices, 268 M elements; 82,944 AdamW
+elements; bf16 gradients, fp32 masters, bf16 shadow). Its inputs (~2.6 GB
+touched per step) exceed the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0). value = optimizer steps/s for the whole job;
+under torchrun each rank runs an independent replica (the optimizer step of
+one model does not shard here: "replicas only"), so value = N * K / (max over
+ranks of the timed region). Extra keys: per-kernel CUDA-event breakdown, the
+roofline of the dominant kernel (the Newton-Schulz GEMM), the SM clocks seen
+during the timed region, an end-to-end figure (gradients copied from pinned
+host memory every step, the norm read back), and the fp64 oracle timed on a
+bounded sample on the host cores (cpu_baseline).
+
+--impl reference times the fp64 CPU oracle (the only reference that exists:
+the source pages ship no code) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "optimizer steps/s; NS5 TFLOP/s vs bf16 peak; AdamW HBM GB/s vs peak"
+KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "adamw")
+NS_KINDS = ("ns_gram", "ns_poly", "ns_update")
+STREAM_KINDS = ("grad_norm", "momentum", "adamw")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# multi-rank plumbing (replicas only)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when dist is None)."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(steps: int, n_ranks: int, max_seconds: float) -> float:
+    """Whole-job optimizer steps/s: every rank ran `steps` steps of its replica."""
+    return n_ranks * steps / max_seconds
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample_seconds(w, layers_sampled: int = 1):
+    """Time the fp64 oracle on a bounded sample of workload `w` and scale it
+    to one full step. Returns (seconds per full step, description)."""
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    names = [t.name for t in w.tensors]
+    groups = [oracle.route(n, len(t.shape), frozen=t.frozen) for n, t in zip(names, w.tensors)]
+    muon = [i for i, g in enumerate(groups) if g == "muon"]
+    adam = [i for i, g in enumerate(groups) if g == "adamw"]
+    # sample: the Muon matrices of the first `layers_sampled` layers (all shapes),
+    # and AdamW tensors up to 1 M elements
+    layer_of = lambda n: n.split(".layers.")[1].split(".")[0] if ".layers." in n else None  # noqa: E731
+    first_layers = []
+    for i in muon:
+        lid = layer_of(names[i])
+        if lid not in first_layers:
+            first_layers.append(lid)
+    keep_layers = set(first_layers[:layers_sampled])
+    ms = [i for i in muon if layer_of(names[i]) in keep_layers]
+    ad, tot = [], 0
+    for i in adam:
+        if tot >= 1_000_000:
+            break
+        ad.append(i)
+        tot += w.tensors[i].numel
+    idx = ms + ad
+    sub = type(w)(w.name + "_sample", tuple(w.tensors[i] for i in idx), w.policy, w.grad_dtype, 1, w.lr)
+    masters = [workloads.master_weight(w, i).astype(np.float64) for i in idx]
+    grads = [workloads.gradient(w, i, 1) for i in idx]
+    orc = oracle.HybridOracle([names[i] for i in idx], [w.tensors[i].shape for i in idx])
+    t0 = time.perf_counter()
+    orc.step(masters, grads, w.lr)
+    dt = time.perf_counter() - t0
+
+    def ns_flops(shape):
+        s, l = min(shape), max(shape)
+        return 5 * (4 * s * s * l + 2 * s * s * s)
+
+    f_all = sum(ns_flops(w.tensors[i].shape) for i in muon)
+    f_smp = sum(ns_flops(w.tensors[i].shape) for i in ms) or 1
+    e_all = sum(w.tensors[i].numel for i in adam)
+    e_smp = sum(w.tensors[i].numel for i in ad) or 1
+    # split the sample time by a separate timing of its AdamW part
+    t1 = time.perf_counter()
+    orc2 = oracle.HybridOracle([names[i] for i in ad], [w.tensors[i].shape for i in ad])
+    orc2.step([masters[len(ms) + k].copy() for k in range(len(ad))], grads[len(ms):], w.lr)
+    dt_ad = time.perf_counter() - t1
+    dt_ms = max(dt - dt_ad, 0.0)
+    full = dt_ms * (f_all / f_smp) + (dt_ad * (e_all / e_smp) if ad else 0.0)
+    desc = (f"fp64 numpy oracle, one step over the Muon matrices of {len(keep_layers)} of "
+            f"{len(first_layers)} layers ({len(ms)} matrices) and {len(ad)} AdamW tensors "
+            f"({e_smp} elements), {dt:.2f} s; scaled to the full step by NS flops and AdamW elements")
+    return full, desc, dt
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import muon_adamw_hybrid_grad_gb300 as mx
+    import workloads
+    from muon_adamw_hybrid_grad_gb300 import build as _b
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    _b.build()
+    mx.load_library()
+    dev = torch.device("cuda", local)
+    w = workloads.get_workload(args.workload)
+    lr = w.lr
+    if w.schedule is not None:
+        step_, total_, warm_, min_rate = w.schedule
+        lr = w.lr * mx.muon_adamw_cosine_with_min_lr(step_, total_, warm_, min_rate)
+    gdt = torch.bfloat16 if w.grad_dtype == "bf16" else torch.float32
+    masters = workloads.master_weights(w)
+    grads = workloads.gradients(w, 1)
+    P, G, S, entries = [], [], [], []
+    host_grads = []
+    for i, t in enumerate(w.tensors):
+        p = torch.from_numpy(masters[i]).to(dev)
+        g = None if t.frozen else torch.from_numpy(grads[i]).to(dev).to(gdt)
+        s = torch.empty(t.shape, dtype=torch.bfloat16, device=dev) if (w.policy == "bf16_mixed" and not t.frozen) \
+            else None
+        P.append(p)
+        G.append(g)
+        S.append(s)
+        entries.append((t.name, p, g, s, mx.MA_GROUP_FROZEN if t.frozen else None))
+        if g is not None:
+            host_grads.append(g.cpu().pin_memory())
+    del masters, grads
+    stream = torch.cuda.current_stream()
+    opt = mx.MuonAdamW(entries, precision=mx.MA_BF16_MIXED if w.policy == "bf16_mixed" else mx.MA_FP32_MIXED,
+                       stream=stream)
+    for _ in range(args.warmup):
+        opt.step(lr)
+    torch.cuda.synchronize()
+    info = opt.plan_info()
+    # ---- timed region (device time, CUDA events on the launching stream) ----
+    mx.muon_adamw_reset_profile(opt.handle)
+    mx.muon_adamw_set_profiling(opt.handle, True)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        opt.step(lr)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    mx.muon_adamw_set_profiling(opt.handle, False)
+    prof = opt.profile()
+    max_s = max_over_ranks(ms / 1e3, dist, dev)
+    value = aggregate(args.steps, world, max_s)
+
+    # ---- end to end: grads from pinned host memory each step, norm read back ----
+    h2d = sum(h.numel() * h.element_size() for h in host_grads)
+    gdev = [g for g in G if g is not None]
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for hd, gd in zip(host_grads, gdev):
+            gd.copy_(hd, non_blocking=True)
+        opt.step(lr, want_norm=True)  # synchronises and reads the 4-byte norm
+    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, dist, dev)
+
+    peaks = load_peaks()
+    ns_ms = sum(prof[k]["ms"] for k in NS_KINDS)
+    ns_flops = sum(prof[k]["units"] for k in NS_KINDS)
+    ns_launches = sum(prof[k]["launches"] for k in NS_KINDS)
+    ns_tflops = ns_flops / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
+    kernels = {}
+    for k in KINDS:
+        e = prof[k]
+        if e["launches"] == 0:
+            continue
+        d = {"launches": e["launches"], "ms_total": round(e["ms"], 4),
+             "ms_per_launch": round(e["ms"] / e["launches"], 5)}
+        if k in NS_KINDS:
+            d["tflops"] = round(e["units"] / (e["ms"] / 1e3) / 1e12, 1)
+            d["frac_bf16_peak"] = round(d["tflops"] / peaks["bf16_tflops"], 3)
+        elif k in STREAM_KINDS:
+            d["gbs"] = round(e["units"] / (e["ms"] / 1e3) / 1e9, 1)
+            d["frac_hbm"] = round(d["gbs"] / peaks["hbm_gbs"], 3)
+        kernels[k] = d
+    launches = sum(prof[k]["launches"] for k in KINDS)
+    out = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_s * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) fp32 masters, N(0,1e-3)+rank-8 bf16 gradients)",
+        "config": {
+            "workload": f"{w.name}: {len(w.tensors)} tensors, {info['n_muon']} Muon matrices "
+                        f"({info['muon_elems']} elements, {info['n_buckets']} shape buckets), "
+                        f"{info['adamw_elems']} AdamW elements, {w.grad_dtype} grads, {w.policy}",
+            "lr": lr,
+            "l2": "no flush: each step touches "
+                  f"{info['stream_bytes_per_step'] / 1e9:.2f} GB of state and gradients, far above the 129 MB L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "ns5_tflops": round(ns_tflops, 1) if ns_tflops else None,
+        "ns5_frac_bf16_peak": round(ns_tflops / peaks["bf16_tflops"], 3) if ns_tflops else None,
+        "ns5_dense_equiv_tflops": round(info["ns_dense_flops_per_step"] * args.steps / (ns_ms / 1e3) / 1e12, 1)
+        if ns_ms > 0 else None,
+        "kernels": kernels,
+        "roofline": {
+            "kernel": "ns_tc_kernel (tcgen05 Newton-Schulz GEMMs: X X^T, A A, B X; all launches)",
+            "bound": "tensor",
+            "achieved": round(ns_tflops, 1) if ns_tflops else None,
+            "peak": peaks["bf16_tflops"],
+            "peak_kind": f"bf16 dense burst, {peaks['source']} (MEASURED_PEAKS.json)",
+            "unit": "TFLOP/s",
+            "frac": round(ns_tflops / peaks["bf16_tflops"], 3) if ns_tflops else None,
+            "traffic": None,
+            "launches_timed": ns_launches,
+            "algorithmic_flops_per_launch": round(ns_flops / max(1, ns_launches)),
+        },
+        "clocks": clk,
+        "e2e": {"value": round(args.steps * world / e2e_s, 3), "unit": "steps/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4,
+                "how": "every step: all gradients copied host->device from pinned memory, "
+                       "then muon_adamw_step with the norm read back (synchronising)"},
+        "gpu_launches": int(launches),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        full, desc, spent = oracle_sample_seconds(w, layers_sampled=args.cpu_layers)
+        out["cpu_baseline"] = {"value": round(1.0 / full, 6), "unit": "steps/s", "cores": host_cores(),
+                               "kind": "oracle", "sample": desc}
+    opt.close()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    import workloads
+
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = workloads.get_workload(args.workload)
+    for _ in range(args.warmup):
+        oracle_sample_seconds(w, layers_sampled=1)
+    per_step = []
+    desc = ""
+    for _ in range(args.steps):
+        full, desc, _spent = oracle_sample_seconds(w, layers_sampled=1)
+        per_step.append(full)
+    total = sum(per_step)
+    value = args.steps / total
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total * 1e3 / args.steps, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same seeded inputs as the GPU arm)",
+        "config": {"workload": w.name, "parallelism": "host CPU, rank 0 only"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": host_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="h1024")
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-layers", type=int, default=2, help="layers in the oracle's timed sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

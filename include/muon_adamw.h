@@ -88,19 +88,22 @@ typedef enum { MA_NS_TCGEN05 = 0, MA_NS_SIMT = 1 } ma_ns_kernel;
 typedef struct {
   int32_t mode;
   int32_t precision;
-  float muon_momentum;
   int32_t muon_nesterov;
   int32_t ns_steps;
-  float ns_a, ns_b, ns_c;
-  float ns_eps;
-  float moonlight_coef;
-  float muon_lr_scale;
-  float muon_weight_decay;
-  float adam_beta1, adam_beta2, adam_eps, adam_weight_decay;
-  float max_grad_norm;
-  float clip_eps;
   int32_t ns_kernel;
   int32_t reserved[7];
+  /* Real-valued settings are doubles (like Python floats); the kernels get
+   * fp32 values derived from them on the host, e.g. 1 - adam_beta2 is formed
+   * in double before rounding, so 0.999 yields exactly fp32(0.001). */
+  double muon_momentum;
+  double ns_a, ns_b, ns_c;
+  double ns_eps;
+  double moonlight_coef;
+  double muon_lr_scale;
+  double muon_weight_decay;
+  double adam_beta1, adam_beta2, adam_eps, adam_weight_decay;
+  double max_grad_norm;
+  double clip_eps;
 } muon_adamw_config;
 
 /* Per-kernel timing collected while profiling is on (see muon_adamw_set_profiling).
@@ -167,9 +170,10 @@ MA_API ma_status muon_adamw_create(const muon_adamw_config* cfg, void* cuda_stre
  *   name        host UTF-8 string (copied), used for routing;
  *   ndim, shape host array of ndim int64 sizes (ndim 0..8, sizes >= 0);
  *   param_fp32  device fp32 master weights, numel elements (updated in place;
- *               may be NULL only for MA_GROUP_FROZEN);
+ *               may be NULL only for MA_GROUP_FROZEN or numel == 0);
  *   grad        device gradient, numel elements of grad_dtype (MA_DT_BF16 or
- *               MA_DT_F32); read each step, never written; NULL only when frozen;
+ *               MA_DT_F32); read each step, never written; NULL only when
+ *               frozen or numel == 0;
  *   param_bf16_shadow  device bf16 copy written after each update when the
  *               precision is MA_BF16_MIXED, or NULL for none;
  *   group_override  MA_GROUP_AUTO applies the routing predicate (and the
@@ -193,7 +197,7 @@ MA_API ma_status muon_adamw_register_param(muon_adamw_t* h, const char* name, in
  * MA_ERR_DEVICE_CHECK. Non-finite gradients are not skipped: they propagate
  * into the parameters and the norm. Errors: MA_ERR_ARG (lr not finite),
  * MA_ERR_OOM, MA_ERR_CUDA, MA_ERR_DEVICE_CHECK. */
-MA_API ma_status muon_adamw_step(muon_adamw_t* h, float lr, float* grad_norm_out);
+MA_API ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out);
 
 /* Wait for the handle's stream and read the kernels' error flag.
  * MA_ERR_DEVICE_CHECK if a bounded in-kernel wait ran out. */

@@ -54,24 +54,24 @@ class MuonAdamWConfig(ctypes.Structure):
     _fields_ = [
         ("mode", ctypes.c_int32),
         ("precision", ctypes.c_int32),
-        ("muon_momentum", ctypes.c_float),
         ("muon_nesterov", ctypes.c_int32),
         ("ns_steps", ctypes.c_int32),
-        ("ns_a", ctypes.c_float),
-        ("ns_b", ctypes.c_float),
-        ("ns_c", ctypes.c_float),
-        ("ns_eps", ctypes.c_float),
-        ("moonlight_coef", ctypes.c_float),
-        ("muon_lr_scale", ctypes.c_float),
-        ("muon_weight_decay", ctypes.c_float),
-        ("adam_beta1", ctypes.c_float),
-        ("adam_beta2", ctypes.c_float),
-        ("adam_eps", ctypes.c_float),
-        ("adam_weight_decay", ctypes.c_float),
-        ("max_grad_norm", ctypes.c_float),
-        ("clip_eps", ctypes.c_float),
         ("ns_kernel", ctypes.c_int32),
         ("reserved", ctypes.c_int32 * 7),
+        ("muon_momentum", ctypes.c_double),
+        ("ns_a", ctypes.c_double),
+        ("ns_b", ctypes.c_double),
+        ("ns_c", ctypes.c_double),
+        ("ns_eps", ctypes.c_double),
+        ("moonlight_coef", ctypes.c_double),
+        ("muon_lr_scale", ctypes.c_double),
+        ("muon_weight_decay", ctypes.c_double),
+        ("adam_beta1", ctypes.c_double),
+        ("adam_beta2", ctypes.c_double),
+        ("adam_eps", ctypes.c_double),
+        ("adam_weight_decay", ctypes.c_double),
+        ("max_grad_norm", ctypes.c_double),
+        ("clip_eps", ctypes.c_double),
     ]
 
 
@@ -123,7 +123,7 @@ _SIGNATURES = {
     "muon_adamw_register_param": (ctypes.c_int, [_P, ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
                                                  _P, _P, ctypes.c_int, _P, ctypes.c_int,
                                                  ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
-    "muon_adamw_step": (ctypes.c_int, [_P, ctypes.c_float, ctypes.POINTER(ctypes.c_float)]),
+    "muon_adamw_step": (ctypes.c_int, [_P, ctypes.c_double, ctypes.POINTER(ctypes.c_float)]),
     "muon_adamw_sync": (ctypes.c_int, [_P]),
     "muon_adamw_get_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),
     "muon_adamw_set_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),

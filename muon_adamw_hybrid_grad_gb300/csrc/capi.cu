@@ -409,7 +409,9 @@ ma_status build_plan(muon_adamw* h) {
       M.transposed = M.m > M.n;
       M.gdtype = p.gdtype == MA_DT_BF16 ? DT_BF16 : DT_F32;
       M.vec = (M.n % 8 == 0) && (reinterpret_cast<uintptr_t>(p.g) % 16 == 0);
-      M.lr_mult = (float)((double)c.muon_lr_scale * c.moonlight_coef * sqrt((double)M.l));
+      M.pvec = (M.n % 8 == 0) && (reinterpret_cast<uintptr_t>(p.p) % 16 == 0) &&
+               (reinterpret_cast<uintptr_t>(p.shadow) % 16 == 0);
+      M.lr_mult = (float)(c.muon_lr_scale * c.moonlight_coef * sqrt((double)M.l));
       M.tile_begin = (int)tiles.size();
       for (int r0 = 0; r0 < M.m; r0 += kMomTile)
         for (int c0 = 0; c0 < M.n; c0 += kMomTile) tiles.push_back(MomTile{mat_index, r0, c0, 0});
@@ -515,12 +517,12 @@ ma_status build_plan(muon_adamw* h) {
   return MA_OK;
 }
 
-void set_epi(NsEpiArgs& e, const muon_adamw_config& c, float lr) {
-  e.a = c.ns_a;
-  e.b = c.ns_b;
-  e.c = c.ns_c;
-  e.decay = (float)(1.0 - (double)lr * c.muon_weight_decay);
-  e.lr = lr;
+void set_epi(NsEpiArgs& e, const muon_adamw_config& c, double lr) {
+  e.a = (float)c.ns_a;
+  e.b = (float)c.ns_b;
+  e.c = (float)c.ns_c;
+  e.decay = (float)(1.0 - lr * c.muon_weight_decay);
+  e.lr = (float)lr;
 }
 
 ma_status valid_config(const muon_adamw_config* c) {
@@ -529,9 +531,9 @@ ma_status valid_config(const muon_adamw_config* c) {
     return fail(MA_ERR_ARG, "bad precision %d", c->precision);
   if (c->ns_steps < 1 || c->ns_steps > 64) return fail(MA_ERR_ARG, "ns_steps must be in [1, 64]");
   if (c->ns_kernel != MA_NS_TCGEN05 && c->ns_kernel != MA_NS_SIMT) return fail(MA_ERR_ARG, "bad ns_kernel");
-  if (!(c->adam_beta1 >= 0.f && c->adam_beta1 < 1.f) || !(c->adam_beta2 >= 0.f && c->adam_beta2 < 1.f))
+  if (!(c->adam_beta1 >= 0.0 && c->adam_beta1 < 1.0) || !(c->adam_beta2 >= 0.0 && c->adam_beta2 < 1.0))
     return fail(MA_ERR_ARG, "betas must lie in [0, 1)");
-  if (!(c->adam_eps >= 0.f) || !(c->ns_eps >= 0.f) || !(c->clip_eps >= 0.f)) return fail(MA_ERR_ARG, "eps < 0");
+  if (!(c->adam_eps >= 0.0) || !(c->ns_eps >= 0.0) || !(c->clip_eps >= 0.0)) return fail(MA_ERR_ARG, "eps < 0");
   if (!isfinite(c->muon_momentum) || !isfinite(c->max_grad_norm) || !isfinite(c->muon_lr_scale) ||
       !isfinite(c->moonlight_coef) || !isfinite(c->ns_a) || !isfinite(c->ns_b) || !isfinite(c->ns_c))
     return fail(MA_ERR_ARG, "non-finite config value");
@@ -547,22 +549,22 @@ void muon_adamw_config_init(muon_adamw_config* cfg) {
   memset(cfg, 0, sizeof *cfg);
   cfg->mode = MA_MODE_MUON_ADAMW;
   cfg->precision = MA_BF16_MIXED;
-  cfg->muon_momentum = 0.95f;
+  cfg->muon_momentum = 0.95;
   cfg->muon_nesterov = 1;
   cfg->ns_steps = 5;
-  cfg->ns_a = 3.4445f;
-  cfg->ns_b = -4.7750f;
-  cfg->ns_c = 2.0315f;
-  cfg->ns_eps = 1e-7f;
-  cfg->moonlight_coef = 0.2f;
-  cfg->muon_lr_scale = 1.0f;
-  cfg->muon_weight_decay = 0.1f;
-  cfg->adam_beta1 = 0.9f;
-  cfg->adam_beta2 = 0.999f;
-  cfg->adam_eps = 1e-8f;
-  cfg->adam_weight_decay = 0.1f;
-  cfg->max_grad_norm = 1.0f;
-  cfg->clip_eps = 1e-6f;
+  cfg->ns_a = 3.4445;
+  cfg->ns_b = -4.7750;
+  cfg->ns_c = 2.0315;
+  cfg->ns_eps = 1e-7;
+  cfg->moonlight_coef = 0.2;
+  cfg->muon_lr_scale = 1.0;
+  cfg->muon_weight_decay = 0.1;
+  cfg->adam_beta1 = 0.9;
+  cfg->adam_beta2 = 0.999;
+  cfg->adam_eps = 1e-8;
+  cfg->adam_weight_decay = 0.1;
+  cfg->max_grad_norm = 1.0;
+  cfg->clip_eps = 1e-6;
   cfg->ns_kernel = MA_NS_TCGEN05;
 }
 
@@ -643,7 +645,7 @@ ma_status muon_adamw_register_param(muon_adamw_t* h, const char* name, int ndim,
     if (p.shape[0] >= ((int64_t)1 << 30) || p.shape[1] >= ((int64_t)1 << 30))
       return fail(MA_ERR_SHAPE, "Muon matrix dimension too large");
   }
-  if (group != MA_GROUP_FROZEN) {
+  if (group != MA_GROUP_FROZEN && p.numel > 0) {
     if (!param_fp32 || !grad) return fail(MA_ERR_ARG, "param and grad must not be NULL for trainable '%s'", name);
     if (grad_dtype != MA_DT_F32 && grad_dtype != MA_DT_BF16) return fail(MA_ERR_DTYPE, "bad grad dtype %d", grad_dtype);
     if (reinterpret_cast<uintptr_t>(param_fp32) % 4) return fail(MA_ERR_ALIGN, "param not 4-byte aligned");
@@ -662,7 +664,7 @@ ma_status muon_adamw_register_param(muon_adamw_t* h, const char* name, int ndim,
   return ok();
 }
 
-ma_status muon_adamw_step(muon_adamw_t* h, float lr, float* grad_norm_out) {
+ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
   if (!h) return fail(MA_ERR_ARG, "NULL handle");
   if (!isfinite(lr)) return fail(MA_ERR_ARG, "lr is not finite");
   CUDA_TRY(cudaSetDevice(h->device));
@@ -681,8 +683,8 @@ ma_status muon_adamw_step(muon_adamw_t* h, float lr, float* grad_norm_out) {
     CUDA_TRY(cudaMemsetAsync(h->d_norm_partials, 0, sizeof(float), h->s0));
   }
   timed(h, MA_K_CLIP, h->s0, (double)h->norm_grid * 4, [&] {
-    launch_clip_finalize(h->d_norm_partials, h->n_norm_chunks > 0 ? h->norm_grid : 1, c.max_grad_norm, c.clip_eps,
-                         h->d_scalars, h->s0);
+    launch_clip_finalize(h->d_norm_partials, h->n_norm_chunks > 0 ? h->norm_grid : 1, (float)c.max_grad_norm,
+                         (float)c.clip_eps, h->d_scalars, h->s0);
   });
 
   const bool have_adam = h->n_adam_chunks > 0;
@@ -690,27 +692,27 @@ ma_status muon_adamw_step(muon_adamw_t* h, float lr, float* grad_norm_out) {
     CUDA_TRY(cudaEventRecord(h->ev_fork, h->s0));
     CUDA_TRY(cudaStreamWaitEvent(h->s1, h->ev_fork, 0));
     AdamArgs a;
-    a.beta1 = c.adam_beta1;
-    a.beta2 = c.adam_beta2;
-    a.omb1 = (float)(1.0 - (double)c.adam_beta1);
-    a.omb2 = (float)(1.0 - (double)c.adam_beta2);
-    a.eps = c.adam_eps;
-    a.decay = (float)(1.0 - (double)lr * c.adam_weight_decay);
-    const double bc1 = 1.0 - pow((double)c.adam_beta1, t), bc2 = 1.0 - pow((double)c.adam_beta2, t);
-    a.step_size = (float)((double)lr / bc1);
+    a.beta1 = (float)c.adam_beta1;
+    a.beta2 = (float)c.adam_beta2;
+    a.omb1 = (float)(1.0 - c.adam_beta1);
+    a.omb2 = (float)(1.0 - c.adam_beta2);
+    a.eps = (float)c.adam_eps;
+    a.decay = (float)(1.0 - lr * c.adam_weight_decay);
+    const double bc1 = 1.0 - pow(c.adam_beta1, t), bc2 = 1.0 - pow(c.adam_beta2, t);
+    a.step_size = (float)(lr / bc1);
     a.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
     timed(h, MA_K_ADAMW, h->s1, h->bytes_adam,
           [&] { launch_adamw(h->d_adam_chunks, h->n_adam_chunks, h->d_scalars, a, h->adam_grid, h->s1); });
   }
 
   if (h->n_mats > 0) {
-    MomArgs ma_{c.muon_momentum, c.muon_nesterov};
+    MomArgs ma_{(float)c.muon_momentum, c.muon_nesterov};
     timed(h, MA_K_MOMENTUM, h->s0, h->bytes_mom, [&] {
       launch_muon_momentum(h->d_tiles, h->n_tiles, h->d_mats, h->d_scalars, ma_, h->d_tile_partials, h->mom_grid,
                            h->s0);
     });
     timed(h, MA_K_NS_PREP, h->s0, (double)h->n_tiles * 4,
-          [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, c.ns_eps, h->d_rscale, h->s0); });
+          [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, (float)c.ns_eps, h->d_rscale, h->s0); });
     NsEpiArgs epi;
     set_epi(epi, c, lr);
     const double units[3] = {h->unit_gram, h->unit_poly, h->unit_update};
@@ -774,12 +776,12 @@ static ma_status state_ptr(muon_adamw_t* h, int index, int which, float** ptr, i
 }
 
 ma_status muon_adamw_get_state(muon_adamw_t* h, int index, int which, float* dst_host) {
-  if (!dst_host) return fail(MA_ERR_ARG, "dst must not be NULL");
   if (h && !h->planned) return fail(MA_ERR_STATE, "no state before the first step");
   float* src = nullptr;
   int64_t n = 0;
   ma_status st = state_ptr(h, index, which, &src, &n);
   if (st != MA_OK) return st;
+  if (!dst_host && n > 0) return fail(MA_ERR_ARG, "dst must not be NULL");
   CUDA_TRY(cudaSetDevice(h->device));
   CUDA_TRY(cudaStreamSynchronize(h->s0));
   if (n > 0) CUDA_TRY(cudaMemcpy(dst_host, src, n * sizeof(float), cudaMemcpyDeviceToHost));
@@ -787,7 +789,7 @@ ma_status muon_adamw_get_state(muon_adamw_t* h, int index, int which, float* dst
 }
 
 ma_status muon_adamw_set_state(muon_adamw_t* h, int index, int which, const float* src_host) {
-  if (!h || !src_host) return fail(MA_ERR_ARG, "handle and src must not be NULL");
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
   CUDA_TRY(cudaSetDevice(h->device));
   if (!h->planned) {
     ma_status st = build_plan(h);
@@ -797,6 +799,7 @@ ma_status muon_adamw_set_state(muon_adamw_t* h, int index, int which, const floa
   int64_t n = 0;
   ma_status st = state_ptr(h, index, which, &dst, &n);
   if (st != MA_OK) return st;
+  if (!src_host && n > 0) return fail(MA_ERR_ARG, "src must not be NULL");
   CUDA_TRY(cudaStreamSynchronize(h->s0));
   if (n > 0) CUDA_TRY(cudaMemcpy(dst, src_host, n * sizeof(float), cudaMemcpyHostToDevice));
   return ok();

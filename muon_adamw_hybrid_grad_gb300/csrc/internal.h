@@ -47,6 +47,7 @@ struct MuonMat {        // one Muon matrix (device-visible metadata)
   int32_t transposed;   // 1 if m > n (X = update^T)
   int32_t gdtype;
   int32_t vec;          // rows of g/buf allow 16-byte vector access
+  int32_t pvec;         // rows of p (and shadow) allow 8-element vector access
   int32_t tile_begin;   // momentum tiles [tile_begin, tile_end) in the tile list
   int32_t tile_end;
   float lr_mult;        // muon_lr_scale * moonlight * sqrt(max(m, n))

@@ -5,7 +5,7 @@
 // five times, on the short side. Each launch covers one of the three
 // products for every Muon matrix of up to four shape buckets.
 //
-// Structure (one persistent CTA per SM, 192 threads):
+// Structure (one persistent CTA per SM, 320 threads):
 //   warp 0     TMA producer: 128x64 tiles of the left operand and bn x 64
 //              tiles of the right operand into a 4-stage shared-memory ring
 //              (128-byte swizzle), completion tracked by mbarrier tx counts;
@@ -13,8 +13,10 @@
 //              tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32,
 //              M = 128, N = bn, K = 16) and commits stage releases and
 //              accumulator-ready signals to mbarriers;
-//   warps 2-5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane
-//              quarter each), the fused polynomial epilogue, bf16 stores.
+//   warps 2-9  epilogue: tcgen05.ld of the fp32 accumulator (a warp may only
+//              read its TMEM lane quarter, warp % 4; two warps share each
+//              quarter and take alternate 32-column blocks), the fused
+//              polynomial epilogue, vectorised bf16/fp32 stores.
 // Two accumulators (2 x 256 columns) let the epilogue of one tile overlap
 // the main loop of the next. X X^T and A A are symmetric: only output tiles
 // that touch the lower triangle are computed and the epilogue mirrors them.
@@ -40,10 +42,12 @@ constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;      // 16 KB
 constexpr int B_STAGE = BN_MAX * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 8;  // two warps per TMEM lane quarter, splitting the columns
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+constexpr int EPI_LD = 33;                                   // padded row of the staging tile
+constexpr int EPI_STAGE_FLOATS = 32 * EPI_LD;                 // one 32x32 fp32 block per warp
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + EPI_WARPS * EPI_STAGE_FLOATS * 4;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 // error codes written to the device flag
@@ -200,6 +204,166 @@ __device__ __forceinline__ TileCoord decode_tile(const TcLaunch& L, int g) {
     c.tj = t;
   }
   return c;
+}
+
+__device__ __forceinline__ void unpack8_bf16(const uint4& w, float* x) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(u[i] << 16);
+    x[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ void store8_bf16(uint16_t* p, const float* x) {
+  uint4 w;
+  w.x = (uint32_t)ns_f2bf(x[0]) | ((uint32_t)ns_f2bf(x[1]) << 16);
+  w.y = (uint32_t)ns_f2bf(x[2]) | ((uint32_t)ns_f2bf(x[3]) << 16);
+  w.z = (uint32_t)ns_f2bf(x[4]) | ((uint32_t)ns_f2bf(x[5]) << 16);
+  w.w = (uint32_t)ns_f2bf(x[6]) | ((uint32_t)ns_f2bf(x[7]) << 16);
+  *reinterpret_cast<uint4*>(p) = w;
+}
+
+// Epilogue of one 32x32 block of the accumulator: rows row0..row0+31 (this
+// warp's TMEM lane quarter), columns col0..col0+31 of matrix `mat`.
+// `r` holds row (row0 + lane) of the block as tcgen05.ld returned it.
+// The block is staged through the warp's shared tile `sb` (fp32, row stride
+// 33: conflict-free both ways). Row phase: lane handles 8 consecutive
+// columns of rows (lane/4) + 8k, so each 16-byte access of 4 lanes covers a
+// contiguous 128-byte row segment. Column phase (one row per lane): the
+// mirrored stores of the symmetric products and the write-back into tall
+// (transposed) parameters, where lanes are contiguous in memory.
+__device__ __forceinline__ void epilogue_block(const NsProblem& pb, const NsEpiArgs& ep, int mat, int row0, int col0,
+                                               uint32_t taddr, float* sb, int lane) {
+  const MuonMat& M = pb.mats[mat];
+  const int s = M.s;
+  const int cc = (lane & 3) * 8;
+  // Issue this block's global loads (the bf16 aux operand and, on the last
+  // Newton-Schulz iteration, the fp32 parameters) before reading TMEM, so
+  // their latency overlaps the TMEM load and the shared-memory staging.
+  uint4 pre[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    pre[k] = make_uint4(0u, 0u, 0u, 0u);
+    const int gi = row0 + (lane >> 2) + 8 * k, gj = col0 + cc;
+    if (pb.kind == NS_UPDATE) {
+      if (gi < s && gj < M.l)
+        pre[k] = __ldg(reinterpret_cast<const uint4*>(pb.aux + (size_t)mat * pb.S * pb.L + (size_t)gi * pb.L + gj));
+    } else if (pb.kind == NS_POLY) {
+      if (gi < s && gj <= gi && gj < s)
+        pre[k] = __ldg(reinterpret_cast<const uint4*>(pb.aux + (size_t)mat * pb.S * pb.S + (size_t)gi * pb.S + gj));
+    }
+  }
+  uint32_t r[32];
+  tmem_ld_32x32b_x32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int e = 0; e < 32; ++e) sb[lane * EPI_LD + e] = __uint_as_float(r[e]);
+  __syncwarp();
+  if (pb.kind == NS_UPDATE) {
+    const int l = M.l;
+    const size_t mbase = (size_t)mat * pb.S * pb.L;
+    const float rs = pb.first ? pb.rscale[mat] : 1.f;
+    const bool apply = pb.last;
+    const bool direct_apply = apply && !M.transposed;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int rr = (lane >> 2) + 8 * k;
+      const int gi = row0 + rr, gj = col0 + cc;
+      float* v = sb + rr * EPI_LD + cc;
+      if (gi < s && gj < l) {
+        const size_t off = mbase + (size_t)gi * pb.L + gj;
+        float x[8], o[8];
+        unpack8_bf16(pre[k], x);  // padding columns of X are zero, so the full vector was readable
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = fmaf(ep.a, x[e], v[e]) * rs;
+        if (!apply) {
+          if (gj + 8 <= l) {
+            store8_bf16(pb.out + off, o);
+          } else {
+            for (int e = 0; e < 8 && gj + e < l; ++e) pb.out[off + e] = ns_f2bf(o[e]);
+          }
+        } else if (direct_apply) {
+          const float lrm = ep.lr * M.lr_mult;
+          float* pp = M.p + (size_t)gi * M.n + gj;
+          if (gj + 8 <= l && M.pvec) {
+            float4 a0 = reinterpret_cast<float4*>(pp)[0], a1 = reinterpret_cast<float4*>(pp)[1];
+            float q[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[e] = fmaf(q[e], ep.decay, -lrm * o[e]);
+            reinterpret_cast<float4*>(pp)[0] = make_float4(q[0], q[1], q[2], q[3]);
+            reinterpret_cast<float4*>(pp)[1] = make_float4(q[4], q[5], q[6], q[7]);
+            if (M.shadow) store8_bf16(M.shadow + (size_t)gi * M.n + gj, q);
+          } else {
+            for (int e = 0; e < 8 && gj + e < l; ++e) {
+              const float q = fmaf(pp[e], ep.decay, -lrm * o[e]);
+              pp[e] = q;
+              if (M.shadow) M.shadow[(size_t)gi * M.n + gj + e] = ns_f2bf(q);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = o[e];  // transposed apply: column phase below
+        }
+      }
+    }
+    if (apply && M.transposed) {
+      __syncwarp();
+      const int gi = row0 + lane;  // canonical row = parameter column
+      if (gi < s) {
+        const float lrm = ep.lr * M.lr_mult;
+        for (int e = 0; e < 32; ++e) {
+          const int gj = col0 + e;  // canonical column = parameter row
+          if (gj >= l) break;
+          const size_t po = (size_t)gj * M.n + gi;
+          const float q = fmaf(M.p[po], ep.decay, -lrm * sb[lane * EPI_LD + e]);
+          M.p[po] = q;
+          if (M.shadow) M.shadow[po] = ns_f2bf(q);
+        }
+      }
+    }
+  } else {
+    // GRAM / POLY: symmetric s x s output, lower triangle computed, mirrored
+    const size_t mbase = (size_t)mat * pb.S * pb.S;
+    const float sc = pb.kind == NS_GRAM ? (pb.first ? pb.rscale[mat] * pb.rscale[mat] : 1.f) : 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int rr = (lane >> 2) + 8 * k;
+      const int gi = row0 + rr, gj = col0 + cc;
+      float* v = sb + rr * EPI_LD + cc;
+      if (gi < s && gj <= gi && gj < s) {
+        const size_t off = mbase + (size_t)gi * pb.S + gj;
+        float o[8];
+        if (pb.kind == NS_GRAM) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = v[e] * sc;
+        } else {
+          float a[8];
+          unpack8_bf16(pre[k], a);  // A is stored in full (mirrored), padding zero
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = fmaf(ep.c, v[e], ep.b * a[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = o[e];
+        if (gj + 7 <= gi && gj + 8 <= s) {
+          store8_bf16(pb.out + off, o);
+        } else {
+          for (int e = 0; e < 8 && gj + e <= gi && gj + e < s; ++e) pb.out[off + e] = ns_f2bf(o[e]);
+        }
+      }
+    }
+    __syncwarp();
+    // mirror: out[j][i] = out[i][j] for j < i; lanes hold consecutive i
+    const int gi = row0 + lane;
+    if (gi < s) {
+      for (int e = 0; e < 32; ++e) {
+        const int gj = col0 + e;
+        if (gj >= gi) break;
+        pb.out[mbase + (size_t)gj * pb.S + gi] = ns_f2bf(sb[lane * EPI_LD + e]);
+      }
+    }
+  }
+  __syncwarp();
 }
 
 __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant__ TcLaunch L) {
@@ -363,8 +527,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
     }
   } else {
     // ---------------- epilogue ----------------
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. 32*quarter+31
-    const int row = quarter * 32 + lane;
+    const int quarter = warp & 3;      // TMEM lanes 32*quarter .. 32*quarter+31
+    const int half = (warp - 2) >> 2;  // which alternate 32-column blocks
+    float* sb = reinterpret_cast<float*>(smem + (size_t)STAGES * STAGE_BYTES + 256) + (warp - 2) * EPI_STAGE_FLOATS;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int g = blockIdx.x; g < L.total_tiles; g += gridDim.x) {
@@ -374,16 +539,10 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       const bool got = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, L.err, kErrWaitEpilogue);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      const int i = c.ti * BM + row;
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN_MAX);
-      for (int c0 = 0; c0 < P.bn; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
-        tmem_ld_wait();
-        const int j0 = c.tj * P.bn + c0;
-#pragma unroll 4
-        for (int e = 0; e < 32; ++e) ns_epilogue_element(P.p, L.epi, c.mat, i, j0 + e, __uint_as_float(r[e]));
-      }
+      const int row0 = c.ti * BM + quarter * 32;
+      for (int c0 = 32 * half; c0 < P.bn; c0 += 64)
+        epilogue_block(P.p, L.epi, c.mat, row0, c.tj * P.bn + c0, tbase + (uint32_t)c0, sb, lane);
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
       if (++acc == 2) {

@@ -46,6 +46,11 @@ struct Kahan {
   __device__ __forceinline__ void add(float x) {
     float y = x - c;
     float t = s + y;
+    if (__builtin_expect(isinf(t), 0)) {  // inf - inf in the compensation would turn it into NaN
+      s = t;
+      c = 0.f;
+      return;
+    }
     c = (t - s) - y;
     s = t;
   }

@@ -102,7 +102,7 @@ def test_config_defaults_match_page(mx):
     page = json.load(open(os.path.join(GOLDEN, "hparams_page.json")))
     spec = json.load(open(os.path.join(GOLDEN, "hparams_workload.json")))
     c = mx.muon_adamw_config_init()
-    f32 = lambda x: float(ctypes.c_float(x).value)  # noqa: E731
+    f32 = float
     assert c.muon_momentum == f32(page["muon_momentum"]["value"])
     assert bool(c.muon_nesterov) == page["muon_nesterov"]["value"]
     assert c.ns_steps == page["muon_ns_steps"]["value"]
@@ -119,7 +119,7 @@ def test_null_handle_calls_return_errors(mx):
     lib = mx.load_library()
     assert lib.muon_adamw_destroy(None) == mx.MA_ERR_ARG
     assert "NULL" in mx.muon_adamw_last_error()
-    assert lib.muon_adamw_step(None, ctypes.c_float(1e-3), None) == mx.MA_ERR_ARG
+    assert lib.muon_adamw_step(None, 1e-3, None) == mx.MA_ERR_ARG
     assert lib.muon_adamw_sync(None) == mx.MA_ERR_ARG
     assert lib.muon_adamw_set_profiling(None, 1) == mx.MA_ERR_ARG
     assert lib.muon_adamw_register_param(None, b"x", 0, None, None, None, 0, None, 0, None, None) == mx.MA_ERR_ARG

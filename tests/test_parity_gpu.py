@@ -1,0 +1,315 @@
+"""GPU parity of the CUDA optimizer step against the fp64 oracle (via the C ABI).
+
+Tolerances are those of ``tests/harness.py``: norm 1e-5 relative; AdamW
+p/m/v and Muon momentum 1e-6 relative to the magnitude of their terms;
+orthogonalised update 2e-2 relative Frobenius per matrix.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import workloads
+from harness import O_TOL, GpuSide, relative_frobenius, run_parity
+from workloads import TensorSpec
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mx():
+    from muon_adamw_hybrid_grad_gb300 import build
+
+    build.build()
+    import muon_adamw_hybrid_grad_gb300 as m
+
+    m.load_library()
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+KERNELS = [0, 1]  # MA_NS_TCGEN05, MA_NS_SIMT
+KNAMES = {0: "tcgen05", 1: "simt"}
+
+
+@pytest.mark.parametrize("ns_kernel", KERNELS, ids=lambda k: KNAMES[k])
+@pytest.mark.parametrize("policy", ["fp32_mixed", "bf16_mixed"])
+def test_tiny_three_steps(mx, ns_kernel, policy):
+    w = workloads.get_workload("tiny")
+    w = workloads.custom_workload("tiny", w.tensors, policy=policy, steps=3)
+    r = run_parity(w, config={"ns_kernel": ns_kernel})
+    assert r["worst_o"] <= O_TOL
+
+
+def _many_small_reduced():
+    lens = workloads.many_small_lengths()[:256]
+    t = [TensorSpec(f"model.action_expert.layers.{k}.w_a.weight", (128, 512)) for k in range(64)]
+    t += [TensorSpec(f"model.action_expert.layers.{64 + k}.w_b.weight", (512, 128)) for k in range(32)]
+    t += [TensorSpec(f"model.vlm.layers.{k}.ln.weight", (int(n),)) for k, n in enumerate(lens)]
+    return workloads.custom_workload("many_small_reduced", t, policy="fp32_mixed", steps=2)
+
+
+@pytest.mark.parametrize("ns_kernel", KERNELS, ids=lambda k: KNAMES[k])
+def test_many_small_mixed_orientation(mx, ns_kernel):
+    r = run_parity(_many_small_reduced(), config={"ns_kernel": ns_kernel})
+    assert r["worst_o"] <= O_TOL
+
+
+def _ragged():
+    shapes = [(100, 300), (300, 100), (37, 53), (53, 37), (1, 129), (129, 1), (200, 200), (640, 384),
+              (384, 640), (130, 258), (8, 8)]
+    t = [TensorSpec(f"model.action_expert.layers.{k}.mlp.w{k}.weight", s) for k, s in enumerate(shapes)]
+    t += [TensorSpec(f"model.vlm.v{k}.weight", (n,)) for k, n in enumerate((1, 7, 65535, 65537, 131073))]
+    t += [TensorSpec("model.vlm.mat.weight", (33, 65))]
+    return workloads.custom_workload("ragged", t, policy="bf16_mixed", steps=2)
+
+
+@pytest.mark.parametrize("ns_kernel", KERNELS, ids=lambda k: KNAMES[k])
+def test_ragged_shapes_and_chunk_tails(mx, ns_kernel):
+    r = run_parity(_ragged(), config={"ns_kernel": ns_kernel})
+    assert r["worst_o"] <= O_TOL
+
+
+def test_fp32_gradients(mx):
+    w = workloads.get_workload("tiny")
+    w = workloads.custom_workload("tiny_fp32g", w.tensors, grad_dtype="fp32", policy="fp32_mixed", steps=2)
+    run_parity(w)
+
+
+def test_h1024_full_size_sampled(mx):
+    """The benchmark workload at full size (16 layers, 268 M Muon elements):
+    every momentum and AdamW element checked; O checked on layers 0, 8, 15
+    for every shape (1024x1024, 4096x1024, 1024x4096)."""
+    w = workloads.get_workload("h1024")
+    per_layer = 7
+    sample = [layer * per_layer + k for layer in (0, 8, 15) for k in (0, 4, 6)]
+    r = run_parity(w, steps=2, muon_sample=sample)
+    assert r["worst_o"] <= O_TOL
+
+
+def test_zero_gradients(mx):
+    w = workloads.get_workload("tiny")
+    run_parity(w, steps=2, grad_scale=0.0)
+
+
+def test_large_gradients_clip(mx):
+    # grads scaled by 1e3: the clip coefficient is far below 1
+    w = workloads.get_workload("tiny")
+    run_parity(w, steps=2, grad_scale=1e3)
+
+
+def test_clipping_disabled(mx):
+    w = workloads.get_workload("tiny")
+    run_parity(w, steps=2, config={"max_grad_norm": 0.0}, oracle_overrides={"max_grad_norm": 0.0})
+
+
+def test_adamw_only_mode(mx):
+    w = workloads.get_workload("tiny")
+    r = run_parity(w, steps=2, config={"mode": mx.MA_MODE_ADAMW_ONLY}, optim="adamw")
+    assert set(r["groups"]) == {"adamw"}
+
+
+@pytest.mark.parametrize("steps_ns", [1, 2, 3])
+@pytest.mark.parametrize("ns_kernel", KERNELS, ids=lambda k: KNAMES[k])
+def test_other_newton_schulz_step_counts(mx, steps_ns, ns_kernel):
+    w = workloads.get_workload("tiny")
+    run_parity(w, steps=2, config={"ns_steps": steps_ns, "ns_kernel": ns_kernel},
+               oracle_overrides={"muon_ns_steps": steps_ns})
+
+
+def test_frozen_and_empty_parameters(mx):
+    t = [TensorSpec("model.action_expert.layers.0.q.weight", (256, 512)),
+         TensorSpec("model.vlm.embed_tokens.weight", (500, 64), frozen=True),
+         TensorSpec("model.action_expert.layers.0.k.weight", (0, 64)),
+         TensorSpec("model.vlm.empty.bias", (0,)),
+         TensorSpec("model.vlm.ln.weight", (64,))]
+    w = workloads.custom_workload("frozen", t, policy="bf16_mixed", steps=2)
+    r = run_parity(w)
+    assert r["groups"] == ["muon", "frozen", "muon", "adamw", "adamw"]
+
+
+def test_nan_gradient_propagates(mx):
+    import torch
+
+    w = workloads.get_workload("tiny")
+    masters = workloads.master_weights(w)
+    gpu = GpuSide(w, masters)
+    try:
+        grads = workloads.gradients(w, 1)
+        grads[0] = grads[0].copy()
+        grads[0][3, 5] = np.nan
+        gpu.load_grads(grads)
+        total = gpu.step(w.lr)
+        assert math.isnan(total)
+        for i in range(len(w.tensors)):
+            assert torch.isnan(gpu.P[i]).all(), w.tensors[i].name
+    finally:
+        gpu.close()
+
+
+def test_inf_gradient_zero_clip(mx):
+    w = workloads.get_workload("tiny")
+    masters = workloads.master_weights(w)
+    gpu = GpuSide(w, masters)
+    try:
+        grads = workloads.gradients(w, 1)
+        # an infinite entry in an AdamW tensor: norm inf, clip factor 0
+        idx = len(w.tensors) - 1
+        grads[idx] = grads[idx].copy()
+        grads[idx][0, 0] = np.inf
+        gpu.load_grads(grads)
+        assert gpu.step(w.lr) == math.inf
+        total, coef = gpu.mx.muon_adamw_last_norm(gpu.opt.handle)
+        assert coef == 0.0
+        # a finite Muon matrix gets a zero direction: O = 0, pure decay
+        p0 = masters[0].astype(np.float64)
+        decay = float(np.float32(1.0 - w.lr * 0.1))
+        assert np.allclose(gpu.param(0), p0 * decay, rtol=1e-7, atol=0)
+    finally:
+        gpu.close()
+
+
+def test_deterministic(mx):
+    w = _many_small_reduced()
+    outs = []
+    for _ in range(2):
+        masters = workloads.master_weights(w)
+        gpu = GpuSide(w, masters)
+        try:
+            for s in (1, 2):
+                gpu.load_grads(workloads.gradients(w, s))
+                gpu.step(w.lr)
+            outs.append([gpu.param(i) for i in range(len(w.tensors))])
+        finally:
+            gpu.close()
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+
+
+def test_tcgen05_matches_simt_kernel(mx):
+    """Same inputs through the tensor-core and the CUDA-core GEMM: both are
+    bf16-in/fp32-accumulate, so their O agree far more closely than either
+    agrees with the fp64 oracle."""
+    w = workloads.scaled_workload("mid", layers=2, hidden=512, mlp=1536)
+    res = []
+    for k in KERNELS:
+        masters = workloads.master_weights(w)
+        gpu = GpuSide(w, masters, config={"ns_kernel": k})
+        try:
+            gpu.load_grads(workloads.gradients(w, 1))
+            gpu.step(w.lr)
+            res.append([gpu.param(i).astype(np.float64) - masters[i] for i in range(len(w.tensors))])
+        finally:
+            gpu.close()
+    for i, t in enumerate(w.tensors):
+        if len(t.shape) == 2:
+            assert relative_frobenius(res[0][i], res[1][i]) < 5e-3, t.name
+
+
+def test_checkpoint_roundtrip_bitwise(mx):
+    """get_state/set_state/set_step resume: a restored optimizer continues
+    bit for bit like the original."""
+    import torch
+
+    w = _many_small_reduced()
+    masters = workloads.master_weights(w)
+    a = GpuSide(w, masters)
+    try:
+        for s in (1, 2):
+            a.load_grads(workloads.gradients(w, s))
+            a.step(w.lr)
+        snap_p = [a.param(i) for i in range(len(w.tensors))]
+        b = GpuSide(w, snap_p)
+        try:
+            for i, grp in enumerate(a.opt.groups):
+                if grp == "muon":
+                    b.opt.set_state(i, 0, a.opt.state(i, 0))
+                elif grp == "adamw":
+                    b.opt.set_state(i, 0, a.opt.state(i, 0))
+                    b.opt.set_state(i, 1, a.opt.state(i, 1))
+            mxm = a.mx
+            mxm.muon_adamw_set_step(b.opt.handle, mxm.muon_adamw_get_step(a.opt.handle))
+            g3 = workloads.gradients(w, 3)
+            a.load_grads(g3)
+            b.load_grads(g3)
+            a.step(w.lr)
+            b.step(w.lr)
+            for i in range(len(w.tensors)):
+                assert np.array_equal(a.param(i), b.param(i)), w.tensors[i].name
+        finally:
+            b.close()
+    finally:
+        a.close()
+
+
+def test_error_paths(mx):
+    import torch
+
+    dev = torch.device("cuda")
+    cfg = mx.muon_adamw_config_init()
+    h = mx.muon_adamw_create(cfg, torch.cuda.current_stream().cuda_stream)
+    try:
+        p = torch.zeros(64, 64, device=dev)
+        g = torch.zeros(64, 64, device=dev, dtype=torch.bfloat16)
+        with pytest.raises(mx.MuonAdamWError) as e:
+            mx.muon_adamw_register_param(h, "x.weight", (64, 64), p.data_ptr(), g.data_ptr(), 7)
+        assert e.value.status == mx.MA_ERR_DTYPE
+        with pytest.raises(mx.MuonAdamWError) as e:
+            mx.muon_adamw_register_param(h, "x.weight", (64, 64), p.data_ptr(), g.data_ptr() + 1, mx.MA_DT_BF16)
+        assert e.value.status == mx.MA_ERR_ALIGN
+        with pytest.raises(mx.MuonAdamWError) as e:
+            mx.muon_adamw_register_param(h, "v", (64,), p.data_ptr(), g.data_ptr(), mx.MA_DT_BF16, 0,
+                                         mx.MA_GROUP_MUON)
+        assert e.value.status == mx.MA_ERR_SHAPE
+        with pytest.raises(mx.MuonAdamWError) as e:
+            mx.muon_adamw_register_param(h, "x.weight", (64, 64), 0, g.data_ptr(), mx.MA_DT_BF16)
+        assert e.value.status == mx.MA_ERR_ARG
+        with pytest.raises(mx.MuonAdamWError) as e:
+            mx.muon_adamw_plan_info(h)
+        assert e.value.status == mx.MA_ERR_STATE
+        idx, grp = mx.muon_adamw_register_param(h, "model.action_expert.layers.0.q.weight", (64, 64),
+                                                p.data_ptr(), g.data_ptr(), mx.MA_DT_BF16)
+        assert (idx, grp) == (0, mx.MA_GROUP_MUON)
+        out = torch.empty(64, 64)
+        with pytest.raises(mx.MuonAdamWError) as e:
+            mx.muon_adamw_get_state(h, 0, 0, out.data_ptr())
+        assert e.value.status == mx.MA_ERR_STATE
+        with pytest.raises(mx.MuonAdamWError) as e:
+            mx.muon_adamw_step(h, float("nan"))
+        assert e.value.status == mx.MA_ERR_ARG
+        assert mx.muon_adamw_step(h, 1e-3, want_norm=True) == 0.0
+        with pytest.raises(mx.MuonAdamWError) as e:
+            mx.muon_adamw_register_param(h, "late.weight", (64, 64), p.data_ptr(), g.data_ptr(), mx.MA_DT_BF16)
+        assert e.value.status == mx.MA_ERR_STATE
+        with pytest.raises(mx.MuonAdamWError) as e:
+            mx.muon_adamw_get_state(h, 0, 1, out.data_ptr())  # Muon has no second moment
+        assert e.value.status == mx.MA_ERR_ARG
+        with pytest.raises(mx.MuonAdamWError) as e:
+            mx.muon_adamw_get_state(h, 5, 0, out.data_ptr())
+        assert e.value.status == mx.MA_ERR_ARG
+        mx.muon_adamw_sync(h)
+        info = mx.muon_adamw_plan_info(h)
+        assert info.n_muon == 1 and info.n_buckets == 1
+    finally:
+        mx.muon_adamw_destroy(h)
+
+
+def test_profiling_counts_launches(mx):
+    w = workloads.get_workload("tiny")
+    masters = workloads.master_weights(w)
+    gpu = GpuSide(w, masters)
+    try:
+        gpu.load_grads(workloads.gradients(w, 1))
+        gpu.mx.muon_adamw_set_profiling(gpu.opt.handle, True)
+        gpu.step(w.lr)
+        gpu.step(w.lr)
+        prof = gpu.opt.profile()
+        assert prof["steps"] == 2
+        assert prof["ns_gram"]["launches"] == 2 * 5
+        assert prof["adamw"]["launches"] == 2 and prof["momentum"]["launches"] == 2
+        for k in ("grad_norm", "momentum", "ns_gram", "ns_poly", "ns_update", "adamw"):
+            assert prof[k]["ms"] > 0 and prof[k]["units"] > 0
+    finally:
+        gpu.close()
