@@ -238,6 +238,39 @@ MA_API ma_status muon_adamw_reset_profile(muon_adamw_t* h);
  * and the handle. Caller memory is not touched. h == NULL is MA_ERR_ARG. */
 MA_API ma_status muon_adamw_destroy(muon_adamw_t* h);
 
+/* ---- Allocation-free gradient norm ----
+ * The article has no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc, such as a host that gives all device memory
+ * to its own pool allocator at start-up and forbids later allocations, or a
+ * latency-critical loop that cannot accept cudaMalloc's implicit device-wide
+ * synchronisation. It computes the same global gradient norm and clip
+ * coefficient as muon_adamw_step(), without a handle and without allocating:
+ * its scratch is a fixed file-scope device array of MA_NOALLOC_MAX_PARTIALS
+ * floats (4 KiB) that every GPU loading this library keeps until the process
+ * exits, and the tensor list travels in the kernel's parameters.
+ *
+ *   grads, numels, dtypes  host arrays of n_tensors entries: device pointer,
+ *                          element count, MA_DT_F32 or MA_DT_BF16;
+ *   n_tensors              0 .. MA_NOALLOC_MAX_TENSORS; more is MA_ERR_ARG;
+ *   max_norm, clip_eps     clip = min(1, max_norm / (norm + clip_eps));
+ *                          max_norm <= 0 gives 1; a NaN norm gives NaN;
+ *   out_total_coef         device pointer to 2 floats: [0] norm, [1] clip;
+ *   cuda_stream            cudaStream_t on the current device (NULL = default).
+ * Work is queued on the stream; the call does not wait for it. The first call
+ * on a device also looks up the scratch array's device address for that
+ * device (cudaGetSymbolAddress), so make that first call before any stream
+ * capture. All calls share the one scratch array, which keeps the last call's
+ * partial sums; each call rewrites every slot it reads, so nothing needs
+ * clearing, but calls whose work overlaps on the GPU (different streams, or
+ * host threads racing on one device) corrupt each other's partial sums:
+ * order them on one stream. Errors: MA_ERR_ARG, MA_ERR_SHAPE, MA_ERR_DTYPE,
+ * MA_ERR_ALIGN, MA_ERR_CUDA; no allocation is attempted on any path. */
+#define MA_NOALLOC_MAX_TENSORS 64
+#define MA_NOALLOC_MAX_PARTIALS 1024
+MA_API ma_status muon_adamw_grad_norm_noalloc(const void* const* grads, const int64_t* numels,
+                                              const int32_t* dtypes, int n_tensors, double max_norm,
+                                              double clip_eps, float* out_total_coef, void* cuda_stream);
+
 /* Message of the last error on this thread ("" if none). Never NULL. */
 MA_API const char* muon_adamw_last_error(void);
 

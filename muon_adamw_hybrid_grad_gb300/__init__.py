@@ -135,6 +135,9 @@ _SIGNATURES = {
     "muon_adamw_get_profile": (ctypes.c_int, [_P, ctypes.POINTER(Profile)]),
     "muon_adamw_reset_profile": (ctypes.c_int, [_P]),
     "muon_adamw_destroy": (ctypes.c_int, [_P]),
+    "muon_adamw_grad_norm_noalloc": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_int64),
+                                                    ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_double,
+                                                    ctypes.c_double, _P, _P]),
     "muon_adamw_last_error": (ctypes.c_char_p, []),
     "muon_adamw_version": (ctypes.c_char_p, []),
 }
@@ -263,6 +266,20 @@ def muon_adamw_reset_profile(h: int) -> None:
 
 def muon_adamw_destroy(h: int) -> None:
     _check(load_library().muon_adamw_destroy(_P(h)))
+
+
+MA_NOALLOC_MAX_TENSORS = 64
+
+
+def muon_adamw_grad_norm_noalloc(grad_ptrs: Sequence[int], numels: Sequence[int], dtypes: Sequence[int],
+                                 max_norm: float, clip_eps: float, out_ptr: int, cuda_stream: int = 0) -> None:
+    """Allocation-free global norm + clip factor into 2 device floats at out_ptr."""
+    n = len(grad_ptrs)
+    ptrs = (_P * max(1, n))(*[_P(p or None) for p in grad_ptrs])
+    nums = (ctypes.c_int64 * max(1, n))(*[int(x) for x in numels])
+    dts = (ctypes.c_int32 * max(1, n))(*[int(x) for x in dtypes])
+    _check(load_library().muon_adamw_grad_norm_noalloc(ptrs, nums, dts, n, float(max_norm), float(clip_eps),
+                                                       _P(out_ptr), _P(cuda_stream or None)))
 
 
 def muon_adamw_last_error() -> str:

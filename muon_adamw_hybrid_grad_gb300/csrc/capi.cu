@@ -111,6 +111,11 @@ struct ProfRec {
 
 }  // namespace
 
+namespace ma {
+void set_last_error(const char* msg) { g_last_error = msg; }
+void clear_last_error() { g_last_error.clear(); }
+}  // namespace ma
+
 struct muon_adamw {
   muon_adamw_config cfg{};
   int device = 0;

@@ -103,6 +103,10 @@ struct NsProblem {
   int32_t first, last;  // first / last Newton-Schulz iteration
 };
 
+// ---- the thread-local message behind muon_adamw_last_error() (capi.cu) ----
+void set_last_error(const char* msg);
+void clear_last_error();
+
 // ---- launchers (stream_kernels.cu) ----
 void launch_grad_sumsq(const GradChunk* chunks, int nchunks, float* partials, int grid, cudaStream_t st);
 void launch_clip_finalize(const float* partials, int n, float max_norm, float clip_eps, StepScalars* out,
