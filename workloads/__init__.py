@@ -190,10 +190,17 @@ WORKLOADS = tuple(_BUILDERS)
 
 
 def get_workload(name: str) -> Workload:
+    """A named workload, or ``expert:<hidden>:<mlp>:<layers>`` for an action
+    expert of that size built like h1024 (bf16 grads with the rank-8 part,
+    bf16_mixed policy)."""
+    if name.startswith("expert:"):
+        hidden, mlp, layers = (int(x) for x in name.split(":")[1:4])
+        t = _expert_layers(hidden, mlp, layers, rank8=True) + _expert_vectors(hidden, layers)
+        return Workload(name, tuple(t), policy="bf16_mixed", grad_dtype="bf16", steps=10, lr=BASE_LR)
     try:
         return _BUILDERS[name]()
     except KeyError:
-        raise KeyError(f"unknown workload {name!r}; known: {', '.join(WORKLOADS)}") from None
+        raise KeyError(f"unknown workload {name!r}; known: {', '.join(WORKLOADS)} or expert:H:M:L") from None
 
 
 def scaled_workload(name: str, *, layers: int, hidden: int, mlp: int, vectors: bool = True) -> Workload:
