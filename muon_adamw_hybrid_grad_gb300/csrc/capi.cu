@@ -23,7 +23,7 @@
 #include <utility>
 #include <vector>
 
-#include "../../include/muon_adamw.h"
+#include "muon_adamw.h"
 #include "internal.h"
 
 using namespace ma;
@@ -268,19 +268,16 @@ ma_status build_plan(muon_adamw* h) {
     off += al(h->params[pi].numel * sizeof(float));
   }
   h->state_bytes = off;
+  // per bucket: X ping, X pong (s x l), A, B (s x s), all bf16
   std::vector<size_t> ws_off(h->buckets.size() * 4);
   for (size_t b = 0; b < h->buckets.size(); ++b) {
     const Bucket& B = h->buckets[b];
     const size_t nb = B.params.size();
     const size_t xs = al(nb * (size_t)B.S * B.L * 2), as = al(nb * (size_t)B.S * B.S * 2);
-    ws_off[4 * b + 0] = off;
-    off += xs;
-    ws_off[4 * b + 1] = off;
-    off += xs;
-    ws_off[4 * b + 2] = off;
-    off += as;
-    ws_off[4 * b + 3] = off;
-    off += as;
+    for (int q = 0; q < 4; ++q) {
+      ws_off[4 * b + q] = off;
+      off += q < 2 ? xs : as;
+    }
   }
   h->workspace_bytes = off - h->state_bytes;
 
@@ -486,7 +483,7 @@ ma_status build_plan(muon_adamw* h) {
         } else {
           p.P = B.B;
           p.Q = Xcur;
-          p.aux = Xcur;
+          p.aux = nullptr;
           p.out = Xnext;
           p.M = B.S;
           p.N = B.L;

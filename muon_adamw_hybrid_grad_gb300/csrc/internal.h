@@ -85,15 +85,19 @@ struct NsEpiArgs {
   float lr;
 };
 
-// One grouped GEMM problem: all same-shape matrices of one bucket.
-//   GRAM:   out[S][S] = X X^T          (P = Q = X, K = L)      symmetric
-//   POLY:   out[S][S] = b A + c A A    (P = Q = A, K = S)      symmetric
-//   UPDATE: out[S][L] = a X + B X      (P = B, Q = X MN-major, K = S)
+// One grouped GEMM problem: all same-shape matrices of one bucket. The
+// quintic step X <- a X + (b A + c A A) X is evaluated as
+//   GRAM:   A = X X^T                     (P = Q = X, K = L)         symmetric
+//   POLY:   B = a I + b A + c A A         (P = Q = A, K = S)         symmetric
+//   UPDATE: X' = B X                      (P = B, Q = X MN-major, K = S)
+// so that the largest product's epilogue reads nothing back; only POLY
+// reads A for its b A term. Iteration 1 scales A by r^2 and X' by r, with
+// r = 1 / (||update||_F + eps).
 struct NsProblem {
   const uint16_t* P;
   const uint16_t* Q;
-  const uint16_t* aux;  // POLY: A; UPDATE: X
-  uint16_t* out;
+  const uint16_t* aux;  // POLY: A; otherwise unused
+  uint16_t* out;        // GRAM: A; POLY: B; UPDATE: X'
   const MuonMat* mats;  // this bucket's matrices
   const float* rscale;  // per matrix 1 / (||update||_F + eps), same indexing
   int32_t kind;

@@ -20,7 +20,7 @@
 #include <atomic>
 #include <mutex>
 
-#include "../../include/muon_adamw.h"
+#include "muon_adamw.h"
 #include "internal.h"
 
 // The scratch: one fp32 partial sum of squares per block of the reduction.

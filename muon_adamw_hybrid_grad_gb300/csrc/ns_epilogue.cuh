@@ -3,10 +3,14 @@
 // Newton-Schulz as described in the OpenDM article (核心揭秘一 / Muon 的工作原理):
 // five iterations of  A = X X^T,  B = b A + c A A,  X <- a X + B X,  on the
 // short side of the update, starting from X0 = update / (||update||_F + eps).
-// The normalisation is folded in: X0 is stored unscaled (U) and r = 1/(||U||+eps)
-// is applied as r^2 to the first Gram matrix and r to the first X update.
-// The last update does not store X: it applies the Muon step to the fp32
-// master weights (transposing back for tall matrices):
+// The factor a is folded into B (B = a I + b A + c A A), so the update is
+// the plain product X' = B X and its epilogue reads nothing back; the bf16
+// rounding points stay those of the textbook order (X, A and B stored in
+// bf16), which keeps the error of the original evaluation. The
+// normalisation is folded in too: X0 is stored unscaled (U) and
+// r = 1/(||U||+eps) is applied as r^2 to the first Gram matrix and r to the
+// first X update. The last update does not store X: it applies the Muon
+// step to the fp32 master weights (transposing back for tall matrices):
 //   p <- p * (1 - lr * wd) - lr * muon_lr_scale * 0.2 * sqrt(max(m, n)) * O.
 // Padding rows/cols of the workspaces are never written, so they stay zero.
 #pragma once
@@ -36,7 +40,7 @@ __device__ __forceinline__ void ns_epilogue_element(const NsProblem& pb, const N
       const float r = pb.first ? pb.rscale[mat] : 1.f;
       v = acc * (r * r);
     } else {
-      v = fmaf(ep.c, acc, ep.b * ns_bf2f(pb.aux[base + (size_t)i * pb.S + j]));
+      v = fmaf(ep.c, acc, fmaf(ep.b, ns_bf2f(pb.aux[base + (size_t)i * pb.S + j]), i == j ? ep.a : 0.f));
     }
     const uint16_t h = ns_f2bf(v);
     pb.out[base + (size_t)i * pb.S + j] = h;
@@ -46,8 +50,7 @@ __device__ __forceinline__ void ns_epilogue_element(const NsProblem& pb, const N
   // NS_UPDATE
   if (i >= M.s || j >= M.l) return;
   const size_t idx = (size_t)mat * pb.S * pb.L + (size_t)i * pb.L + j;
-  float v = fmaf(ep.a, ns_bf2f(pb.aux[idx]), acc);
-  if (pb.first) v *= pb.rscale[mat];
+  const float v = pb.first ? acc * pb.rscale[mat] : acc;
   if (!pb.last) {
     pb.out[idx] = ns_f2bf(v);
     return;

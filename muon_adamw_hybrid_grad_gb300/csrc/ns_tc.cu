@@ -2,8 +2,10 @@
 //
 // Newton-Schulz orthogonalisation as described in the OpenDM article
 // (核心揭秘一 / Muon 的工作原理): A = X X^T, B = b A + c A A, X <- a X + B X,
-// five times, on the short side. Each launch covers one of the three
-// products for every Muon matrix of up to four shape buckets.
+// five times, on the short side, evaluated as A = X X^T, B = a I + b A + c A A,
+// X' = B X so that the largest product's epilogue reads nothing back. Each
+// launch covers one of the three products for every Muon matrix of up to
+// four shape buckets.
 //
 // Structure (one persistent CTA per SM, 320 threads):
 //   warp 0     TMA producer: 128x64 tiles of the left operand and bn x 64
@@ -206,15 +208,6 @@ __device__ __forceinline__ TileCoord decode_tile(const TcLaunch& L, int g) {
   return c;
 }
 
-__device__ __forceinline__ void unpack8_bf16(const uint4& w, float* x) {
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = __uint_as_float(u[i] << 16);
-    x[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-  }
-}
-
 __device__ __forceinline__ void store8_bf16(uint16_t* p, const float* x) {
   uint4 w;
   w.x = (uint32_t)ns_f2bf(x[0]) | ((uint32_t)ns_f2bf(x[1]) << 16);
@@ -225,33 +218,43 @@ __device__ __forceinline__ void store8_bf16(uint16_t* p, const float* x) {
 }
 
 // Epilogue of one 32x32 block of the accumulator: rows row0..row0+31 (this
-// warp's TMEM lane quarter), columns col0..col0+31 of matrix `mat`.
-// `r` holds row (row0 + lane) of the block as tcgen05.ld returned it.
-// The block is staged through the warp's shared tile `sb` (fp32, row stride
-// 33: conflict-free both ways). Row phase: lane handles 8 consecutive
-// columns of rows (lane/4) + 8k, so each 16-byte access of 4 lanes covers a
-// contiguous 128-byte row segment. Column phase (one row per lane): the
-// mirrored stores of the symmetric products and the write-back into tall
-// (transposed) parameters, where lanes are contiguous in memory.
+// warp's TMEM lane quarter), columns col0..col0+31 of matrix `mat`. The
+// block goes through the warp's shared tile `sb` (fp32, row stride 33:
+// conflict-free both ways). Row phase: a lane handles 8 consecutive columns
+// of rows (lane/4) + 8k, so each 16-byte access of 4 lanes covers a
+// contiguous row segment. Column phase (one row per lane): the mirrored
+// stores of the symmetric products and the write-back into tall
+// (transposed) parameters, where lanes are contiguous in memory. Only the
+// b A term of B and the last iteration's parameters are read from memory.
 __device__ __forceinline__ void epilogue_block(const NsProblem& pb, const NsEpiArgs& ep, int mat, int row0, int col0,
                                                uint32_t taddr, float* sb, int lane) {
   const MuonMat& M = pb.mats[mat];
   const int s = M.s;
   const int cc = (lane & 3) * 8;
-  // Issue this block's global loads (the bf16 aux operand and, on the last
-  // Newton-Schulz iteration, the fp32 parameters) before reading TMEM, so
-  // their latency overlaps the TMEM load and the shared-memory staging.
-  uint4 pre[4];
+  const bool direct_apply = pb.kind == NS_UPDATE && pb.last && !M.transposed;
+  // Global loads are issued before TMEM is read so that their latency
+  // overlaps the TMEM load and the shared-memory staging.
+  uint4 preA[4];
+  if (pb.kind == NS_POLY) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    pre[k] = make_uint4(0u, 0u, 0u, 0u);
-    const int gi = row0 + (lane >> 2) + 8 * k, gj = col0 + cc;
-    if (pb.kind == NS_UPDATE) {
-      if (gi < s && gj < M.l)
-        pre[k] = __ldg(reinterpret_cast<const uint4*>(pb.aux + (size_t)mat * pb.S * pb.L + (size_t)gi * pb.L + gj));
-    } else if (pb.kind == NS_POLY) {
-      if (gi < s && gj <= gi && gj < s)
-        pre[k] = __ldg(reinterpret_cast<const uint4*>(pb.aux + (size_t)mat * pb.S * pb.S + (size_t)gi * pb.S + gj));
+    for (int k = 0; k < 4; ++k) {
+      const int gi = row0 + (lane >> 2) + 8 * k, gj = col0 + cc;
+      preA[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (gi < s && gj <= gi && gj < s)  // A is stored in full (mirrored); padding is zero
+        preA[k] = __ldg(reinterpret_cast<const uint4*>(pb.aux + (size_t)mat * pb.S * pb.S + (size_t)gi * pb.S + gj));
+    }
+  }
+  float4 pre[4][2];
+  if (direct_apply) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int gi = row0 + (lane >> 2) + 8 * k, gj = col0 + cc;
+      pre[k][0] = pre[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (gi < s && gj + 8 <= M.l && M.pvec) {
+        const float4* pp = reinterpret_cast<const float4*>(M.p + (size_t)gi * M.n + gj);
+        pre[k][0] = pp[0];
+        pre[k][1] = pp[1];
+      }
     }
   }
   uint32_t r[32];
@@ -264,31 +267,28 @@ __device__ __forceinline__ void epilogue_block(const NsProblem& pb, const NsEpiA
     const int l = M.l;
     const size_t mbase = (size_t)mat * pb.S * pb.L;
     const float rs = pb.first ? pb.rscale[mat] : 1.f;
-    const bool apply = pb.last;
-    const bool direct_apply = apply && !M.transposed;
+    const float lrm = ep.lr * M.lr_mult;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int rr = (lane >> 2) + 8 * k;
       const int gi = row0 + rr, gj = col0 + cc;
       float* v = sb + rr * EPI_LD + cc;
       if (gi < s && gj < l) {
-        const size_t off = mbase + (size_t)gi * pb.L + gj;
-        float x[8], o[8];
-        unpack8_bf16(pre[k], x);  // padding columns of X are zero, so the full vector was readable
+        float o[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = fmaf(ep.a, x[e], v[e]) * rs;
-        if (!apply) {
+        for (int e = 0; e < 8; ++e) o[e] = v[e] * rs;
+        if (!pb.last) {
+          const size_t off = mbase + (size_t)gi * pb.L + gj;
           if (gj + 8 <= l) {
             store8_bf16(pb.out + off, o);
           } else {
             for (int e = 0; e < 8 && gj + e < l; ++e) pb.out[off + e] = ns_f2bf(o[e]);
           }
         } else if (direct_apply) {
-          const float lrm = ep.lr * M.lr_mult;
           float* pp = M.p + (size_t)gi * M.n + gj;
           if (gj + 8 <= l && M.pvec) {
-            float4 a0 = reinterpret_cast<float4*>(pp)[0], a1 = reinterpret_cast<float4*>(pp)[1];
-            float q[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float q[8] = {pre[k][0].x, pre[k][0].y, pre[k][0].z, pre[k][0].w,
+                          pre[k][1].x, pre[k][1].y, pre[k][1].z, pre[k][1].w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) q[e] = fmaf(q[e], ep.decay, -lrm * o[e]);
             reinterpret_cast<float4*>(pp)[0] = make_float4(q[0], q[1], q[2], q[3]);
@@ -307,25 +307,31 @@ __device__ __forceinline__ void epilogue_block(const NsProblem& pb, const NsEpiA
         }
       }
     }
-    if (apply && M.transposed) {
+    if (pb.last && M.transposed) {
       __syncwarp();
       const int gi = row0 + lane;  // canonical row = parameter column
-      if (gi < s) {
-        const float lrm = ep.lr * M.lr_mult;
+      const int cnt = l - col0 < 32 ? l - col0 : 32;
+      if (gi < s && cnt > 0) {
+        float pv[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (e < cnt) pv[e] = M.p[(size_t)(col0 + e) * M.n + gi];  // canonical column = parameter row
+#pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int gj = col0 + e;  // canonical column = parameter row
-          if (gj >= l) break;
-          const size_t po = (size_t)gj * M.n + gi;
-          const float q = fmaf(M.p[po], ep.decay, -lrm * sb[lane * EPI_LD + e]);
-          M.p[po] = q;
-          if (M.shadow) M.shadow[po] = ns_f2bf(q);
+          if (e < cnt) {
+            const size_t po = (size_t)(col0 + e) * M.n + gi;
+            const float q = fmaf(pv[e], ep.decay, -lrm * sb[lane * EPI_LD + e]);
+            M.p[po] = q;
+            if (M.shadow) M.shadow[po] = ns_f2bf(q);
+          }
         }
       }
     }
   } else {
     // GRAM / POLY: symmetric s x s output, lower triangle computed, mirrored
+    const bool gram = pb.kind == NS_GRAM;
     const size_t mbase = (size_t)mat * pb.S * pb.S;
-    const float sc = pb.kind == NS_GRAM ? (pb.first ? pb.rscale[mat] * pb.rscale[mat] : 1.f) : 0.f;
+    const float sc = gram && pb.first ? pb.rscale[mat] * pb.rscale[mat] : 1.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int rr = (lane >> 2) + 8 * k;
@@ -334,14 +340,16 @@ __device__ __forceinline__ void epilogue_block(const NsProblem& pb, const NsEpiA
       if (gi < s && gj <= gi && gj < s) {
         const size_t off = mbase + (size_t)gi * pb.S + gj;
         float o[8];
-        if (pb.kind == NS_GRAM) {
+        if (gram) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) o[e] = v[e] * sc;
         } else {
-          float a[8];
-          unpack8_bf16(pre[k], a);  // A is stored in full (mirrored), padding zero
+          const uint32_t u[4] = {preA[k].x, preA[k].y, preA[k].z, preA[k].w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = fmaf(ep.c, v[e], ep.b * a[e]);
+          for (int e = 0; e < 8; ++e) {
+            const float a = __uint_as_float((e & 1) ? (u[e >> 1] & 0xFFFF0000u) : (u[e >> 1] << 16));
+            o[e] = fmaf(ep.c, v[e], fmaf(ep.b, a, gj + e == gi ? ep.a : 0.f));
+          }
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = o[e];
