@@ -42,6 +42,28 @@ NS_KINDS = ("ns_gram", "ns_poly", "ns_update")
 STREAM_KINDS = ("grad_norm", "momentum", "adamw")
 
 
+# DRAM bytes per ns_tc_kernel launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
+# capture of the 6-layer case of this workload (profiles/ns_tc_kernel_expert1024x6.md: one launch of
+# each product), scaled to the 16-layer h1024 workload by the matrices processed (16/6) and averaged
+# over the three products. It describes only the kernel sources it was measured on: any change to
+# them makes it null until it is measured again.
+NS_TRAFFIC = {"sources_sha256": "7275095b701724277b8aa633dbe433eca812e2060ea7c295e76a60b0d0bdd941",
+              "bytes_per_launch": 760909824, "workload": "h1024"}
+NS_SOURCES = ("ns_tc.cu", "ns_epilogue.cuh", "internal.h")
+
+
+def ns_traffic_per_launch(workload: str):
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in NS_SOURCES:
+        with open(os.path.join(ROOT, "muon_adamw_hybrid_grad_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != NS_TRAFFIC["sources_sha256"] or workload != NS_TRAFFIC["workload"]:
+        return None
+    return NS_TRAFFIC["bytes_per_launch"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -306,6 +328,9 @@ def run_ours(args):
         elif k in STREAM_KINDS:
             d["gbs"] = round(e["units"] / (e["ms"] / 1e3) / 1e9, 1)
             d["frac_hbm"] = round(d["gbs"] / peaks["hbm_gbs"], 3)
+            if k == "adamw":
+                d["note"] = ("second stream, concurrent with the Newton-Schulz chain: the event time includes "
+                             "waiting for SMs")
         kernels[k] = d
     launches = sum(prof[k]["launches"] for k in KINDS)
     out = {
@@ -343,7 +368,8 @@ def run_ours(args):
             "peak_kind": f"bf16 dense burst, {peaks['source']} (MEASURED_PEAKS.json)",
             "unit": "TFLOP/s",
             "frac": round(ns_tflops / peaks["bf16_tflops"], 3) if ns_tflops else None,
-            "traffic": None,
+            "traffic": ns_traffic_per_launch(w.name),
+            "traffic_unit": "bytes per launch (ncu, scaled from the 6-layer case; null when stale)",
             "launches_timed": ns_launches,
             "algorithmic_flops_per_launch": round(ns_flops / max(1, ns_launches)),
         },

@@ -828,6 +828,8 @@ ma_status muon_adamw_last_norm(muon_adamw_t* h, float* total_out, float* coef_ou
   CUDA_TRY(cudaStreamSynchronize(h->s0));
   if (total_out) *total_out = sc.total;
   if (coef_out) *coef_out = sc.coef;
+  ma_status st = check_device_flag(h);
+  if (st != MA_OK) return st;
   return ok();
 }
 
