@@ -120,6 +120,7 @@ struct muon_adamw {
   muon_adamw_config cfg{};
   int device = 0;
   int num_sms = 0;
+  int max_pairs = 1;          // co-resident CTA pairs of the tensor-core kernel
   cudaStream_t s0 = nullptr;  // caller's stream
   cudaStream_t s1 = nullptr;  // AdamW stream (library-owned)
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -493,28 +494,42 @@ ma_status build_plan(muon_adamw* h) {
       }
       h->simt[kind][it] = probs;
       if (c.ns_kernel == MA_NS_TCGEN05) {
-        for (size_t b0 = 0; b0 < probs.size(); b0 += kTcMaxProblems) {
-          TcLaunch L;
-          memset(&L, 0, sizeof L);
-          int tiles_total = 0;
-          for (size_t q = 0; q < (size_t)kTcMaxProblems && b0 + q < probs.size(); ++q) {
-            TcProblem& tp = L.prob[q];
-            tp.p = probs[b0 + q];
-            char eb[256];
-            if (!tc_encode_problem(tp, eb, sizeof eb)) return fail(MA_ERR_CUDA, "%s", eb);
-            tp.tile_begin = tiles_total;
-            tiles_total += tp.tiles_per_mat * tp.p.nmat;
-            L.nprob = (int)q + 1;
+        // problems whose row blocks pair up run in CTA pairs (operand multicast); the rest singly
+        const bool allow_pairs = !(c.reserved[0] & 2);
+        for (int cl = 2; cl >= 1; --cl) {
+          std::vector<NsProblem> group;
+          for (const NsProblem& pp : probs)
+            if ((cl == 2) == (allow_pairs && ns_tc_pairable(pp))) group.push_back(pp);
+          // longest work units first: the static round-robin then ends on short units
+          std::stable_sort(group.begin(), group.end(),
+                           [](const NsProblem& a, const NsProblem& b) { return a.K > b.K; });
+          for (size_t b0 = 0; b0 < group.size(); b0 += kTcMaxProblems) {
+            TcLaunch L;
+            memset(&L, 0, sizeof L);
+            int tiles_total = 0;
+            for (size_t q = 0; q < (size_t)kTcMaxProblems && b0 + q < group.size(); ++q) {
+              TcProblem& tp = L.prob[q];
+              tp.p = group[b0 + q];
+              char eb[256];
+              if (!tc_encode_problem(tp, cl, eb, sizeof eb)) return fail(MA_ERR_CUDA, "%s", eb);
+              tp.tile_begin = tiles_total;
+              tiles_total += tp.tiles_per_mat * tp.p.nmat;
+              L.nprob = (int)q + 1;
+            }
+            L.total_tiles = tiles_total;
+            L.err = h->d_err;
+            L.mn_swap = (c.reserved[0] & 1) ? 1 : 0;
+            L.cl = cl;
+            h->tc[kind][it].push_back(L);
           }
-          L.total_tiles = tiles_total;
-          L.err = h->d_err;
-          L.mn_swap = (c.reserved[0] & 1) ? 1 : 0;
-          h->tc[kind][it].push_back(L);
         }
       }
     }
   }
-  if (c.ns_kernel == MA_NS_TCGEN05 && !h->buckets.empty()) CUDA_TRY(ns_tc_prepare());
+  if (c.ns_kernel == MA_NS_TCGEN05 && !h->buckets.empty()) {
+    CUDA_TRY(ns_tc_prepare(&h->max_pairs));
+    if (h->max_pairs < 1) h->max_pairs = 1;
+  }
   h->planned = true;
   return MA_OK;
 }
@@ -723,8 +738,9 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
         if (c.ns_kernel == MA_NS_TCGEN05) {
           for (TcLaunch& L : h->tc[kind][it]) {
             L.epi = epi;
+            const int grid_units = L.cl == 2 ? h->max_pairs : h->num_sms;
             timed(h, MA_K_NS_GRAM + kind, h->s0, units[kind] / h->tc[kind][it].size(),
-                  [&] { launch_ns_tc(L, h->num_sms, h->s0); });
+                  [&] { launch_ns_tc(L, grid_units, h->s0); });
           }
         } else {
           timed(h, MA_K_NS_GRAM + kind, h->s0, units[kind], [&] {

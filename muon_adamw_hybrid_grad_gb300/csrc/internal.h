@@ -135,24 +135,29 @@ struct TcProblem {
   int32_t bn;           // N tile: 128 or 256
   int32_t tiles_m;      // M / 128
   int32_t tiles_n;      // N / bn
-  int32_t tiles_per_mat;
-  int32_t tile_begin;   // first global tile index of this problem
+  int32_t tiles_per_mat;  // work units per matrix (a unit = cl row blocks x one column block)
+  int32_t tile_begin;   // first global work unit of this problem
   int32_t pad[3];
 };
 struct TcLaunch {
   TcProblem prob[kTcMaxProblems];
   int32_t nprob;
-  int32_t total_tiles;
+  int32_t total_tiles;  // work units in the launch
   NsEpiArgs epi;
   int* err;             // device error flag
   int32_t mn_swap;      // cross-check knob: exchange LBO/SBO of the MN-major descriptor
-  int32_t pad;
+  int32_t cl;           // CTAs per cluster: 1, or 2 (operand multicast between a CTA pair)
 };
-// Encode the tensor maps of `tp` (host; uses the driver entry point).
-bool tc_encode_problem(TcProblem& tp, char* errbuf, size_t errlen);
-cudaError_t ns_tc_prepare();  // sets the kernel's dynamic shared-memory limit (current device)
-void launch_ns_tc(const TcLaunch& L, int grid, cudaStream_t st);
+// Whether a problem can run in CTA pairs (its row blocks pair up).
+bool ns_tc_pairable(const NsProblem& p);
+// Encode the tensor maps of `tp` and count its work units for cluster size cl (host).
+bool tc_encode_problem(TcProblem& tp, int cl, char* errbuf, size_t errlen);
+// Sets the kernels' dynamic shared-memory limit (current device) and returns
+// how many CTA pairs can be resident at once.
+cudaError_t ns_tc_prepare(int* max_pairs);
+// grid_units: clusters to launch (CTAs = grid_units * cl), capped at the work units.
+cudaError_t launch_ns_tc(const TcLaunch& L, int grid_units, cudaStream_t st);
 size_t ns_tc_smem_bytes();
-int ns_tc_num_tiles_sym(int tiles_m, int bn);  // lower-triangle tile count per matrix
+int ns_tc_num_tiles_sym(int units_m, int bmu, int bn);  // lower-triangle work units per matrix
 
 }  // namespace ma

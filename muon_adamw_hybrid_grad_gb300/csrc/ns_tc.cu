@@ -47,9 +47,8 @@ constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int EPI_WARPS = 8;  // two warps per TMEM lane quarter, splitting the columns
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int EPI_LD = 33;                                   // padded row of the staging tile
-constexpr int EPI_STAGE_FLOATS = 32 * EPI_LD;                 // one 32x32 fp32 block per warp
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + EPI_WARPS * EPI_STAGE_FLOATS * 4;
+constexpr int EPI_STAGE_WORDS = 32 * 16;  // one 32x32 bf16 block per warp (2 KiB)
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + EPI_WARPS * EPI_STAGE_WORDS * 4;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 // error codes written to the device flag
@@ -119,6 +118,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar,
+                                                      uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -134,6 +153,15 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
 
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Arrive (when this thread's prior MMAs complete) on the mbarrier at the same
+// shared-memory offset in every CTA of `cta_mask`.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(cta_mask)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -181,6 +209,8 @@ struct TileCoord {
   int prob, mat, ti, tj;
 };
 
+// Work unit g -> (problem, matrix, row unit, column block). A row unit is
+// L.cl consecutive 128-row blocks (one per CTA of the cluster).
 __device__ __forceinline__ TileCoord decode_tile(const TcLaunch& L, int g) {
   TileCoord c{0, 0, 0, 0};
   int pi = 0;
@@ -194,10 +224,11 @@ __device__ __forceinline__ TileCoord decode_tile(const TcLaunch& L, int g) {
     c.ti = t / P.tiles_n;
     c.tj = t - c.ti * P.tiles_n;
   } else {
-    // row block ti holds the tiles whose columns start at or before its last row
+    // row unit ti holds the tiles whose columns start at or before its last row
+    const int bmu = BM * L.cl;
     int ti = 0;
     for (;;) {
-      const int cnt = (ti * BM + BM - 1) / P.bn + 1;
+      const int cnt = (ti * bmu + bmu - 1) / P.bn + 1;
       if (t < cnt) break;
       t -= cnt;
       ++ti;
@@ -208,172 +239,181 @@ __device__ __forceinline__ TileCoord decode_tile(const TcLaunch& L, int g) {
   return c;
 }
 
-__device__ __forceinline__ void store8_bf16(uint16_t* p, const float* x) {
-  uint4 w;
-  w.x = (uint32_t)ns_f2bf(x[0]) | ((uint32_t)ns_f2bf(x[1]) << 16);
-  w.y = (uint32_t)ns_f2bf(x[2]) | ((uint32_t)ns_f2bf(x[3]) << 16);
-  w.z = (uint32_t)ns_f2bf(x[4]) | ((uint32_t)ns_f2bf(x[5]) << 16);
-  w.w = (uint32_t)ns_f2bf(x[6]) | ((uint32_t)ns_f2bf(x[7]) << 16);
-  *reinterpret_cast<uint4*>(p) = w;
+
+__device__ __forceinline__ uint32_t u4_get(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)ns_f2bf(lo) | ((uint32_t)ns_f2bf(hi) << 16);
 }
 
 // Epilogue of one 32x32 block of the accumulator: rows row0..row0+31 (this
-// warp's TMEM lane quarter), columns col0..col0+31 of matrix `mat`. The
-// block goes through the warp's shared tile `sb` (fp32, row stride 33:
-// conflict-free both ways). Row phase: a lane handles 8 consecutive columns
-// of rows (lane/4) + 8k, so each 16-byte access of 4 lanes covers a
-// contiguous row segment. Column phase (one row per lane): the mirrored
-// stores of the symmetric products and the write-back into tall
-// (transposed) parameters, where lanes are contiguous in memory. Only the
-// b A term of B and the last iteration's parameters are read from memory.
+// warp's TMEM lane quarter; lane l holds row row0 + l), columns
+// col0..col0+31 of matrix `mat`. Values are computed in registers in that
+// one-row-per-lane layout. Row-major stores go through the warp's 2 KiB
+// shared tile `sb16` as bf16 (four 16-byte stores and loads per lane; the
+// 16-byte chunk q of row r sits at chunk q ^ ((r >> 1) & 3), which keeps
+// both directions free of bank conflicts) and leave as 16-byte vectors of
+// which four lanes cover 64 contiguous bytes of a row. The mirrored half of
+// the symmetric products and the write-back into tall (transposed)
+// parameters are stored straight from registers: there the lanes' addresses
+// are contiguous. Only the b A term of B and the last iteration's
+// parameters are read from memory, and those loads are issued before TMEM is
+// read so that their latency overlaps it.
 __device__ __forceinline__ void epilogue_block(const NsProblem& pb, const NsEpiArgs& ep, int mat, int row0, int col0,
-                                               uint32_t taddr, float* sb, int lane) {
+                                               uint32_t taddr, uint32_t* sb16, int lane) {
   const MuonMat& M = pb.mats[mat];
   const int s = M.s;
-  const int cc = (lane & 3) * 8;
-  const bool direct_apply = pb.kind == NS_UPDATE && pb.last && !M.transposed;
-  // Global loads are issued before TMEM is read so that their latency
-  // overlaps the TMEM load and the shared-memory staging.
+  const int gi = row0 + lane;
+  const bool update = pb.kind == NS_UPDATE;
+  const bool apply = update && pb.last;
   uint4 preA[4];
+  float4 preP[8];
   if (pb.kind == NS_POLY) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int gi = row0 + (lane >> 2) + 8 * k, gj = col0 + cc;
-      preA[k] = make_uint4(0u, 0u, 0u, 0u);
-      if (gi < s && gj <= gi && gj < s)  // A is stored in full (mirrored); padding is zero
-        preA[k] = __ldg(reinterpret_cast<const uint4*>(pb.aux + (size_t)mat * pb.S * pb.S + (size_t)gi * pb.S + gj));
+    for (int q = 0; q < 4; ++q) preA[q] = make_uint4(0u, 0u, 0u, 0u);
+    if (gi < s && col0 <= gi) {  // A is stored in full (mirrored); padding is zero
+      const uint4* ap = reinterpret_cast<const uint4*>(pb.aux + (size_t)mat * pb.S * pb.S + (size_t)gi * pb.S + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) preA[q] = __ldg(ap + q);
     }
   }
-  float4 pre[4][2];
-  if (direct_apply) {
+  const bool pfull = apply && !M.transposed && gi < s && col0 + 32 <= M.l && M.pvec;
+  if (pfull) {
+    const float4* pp = reinterpret_cast<const float4*>(M.p + (size_t)gi * M.n + col0);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int gi = row0 + (lane >> 2) + 8 * k, gj = col0 + cc;
-      pre[k][0] = pre[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (gi < s && gj + 8 <= M.l && M.pvec) {
-        const float4* pp = reinterpret_cast<const float4*>(M.p + (size_t)gi * M.n + gj);
-        pre[k][0] = pp[0];
-        pre[k][1] = pp[1];
-      }
-    }
+    for (int q = 0; q < 8; ++q) preP[q] = pp[q];
   }
   uint32_t r[32];
   tmem_ld_32x32b_x32(taddr, r);
   tmem_ld_wait();
-#pragma unroll
-  for (int e = 0; e < 32; ++e) sb[lane * EPI_LD + e] = __uint_as_float(r[e]);
-  __syncwarp();
-  if (pb.kind == NS_UPDATE) {
-    const int l = M.l;
-    const size_t mbase = (size_t)mat * pb.S * pb.L;
+  float o[32];
+  if (update) {
     const float rs = pb.first ? pb.rscale[mat] : 1.f;
-    const float lrm = ep.lr * M.lr_mult;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int rr = (lane >> 2) + 8 * k;
-      const int gi = row0 + rr, gj = col0 + cc;
-      float* v = sb + rr * EPI_LD + cc;
-      if (gi < s && gj < l) {
-        float o[8];
+    for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]) * rs;
+  } else if (pb.kind == NS_GRAM) {
+    const float sc = pb.first ? pb.rscale[mat] * pb.rscale[mat] : 1.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = v[e] * rs;
-        if (!pb.last) {
-          const size_t off = mbase + (size_t)gi * pb.L + gj;
-          if (gj + 8 <= l) {
-            store8_bf16(pb.out + off, o);
-          } else {
-            for (int e = 0; e < 8 && gj + e < l; ++e) pb.out[off + e] = ns_f2bf(o[e]);
-          }
-        } else if (direct_apply) {
-          float* pp = M.p + (size_t)gi * M.n + gj;
-          if (gj + 8 <= l && M.pvec) {
-            float q[8] = {pre[k][0].x, pre[k][0].y, pre[k][0].z, pre[k][0].w,
-                          pre[k][1].x, pre[k][1].y, pre[k][1].z, pre[k][1].w};
+    for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]) * sc;
+  } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) q[e] = fmaf(q[e], ep.decay, -lrm * o[e]);
-            reinterpret_cast<float4*>(pp)[0] = make_float4(q[0], q[1], q[2], q[3]);
-            reinterpret_cast<float4*>(pp)[1] = make_float4(q[4], q[5], q[6], q[7]);
-            if (M.shadow) store8_bf16(M.shadow + (size_t)gi * M.n + gj, q);
-          } else {
-            for (int e = 0; e < 8 && gj + e < l; ++e) {
-              const float q = fmaf(pp[e], ep.decay, -lrm * o[e]);
-              pp[e] = q;
-              if (M.shadow) M.shadow[(size_t)gi * M.n + gj + e] = ns_f2bf(q);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = o[e];  // transposed apply: column phase below
-        }
-      }
+    for (int e = 0; e < 32; ++e) {
+      const uint32_t u = u4_get(preA[e >> 3], (e >> 1) & 3);
+      const float a = __uint_as_float((e & 1) ? (u & 0xFFFF0000u) : (u << 16));
+      o[e] = fmaf(ep.c, __uint_as_float(r[e]), fmaf(ep.b, a, col0 + e == gi ? ep.a : 0.f));
     }
-    if (pb.last && M.transposed) {
-      __syncwarp();
-      const int gi = row0 + lane;  // canonical row = parameter column
+  }
+
+  if (apply) {
+    // last Newton-Schulz iteration: p <- p (1 - lr wd) - lr_eff O, O never stored
+    const float lrm = ep.lr * M.lr_mult;
+    const int l = M.l;
+    if (M.transposed) {
+      // canonical row gi = parameter column; canonical column = parameter row
       const int cnt = l - col0 < 32 ? l - col0 : 32;
       if (gi < s && cnt > 0) {
         float pv[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          if (e < cnt) pv[e] = M.p[(size_t)(col0 + e) * M.n + gi];  // canonical column = parameter row
+          if (e < cnt) pv[e] = M.p[(size_t)(col0 + e) * M.n + gi];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           if (e < cnt) {
             const size_t po = (size_t)(col0 + e) * M.n + gi;
-            const float q = fmaf(pv[e], ep.decay, -lrm * sb[lane * EPI_LD + e]);
+            const float q = fmaf(pv[e], ep.decay, -lrm * o[e]);
             M.p[po] = q;
             if (M.shadow) M.shadow[po] = ns_f2bf(q);
           }
         }
       }
-    }
-  } else {
-    // GRAM / POLY: symmetric s x s output, lower triangle computed, mirrored
-    const bool gram = pb.kind == NS_GRAM;
-    const size_t mbase = (size_t)mat * pb.S * pb.S;
-    const float sc = gram && pb.first ? pb.rscale[mat] * pb.rscale[mat] : 1.f;
+    } else if (pfull) {
+      float4* pp = reinterpret_cast<float4*>(M.p + (size_t)gi * M.n + col0);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int rr = (lane >> 2) + 8 * k;
-      const int gi = row0 + rr, gj = col0 + cc;
-      float* v = sb + rr * EPI_LD + cc;
-      if (gi < s && gj <= gi && gj < s) {
-        const size_t off = mbase + (size_t)gi * pb.S + gj;
-        float o[8];
-        if (gram) {
+      for (int q = 0; q < 8; ++q) {
+        float4 v = preP[q];
+        v.x = fmaf(v.x, ep.decay, -lrm * o[4 * q + 0]);
+        v.y = fmaf(v.y, ep.decay, -lrm * o[4 * q + 1]);
+        v.z = fmaf(v.z, ep.decay, -lrm * o[4 * q + 2]);
+        v.w = fmaf(v.w, ep.decay, -lrm * o[4 * q + 3]);
+        pp[q] = v;
+        preP[q] = v;
+      }
+      if (M.shadow) {
+        uint4* sp = reinterpret_cast<uint4*>(M.shadow + (size_t)gi * M.n + col0);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = v[e] * sc;
-        } else {
-          const uint32_t u[4] = {preA[k].x, preA[k].y, preA[k].z, preA[k].w};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float a = __uint_as_float((e & 1) ? (u[e >> 1] & 0xFFFF0000u) : (u[e >> 1] << 16));
-            o[e] = fmaf(ep.c, v[e], fmaf(ep.b, a, gj + e == gi ? ep.a : 0.f));
-          }
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          w.x = pack_bf16x2(preP[2 * q].x, preP[2 * q].y);
+          w.y = pack_bf16x2(preP[2 * q].z, preP[2 * q].w);
+          w.z = pack_bf16x2(preP[2 * q + 1].x, preP[2 * q + 1].y);
+          w.w = pack_bf16x2(preP[2 * q + 1].z, preP[2 * q + 1].w);
+          sp[q] = w;
         }
+      }
+    } else if (gi < s) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = o[e];
-        if (gj + 7 <= gi && gj + 8 <= s) {
-          store8_bf16(pb.out + off, o);
-        } else {
-          for (int e = 0; e < 8 && gj + e <= gi && gj + e < s; ++e) pb.out[off + e] = ns_f2bf(o[e]);
+      for (int e = 0; e < 32; ++e) {
+        if (col0 + e < l) {
+          const size_t po = (size_t)gi * M.n + col0 + e;
+          const float q = fmaf(M.p[po], ep.decay, -lrm * o[e]);
+          M.p[po] = q;
+          if (M.shadow) M.shadow[po] = ns_f2bf(q);
         }
       }
     }
-    __syncwarp();
-    // mirror: out[j][i] = out[i][j] for j < i; lanes hold consecutive i
-    const int gi = row0 + lane;
-    if (gi < s) {
-      for (int e = 0; e < 32; ++e) {
-        const int gj = col0 + e;
-        if (gj >= gi) break;
-        pb.out[mbase + (size_t)gj * pb.S + gi] = ns_f2bf(sb[lane * EPI_LD + e]);
+    return;
+  }
+
+  // bf16 row-major stores, staged through shared memory
+  const int ld = update ? pb.L : pb.S;
+  const size_t mbase = (size_t)mat * pb.S * ld;
+  const int lim = update ? M.l : s;  // valid columns
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(o[8 * q + 0], o[8 * q + 1]);
+    w.y = pack_bf16x2(o[8 * q + 2], o[8 * q + 3]);
+    w.z = pack_bf16x2(o[8 * q + 4], o[8 * q + 5]);
+    w.w = pack_bf16x2(o[8 * q + 6], o[8 * q + 7]);
+    reinterpret_cast<uint4*>(sb16 + lane * 16)[q ^ ((lane >> 1) & 3)] = w;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int rr = (lane >> 2) + 8 * k, q = lane & 3;
+    const int gr = row0 + rr, gj = col0 + 8 * q;
+    const uint4 w = reinterpret_cast<const uint4*>(sb16 + rr * 16)[q ^ ((rr >> 1) & 3)];
+    const int hi = update ? lim : (gr + 1 < lim ? gr + 1 : lim);  // sym: columns j <= i only
+    if (gr < s && gj < hi) {
+      uint16_t* dst = pb.out + mbase + (size_t)gr * ld + gj;
+      if (gj + 8 <= hi) {
+        *reinterpret_cast<uint4*>(dst) = w;
+      } else {
+        for (int e = 0; e < 8 && gj + e < hi; ++e) {
+          const uint32_t u = u4_get(w, e >> 1);
+          dst[e] = (uint16_t)((e & 1) ? (u >> 16) : u);
+        }
       }
     }
   }
   __syncwarp();
+  if (!update && gi < s) {
+    // mirror: out[j][i] = out[i][j] for j < i; lanes hold consecutive i
+    uint16_t* col = pb.out + mbase + gi;
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (col0 + e < gi) col[(size_t)(col0 + e) * pb.S] = ns_f2bf(o[e]);
+  }
 }
 
+// CL = 1: one CTA per work unit. CL = 2: a cluster of two CTAs per unit of
+// two adjacent 128-row blocks that share the right-hand operand tile; each CTA
+// loads half of that tile and multicasts it into both CTAs' shared memory,
+// which cuts the L2 -> SM operand traffic per CTA from 48 KB to 32 KB per
+// k-block. The stage-release barrier then counts the MMA commits of both CTAs.
+template <int CL>
 __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant__ TcLaunch L) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -389,11 +429,15 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
   const uint32_t tfull0 = smem_u32(bars + 2 * STAGES);
   const uint32_t tempty0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+  const uint32_t crank = CL == 2 ? cluster_ctarank() : 0u;
+  const int unit0 = blockIdx.x / CL;   // this cluster's first work unit
+  const int nunits = gridDim.x / CL;   // clusters in the grid
+  const uint16_t mc_mask = (uint16_t)((1u << CL) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, CL);  // one MMA commit per CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -412,6 +456,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
   }
   tc_fence_before();
   __syncthreads();
+  if (CL == 2) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -426,13 +471,17 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int g = blockIdx.x; g < L.total_tiles && ok; g += gridDim.x) {
+      for (int g = unit0; g < L.total_tiles && ok; g += nunits) {
         const TileCoord c = decode_tile(L, g);
         const TcProblem& P = L.prob[c.prob];
         const int kblocks = P.p.K / BK;
-        const int rowP = c.mat * P.p.M + c.ti * BM;
+        const int rowP = c.mat * P.p.M + (c.ti * CL + (int)crank) * BM;
         const bool sym = P.p.kind != NS_UPDATE;
         const uint32_t tx = (uint32_t)(A_STAGE + P.bn * BK * 2);
+        // right-hand operand boxes: 128 rows each (K-major) or 64 columns each (MN-major);
+        // with CL = 2 this CTA loads its half of them and multicasts
+        const int nbox = sym ? P.bn / BM : P.bn / 64;
+        const int box0 = (int)crank * (nbox / CL), box1 = box0 + nbox / CL;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, L.err, kErrWaitProducer)) {
             ok = false;
@@ -443,12 +492,15 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
           const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
           const uint32_t sb = sa + A_STAGE;
           tma_load_2d(sa, &P.tmP, kb * BK, rowP, fb);
-          if (sym) {
-            const int rowQ = c.mat * P.p.N + c.tj * P.bn;
-            for (int h = 0; h < P.bn / BM; ++h) tma_load_2d(sb + h * (BM * BK * 2), &P.tmQ, kb * BK, rowQ + h * BM, fb);
-          } else {
-            const int rowQ = c.mat * P.p.K + kb * BK;
-            for (int q = 0; q < P.bn / 64; ++q) tma_load_2d(sb + q * (64 * BK * 2), &P.tmQ, c.tj * P.bn + q * 64, rowQ, fb);
+          for (int q = box0; q < box1; ++q) {
+            // sym: rows (column block) of the same matrix, K-major; update: X, MN-major
+            const uint32_t dst = sb + q * (sym ? BM * BK * 2 : 64 * BK * 2);
+            const int x = sym ? kb * BK : c.tj * P.bn + q * 64;
+            const int y = sym ? c.mat * P.p.N + c.tj * P.bn + q * BM : c.mat * P.p.K + kb * BK;
+            if (CL == 1)
+              tma_load_2d(dst, &P.tmQ, x, y, fb);
+            else
+              tma_load_2d_multicast(dst, &P.tmQ, x, y, fb, mc_mask);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -485,7 +537,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int g = blockIdx.x; g < L.total_tiles && ok; g += gridDim.x) {
+      for (int g = unit0; g < L.total_tiles && ok; g += nunits) {
         const TileCoord c = decode_tile(L, g);
         const TcProblem& P = L.prob[c.prob];
         const int kblocks = P.p.K / BK;
@@ -510,7 +562,10 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
             const uint64_t bd = sym ? sdesc(sb + kk * 32, 16, 1024) : sdesc(sb + kk * 16 * 128, lbo_mn, sbo_mn);
             umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(empty0 + 8 * stage);
+          if (CL == 1)
+            umma_commit(empty0 + 8 * stage);
+          else
+            umma_commit_multicast(empty0 + 8 * stage, mc_mask);  // both CTAs' copies of this stage are free
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -537,10 +592,10 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
     // ---------------- epilogue ----------------
     const int quarter = warp & 3;      // TMEM lanes 32*quarter .. 32*quarter+31
     const int half = (warp - 2) >> 2;  // which alternate 32-column blocks
-    float* sb = reinterpret_cast<float*>(smem + (size_t)STAGES * STAGE_BYTES + 256) + (warp - 2) * EPI_STAGE_FLOATS;
+    uint32_t* sb = reinterpret_cast<uint32_t*>(smem + (size_t)STAGES * STAGE_BYTES + 256) + (warp - 2) * EPI_STAGE_WORDS;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int g = blockIdx.x; g < L.total_tiles; g += gridDim.x) {
+    for (int g = unit0; g < L.total_tiles; g += nunits) {
       const TileCoord c = decode_tile(L, g);
       const TcProblem& P = L.prob[c.prob];
       // every lane waits; the vote keeps the warp converged for tcgen05.ld
@@ -548,7 +603,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN_MAX);
-      const int row0 = c.ti * BM + quarter * 32;
+      const int row0 = (c.ti * CL + (int)crank) * BM + quarter * 32;
       for (int c0 = 32 * half; c0 < P.bn; c0 += 64)
         epilogue_block(P.p, L.epi, c.mat, row0, c.tj * P.bn + c0, tbase + (uint32_t)c0, sb, lane);
       tc_fence_before();
@@ -562,6 +617,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
 
   tc_fence_before();
   __syncthreads();
+  // Neither CTA of a pair leaves while the other may still multicast into its
+  // shared memory or arrive on its barriers.
+  if (CL == 2) cluster_sync();
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
@@ -610,23 +668,31 @@ bool encode_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, 
 
 }  // namespace
 
-int ns_tc_num_tiles_sym(int tiles_m, int bn) {
+int ns_tc_num_tiles_sym(int units_m, int bmu, int bn) {
   int n = 0;
-  for (int ti = 0; ti < tiles_m; ++ti) n += (ti * BM + BM - 1) / bn + 1;
+  for (int ti = 0; ti < units_m; ++ti) n += (ti * bmu + bmu - 1) / bn + 1;
   return n;
 }
 
-bool tc_encode_problem(TcProblem& tp, char* errbuf, size_t errlen) {
+bool ns_tc_pairable(const NsProblem& p) { return p.M % (2 * BM) == 0; }
+
+bool tc_encode_problem(TcProblem& tp, int cl, char* errbuf, size_t errlen) {
   const NsProblem& p = tp.p;
   if (p.M % BM || p.K % BK || p.N % 128) {
     snprintf(errbuf, errlen, "tcgen05 GEMM needs M%%128 == 0, K%%64 == 0, N%%128 == 0 (M=%d N=%d K=%d)", p.M, p.N,
              p.K);
     return false;
   }
+  if (cl == 2 && !ns_tc_pairable(p)) {
+    snprintf(errbuf, errlen, "paired launch needs M %% 256 == 0 (M=%d)", p.M);
+    return false;
+  }
   tp.bn = (p.N % 256 == 0) ? 256 : 128;
   tp.tiles_m = p.M / BM;
   tp.tiles_n = p.N / tp.bn;
-  tp.tiles_per_mat = p.kind == NS_UPDATE ? tp.tiles_m * tp.tiles_n : ns_tc_num_tiles_sym(tp.tiles_m, tp.bn);
+  const int units_m = tp.tiles_m / cl;
+  tp.tiles_per_mat =
+      p.kind == NS_UPDATE ? units_m * tp.tiles_n : ns_tc_num_tiles_sym(units_m, BM * cl, tp.bn);
   const uint64_t nm = (uint64_t)p.nmat;
   // Left operand: [nmat * M] rows x K cols, K-major tiles of 128 x 64.
   if (!encode_2d(&tp.tmP, p.P, (uint64_t)p.K, nm * p.M, BK, BM, errbuf, errlen)) return false;
@@ -642,14 +708,49 @@ bool tc_encode_problem(TcProblem& tp, char* errbuf, size_t errlen) {
 
 size_t ns_tc_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t ns_tc_prepare() {
-  return cudaFuncSetAttribute(ns_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+cudaError_t ns_tc_prepare(int* max_pairs) {
+  cudaError_t e = cudaFuncSetAttribute(ns_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ns_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, ns_tc_kernel<2>, &cfg);
+  if (e != cudaSuccess) return e;
+  *max_pairs = n;
+  return cudaSuccess;
 }
 
-void launch_ns_tc(const TcLaunch& L, int grid, cudaStream_t st) {
-  if (grid > L.total_tiles) grid = L.total_tiles;
-  if (grid <= 0) return;
-  ns_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(L);
+cudaError_t launch_ns_tc(const TcLaunch& L, int grid_units, cudaStream_t st) {
+  if (grid_units > L.total_tiles) grid_units = L.total_tiles;
+  if (grid_units <= 0) return cudaSuccess;
+  if (L.cl == 1) {
+    ns_tc_kernel<1><<<grid_units, THREADS, SMEM_BYTES, st>>>(L);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * grid_units, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ns_tc_kernel<2>, L);
 }
 
 }  // namespace ma
