@@ -37,8 +37,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "optimizer steps/s; NS5 TFLOP/s vs bf16 peak; AdamW HBM GB/s vs peak"
-KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "adamw")
-NS_KINDS = ("ns_gram", "ns_poly", "ns_update")
+KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "ns_apply", "adamw")
+NS_KINDS = ("ns_gram", "ns_poly", "ns_update", "ns_apply")
 STREAM_KINDS = ("grad_norm", "momentum", "adamw")
 
 

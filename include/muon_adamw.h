@@ -118,9 +118,10 @@ typedef enum {
   MA_K_NS_PREP = 3,     /* per-matrix Frobenius scale */
   MA_K_NS_GRAM = 4,     /* A = X X^T (iteration 1 scaled by 1/||G||^2) */
   MA_K_NS_POLY = 5,     /* B = b A + c A A */
-  MA_K_NS_UPDATE = 6,   /* X <- a X + B X (last iteration applies the step) */
+  MA_K_NS_UPDATE = 6,   /* X <- B X, iterations 1 .. ns_steps-1 */
   MA_K_ADAMW = 7,       /* fused multi-tensor AdamW */
-  MA_K_COUNT = 8
+  MA_K_NS_APPLY = 8,    /* last iteration: B X applied to the parameters (Muon step) */
+  MA_K_COUNT = 9
 } ma_kernel_kind;
 
 typedef struct {

@@ -45,7 +45,7 @@ MA_DT_BF16 = 1
 MA_NS_TCGEN05 = 0
 MA_NS_SIMT = 1
 
-KERNEL_KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "adamw")
+KERNEL_KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "adamw", "ns_apply")
 MA_K_COUNT = len(KERNEL_KINDS)
 GROUP_NAMES = {MA_GROUP_MUON: "muon", MA_GROUP_ADAMW: "adamw", MA_GROUP_FROZEN: "frozen"}
 

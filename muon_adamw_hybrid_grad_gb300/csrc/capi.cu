@@ -307,7 +307,7 @@ ma_status build_plan(muon_adamw* h) {
   const size_t off_tiles = off;
   off += al(n_tiles * sizeof(MomTile));
   const size_t off_tile_part = off;
-  off += al(n_tiles * sizeof(float));
+  off += al(n_tiles * kMomPartialsPerTile * sizeof(float));
   const size_t off_rscale = off;
   off += al(n_mats * sizeof(float));
   const size_t off_scalars = off;
@@ -739,11 +739,12 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
           for (TcLaunch& L : h->tc[kind][it]) {
             L.epi = epi;
             const int grid_units = L.cl == 2 ? h->max_pairs : h->num_sms;
-            timed(h, MA_K_NS_GRAM + kind, h->s0, units[kind] / h->tc[kind][it].size(),
-                  [&] { launch_ns_tc(L, grid_units, h->s0); });
+            const int pk = (kind == NS_UPDATE && it == c.ns_steps - 1) ? MA_K_NS_APPLY : MA_K_NS_GRAM + kind;
+            timed(h, pk, h->s0, units[kind] / h->tc[kind][it].size(), [&] { launch_ns_tc(L, grid_units, h->s0); });
           }
         } else {
-          timed(h, MA_K_NS_GRAM + kind, h->s0, units[kind], [&] {
+          const int pk = (kind == NS_UPDATE && it == c.ns_steps - 1) ? MA_K_NS_APPLY : MA_K_NS_GRAM + kind;
+          timed(h, pk, h->s0, units[kind], [&] {
             for (const NsProblem& p : h->simt[kind][it]) launch_ns_simt(p, epi, h->s0);
           });
         }

@@ -10,8 +10,10 @@ namespace ma {
 
 // Elements per multi-tensor chunk of the gradient-norm and AdamW streams.
 constexpr int64_t kChunk = 1 << 16;
-// Edge of the square tiles the Muon momentum kernel walks.
+// Edge of the square tiles the Muon momentum kernel walks, and the partial
+// sums of squares it writes per tile (one per warp).
 constexpr int kMomTile = 64;
+constexpr int kMomPartialsPerTile = 8;
 // Padding granule of the canonical Newton-Schulz workspaces (rows and cols).
 constexpr int kPad = 128;
 

@@ -184,24 +184,29 @@ __global__ void __launch_bounds__(kClipThreads) clip_finalize_kernel(const float
 // Muon momentum + canonical bf16 pack.
 // One 64x64 tile of one parameter per iteration; 256 threads, each owns an
 // 8-wide column group of two rows. buf <- mu*buf + coef*g; the update
-// (Nesterov: coef*g + mu*buf) goes to shared memory as bf16 and from there
-// to X, transposed for tall matrices so that X is always s x l.
+// (Nesterov: coef*g + mu*buf) goes to X in bf16. Wide matrices (X = update)
+// are written straight from registers, 16 bytes per thread, with no block
+// barrier. Tall matrices (X = update^T) go through a shared-memory tile,
+// double-buffered so that one barrier per tile suffices. Sum of squares of
+// the update: one fp32 partial per warp and tile (fixed order).
 // ---------------------------------------------------------------------------
 constexpr int kMomThreads = 256;
+constexpr int kMomWarps = kMomThreads / 32;
 
 __global__ void __launch_bounds__(kMomThreads) muon_momentum_kernel(const MomTile* __restrict__ tiles, int ntiles,
                                                                     const MuonMat* __restrict__ mats,
                                                                     const StepScalars* __restrict__ sc, MomArgs args,
                                                                     float* __restrict__ tile_partials) {
-  __shared__ __align__(16) uint16_t su[kMomTile][kMomTile + 8];
-  __shared__ double sh[kMomThreads / 32];
+  __shared__ __align__(16) uint16_t su[2][kMomTile][kMomTile + 8];
   const float coef = sc->coef;
   const float mu = args.mu;
   const int cg = threadIdx.x & 7;   // column group (8 columns)
   const int rr = threadIdx.x >> 3;  // row 0..31
+  int ntrans = 0;                   // transposed tiles seen: selects the shared buffer
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const MomTile tl = tiles[t];
     const MuonMat M = mats[tl.mat];
+    uint16_t(*sbuf)[kMomTile + 8] = su[ntrans & 1];
     float acc = 0.f;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -209,7 +214,8 @@ __global__ void __launch_bounds__(kMomThreads) muon_momentum_kernel(const MomTil
       const int64_t gr = tl.r0 + r;
       const int gc = tl.c0 + cg * 8;
       float u[8];
-      if (gr < M.m && gc + 8 <= M.n && M.vec) {
+      const bool vec = gr < M.m && gc + 8 <= M.n && M.vec;
+      if (vec) {
         const int64_t off = gr * (int64_t)M.n + gc;
         float g[8];
         if (M.gdtype == DT_BF16) {
@@ -246,29 +252,31 @@ __global__ void __launch_bounds__(kMomThreads) muon_momentum_kernel(const MomTil
         }
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        acc = fmaf(u[e], u[e], acc);
-        su[r][cg * 8 + e] = f2bf(u[e]);
-      }
-    }
-    __syncthreads();
-    if (!M.transposed) {
-      // X[row][col] = update[row][col]
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int r = rr + 32 * half;
-        const int64_t gr = tl.r0 + r;
-        const int gc = tl.c0 + cg * 8;
+      for (int e = 0; e < 8; ++e) acc = fmaf(u[e], u[e], acc);
+      if (!M.transposed) {
+        // X[row][col] = update[row][col], straight from registers
         if (gr < M.m) {
           uint16_t* dst = M.x0 + gr * (int64_t)M.L + gc;
           if (gc + 8 <= M.n) {
-            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&su[r][cg * 8]);
+            uint4 w;
+            w.x = pack2(u[0], u[1]);
+            w.y = pack2(u[2], u[3]);
+            w.z = pack2(u[4], u[5]);
+            w.w = pack2(u[6], u[7]);
+            *reinterpret_cast<uint4*>(dst) = w;
           } else {
-            for (int e = 0; gc + e < M.n; ++e) dst[e] = su[r][cg * 8 + e];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (gc + e < M.n) dst[e] = f2bf(u[e]);
           }
         }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sbuf[r][cg * 8 + e] = f2bf(u[e]);
       }
-    } else {
+    }
+    if (M.transposed) {
+      __syncthreads();
       // X[col][row] = update[row][col]: canonical row = parameter column
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -278,7 +286,7 @@ __global__ void __launch_bounds__(kMomThreads) muon_momentum_kernel(const MomTil
         if (pc < M.n) {
           uint16_t v[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = su[cg * 8 + e][cc];
+          for (int e = 0; e < 8; ++e) v[e] = sbuf[cg * 8 + e][cc];
           uint16_t* dst = M.x0 + pc * (int64_t)M.L + pr;
           if (pr + 8 <= M.m) {
             uint4 w;
@@ -288,14 +296,17 @@ __global__ void __launch_bounds__(kMomThreads) muon_momentum_kernel(const MomTil
             w.w = (uint32_t)v[6] | ((uint32_t)v[7] << 16);
             *reinterpret_cast<uint4*>(dst) = w;
           } else {
-            for (int e = 0; pr + e < M.m; ++e) dst[e] = v[e];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (pr + e < M.m) dst[e] = v[e];
           }
         }
       }
+      ++ntrans;  // the next transposed tile writes the other buffer
     }
-    const double tot = block_sum_double<kMomThreads>((double)acc, sh);
-    if (threadIdx.x == 0) tile_partials[t] = (float)tot;
-    // block_sum_double ends with a barrier, so su may be rewritten next tile
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if ((threadIdx.x & 31) == 0) tile_partials[(size_t)t * kMomWarps + (threadIdx.x >> 5)] = acc;
   }
 }
 
@@ -307,9 +318,9 @@ __global__ void ns_prep_kernel(const MuonMat* __restrict__ mats, int nmat, const
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= nmat) return;
-  const int b = mats[w].tile_begin, e = mats[w].tile_end;
+  const int64_t b = (int64_t)mats[w].tile_begin * kMomWarps, e = (int64_t)mats[w].tile_end * kMomWarps;
   double s = 0.0;
-  for (int i = b + lane; i < e; i += 32) s += (double)part[i];
+  for (int64_t i = b + lane; i < e; i += 32) s += (double)part[i];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   if (lane == 0) rscale[w] = (float)(1.0 / (sqrt(s) + (double)eps));

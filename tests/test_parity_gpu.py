@@ -309,7 +309,8 @@ def test_profiling_counts_launches(mx):
         assert prof["steps"] == 2
         assert prof["ns_gram"]["launches"] == 2 * 5
         assert prof["adamw"]["launches"] == 2 and prof["momentum"]["launches"] == 2
-        for k in ("grad_norm", "momentum", "ns_gram", "ns_poly", "ns_update", "adamw"):
+        assert prof["ns_update"]["launches"] == 2 * 4 and prof["ns_apply"]["launches"] == 2
+        for k in ("grad_norm", "momentum", "ns_gram", "ns_poly", "ns_update", "ns_apply", "adamw"):
             assert prof[k]["ms"] > 0 and prof[k]["units"] > 0
     finally:
         gpu.close()
