@@ -204,6 +204,16 @@ MA_API ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_ou
  * MA_ERR_DEVICE_CHECK if a bounded in-kernel wait ran out. */
 MA_API ma_status muon_adamw_sync(muon_adamw_t* h);
 
+/* Test hook for the failure path, not for production use. Arms a one-shot
+ * stall: in the next step's first Newton-Schulz launch, one CTA issues no
+ * operand loads, so its MMA warp's bounded wait (2 s) runs out. The kernel
+ * then records the error, drains and releases its resources and returns;
+ * that step's result is invalid and the step reports MA_ERR_DEVICE_CHECK
+ * when its norm is read (or on muon_adamw_sync). Nothing faults, and the
+ * handle and context stay usable for later steps. Errors: MA_ERR_ARG,
+ * MA_ERR_UNSUPPORTED (MA_NS_SIMT has no waits). */
+MA_API ma_status muon_adamw_test_arm_stall(muon_adamw_t* h);
+
 /* Copy optimizer state of parameter `index` to host memory `dst_host`
  * (numel fp32 values). which = 0: Muon momentum buffer or AdamW first
  * moment; which = 1: AdamW second moment. Synchronises the stream.

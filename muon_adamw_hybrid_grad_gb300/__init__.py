@@ -125,6 +125,7 @@ _SIGNATURES = {
                                                  ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "muon_adamw_step": (ctypes.c_int, [_P, ctypes.c_double, ctypes.POINTER(ctypes.c_float)]),
     "muon_adamw_sync": (ctypes.c_int, [_P]),
+    "muon_adamw_test_arm_stall": (ctypes.c_int, [_P]),
     "muon_adamw_get_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),
     "muon_adamw_set_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),
     "muon_adamw_get_step": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int64)]),
@@ -217,6 +218,10 @@ def muon_adamw_step(h: int, lr: float, want_norm: bool = False) -> Optional[floa
 
 def muon_adamw_sync(h: int) -> None:
     _check(load_library().muon_adamw_sync(_P(h)))
+
+
+def muon_adamw_test_arm_stall(h: int) -> None:
+    _check(load_library().muon_adamw_test_arm_stall(_P(h)))
 
 
 def muon_adamw_get_state(h: int, index: int, which: int, dst_ptr: int) -> None:

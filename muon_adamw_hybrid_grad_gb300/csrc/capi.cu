@@ -121,6 +121,7 @@ struct muon_adamw {
   int device = 0;
   int num_sms = 0;
   int max_pairs = 1;          // co-resident CTA pairs of the tensor-core kernel
+  bool stall_test = false;    // one-shot test hook armed by muon_adamw_test_arm_stall
   cudaStream_t s0 = nullptr;  // caller's stream
   cudaStream_t s1 = nullptr;  // AdamW stream (library-owned)
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -738,6 +739,8 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
         if (c.ns_kernel == MA_NS_TCGEN05) {
           for (TcLaunch& L : h->tc[kind][it]) {
             L.epi = epi;
+            L.stall_test = h->stall_test ? 1 : 0;
+            h->stall_test = false;  // one launch only
             const int grid_units = L.cl == 2 ? h->max_pairs : h->num_sms;
             const int pk = (kind == NS_UPDATE && it == c.ns_steps - 1) ? MA_K_NS_APPLY : MA_K_NS_GRAM + kind;
             timed(h, pk, h->s0, units[kind] / h->tc[kind][it].size(), [&] { launch_ns_tc(L, grid_units, h->s0); });
@@ -765,6 +768,13 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
     ma_status st = check_device_flag(h);
     if (st != MA_OK) return st;
   }
+  return ok();
+}
+
+ma_status muon_adamw_test_arm_stall(muon_adamw_t* h) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  if (h->cfg.ns_kernel != MA_NS_TCGEN05) return fail(MA_ERR_UNSUPPORTED, "only the tensor-core kernel has waits");
+  h->stall_test = true;
   return ok();
 }
 

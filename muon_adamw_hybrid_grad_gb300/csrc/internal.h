@@ -149,6 +149,8 @@ struct TcLaunch {
   int* err;             // device error flag
   int32_t mn_swap;      // cross-check knob: exchange LBO/SBO of the MN-major descriptor
   int32_t cl;           // CTAs per cluster: 1, or 2 (operand multicast between a CTA pair)
+  int32_t stall_test;   // test hook: CTA 0's producer issues no loads (its waits then run out)
+  int32_t pad;
 };
 // Whether a problem can run in CTA pairs (its row blocks pair up).
 bool ns_tc_pairable(const NsProblem& p);

@@ -470,7 +470,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
-      bool ok = true;
+      // test hook: with stall_test, CTA 0 issues nothing, so its MMA warp's
+      // bounded wait for the first stage runs out and reports the error
+      bool ok = !(L.stall_test && blockIdx.x == 0);
       for (int g = unit0; g < L.total_tiles && ok; g += nunits) {
         const TileCoord c = decode_tile(L, g);
         const TcProblem& P = L.prob[c.prob];

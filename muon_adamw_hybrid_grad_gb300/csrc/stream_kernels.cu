@@ -311,19 +311,22 @@ __global__ void __launch_bounds__(kMomThreads) muon_momentum_kernel(const MomTil
 }
 
 // ---------------------------------------------------------------------------
-// Per-matrix Frobenius scale, one warp per matrix, fixed-order sum.
+// Per-matrix Frobenius scale: one 256-thread block per matrix sums the
+// matrix's per-warp partials in a fixed order (double precision).
 // ---------------------------------------------------------------------------
-__global__ void ns_prep_kernel(const MuonMat* __restrict__ mats, int nmat, const float* __restrict__ part,
-                               float eps, float* __restrict__ rscale) {
-  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+constexpr int kPrepThreads = 256;
+
+__global__ void __launch_bounds__(kPrepThreads) ns_prep_kernel(const MuonMat* __restrict__ mats, int nmat,
+                                                               const float* __restrict__ part, float eps,
+                                                               float* __restrict__ rscale) {
+  __shared__ double sh[kPrepThreads / 32];
+  const int w = blockIdx.x;
   if (w >= nmat) return;
   const int64_t b = (int64_t)mats[w].tile_begin * kMomWarps, e = (int64_t)mats[w].tile_end * kMomWarps;
   double s = 0.0;
-  for (int64_t i = b + lane; i < e; i += 32) s += (double)part[i];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) rscale[w] = (float)(1.0 / (sqrt(s) + (double)eps));
+  for (int64_t i = b + threadIdx.x; i < e; i += kPrepThreads) s += (double)part[i];
+  const double tot = block_sum_double<kPrepThreads>(s, sh);
+  if (threadIdx.x == 0) rscale[w] = (float)(1.0 / (sqrt(tot) + (double)eps));
 }
 
 // ---------------------------------------------------------------------------
@@ -406,9 +409,7 @@ void launch_muon_momentum(const MomTile* tiles, int ntiles, const MuonMat* mats,
 
 void launch_ns_prep(const MuonMat* mats, int nmat, const float* tile_partials, float eps, float* rscale,
                     cudaStream_t st) {
-  const int threads = 256;
-  const int blocks = (nmat * 32 + threads - 1) / threads;
-  ns_prep_kernel<<<blocks, threads, 0, st>>>(mats, nmat, tile_partials, eps, rscale);
+  if (nmat > 0) ns_prep_kernel<<<nmat, kPrepThreads, 0, st>>>(mats, nmat, tile_partials, eps, rscale);
 }
 
 void launch_adamw(const AdamChunk* chunks, int nchunks, const StepScalars* sc, AdamArgs args, int grid,

@@ -314,3 +314,28 @@ def test_profiling_counts_launches(mx):
             assert prof[k]["ms"] > 0 and prof[k]["units"] > 0
     finally:
         gpu.close()
+
+
+def test_bounded_wait_runs_out_and_reports(mx):
+    """Failure path without a fault: the armed test hook starves one CTA of
+    its operand loads, its bounded mbarrier wait runs out (2 s), and the step
+    reports MA_ERR_DEVICE_CHECK; the handle then steps normally again."""
+    import time
+
+    t = [TensorSpec("model.action_expert.layers.0.w.weight", (128, 512)), TensorSpec("model.vlm.ln.weight", (64,))]
+    w = workloads.custom_workload("stall", t, policy="fp32_mixed", steps=2)
+    gpu = GpuSide(w, workloads.master_weights(w))
+    try:
+        gpu.load_grads(workloads.gradients(w, 1))
+        gpu.mx.muon_adamw_test_arm_stall(gpu.opt.handle)
+        t0 = time.time()
+        with pytest.raises(gpu.mx.MuonAdamWError) as ei:
+            gpu.step(w.lr)
+        assert ei.value.status == gpu.mx.MA_ERR_DEVICE_CHECK
+        assert time.time() - t0 < 60
+        # the flag was consumed; the next steps run normally and stay finite
+        assert math.isfinite(gpu.step(w.lr))
+        gpu.mx.muon_adamw_sync(gpu.opt.handle)
+        assert np.isfinite(gpu.param(1)).all()
+    finally:
+        gpu.close()
