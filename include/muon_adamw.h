@@ -91,6 +91,11 @@ typedef struct {
   int32_t muon_nesterov;
   int32_t ns_steps;
   int32_t ns_kernel;
+  /* reserved[0]: cross-check switches for tests, 0 in normal use. Bit 0
+   * exchanges the strides of the MN-major operand descriptor (a wrong layout
+   * that parity must catch); bit 1 runs every Newton-Schulz product without
+   * CTA pairs; bit 2 writes the last iteration's parameters from registers
+   * instead of through TMA. reserved[1..6] must be 0. */
   int32_t reserved[7];
   /* Real-valued settings are doubles (like Python floats); the kernels get
    * fp32 values derived from them on the host, e.g. 1 - adam_beta2 is formed

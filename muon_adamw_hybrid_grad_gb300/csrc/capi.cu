@@ -143,6 +143,7 @@ struct muon_adamw {
   int n_adam_chunks = 0;
   int adam_grid = 0;
   MuonMat* d_mats = nullptr;
+  CUtensorMap* d_pmaps = nullptr;  // per Muon matrix: TMA maps of p and shadow
   int n_mats = 0;
   MomTile* d_tiles = nullptr;
   int n_tiles = 0;
@@ -305,6 +306,8 @@ ma_status build_plan(muon_adamw* h) {
   off += al(n_adam * sizeof(AdamChunk));
   const size_t off_mats = off;
   off += al(n_mats * sizeof(MuonMat));
+  const size_t off_pmaps = off;
+  off += al(n_mats * 2 * sizeof(CUtensorMap));
   const size_t off_tiles = off;
   off += al(n_tiles * sizeof(MomTile));
   const size_t off_tile_part = off;
@@ -339,6 +342,7 @@ ma_status build_plan(muon_adamw* h) {
   h->d_adam_chunks = reinterpret_cast<AdamChunk*>(base + off_adam_chunks);
   h->n_adam_chunks = (int)n_adam;
   h->d_mats = reinterpret_cast<MuonMat*>(base + off_mats);
+  h->d_pmaps = reinterpret_cast<CUtensorMap*>(base + off_pmaps);
   h->d_tiles = reinterpret_cast<MomTile*>(base + off_tiles);
   h->d_tile_partials = reinterpret_cast<float*>(base + off_tile_part);
   h->d_rscale = reinterpret_cast<float*>(base + off_rscale);
@@ -349,6 +353,7 @@ ma_status build_plan(muon_adamw* h) {
   std::vector<GradChunk> norm_chunks;
   std::vector<AdamChunk> adam_chunks;
   std::vector<MuonMat> mats;
+  std::vector<CUtensorMap> pmaps;
   std::vector<MomTile> tiles;
   norm_chunks.reserve(n_norm);
   adam_chunks.reserve(n_adam);
@@ -416,6 +421,11 @@ ma_status build_plan(muon_adamw* h) {
       M.pvec = (M.n % 8 == 0) && (reinterpret_cast<uintptr_t>(p.p) % 16 == 0) &&
                (reinterpret_cast<uintptr_t>(p.shadow) % 16 == 0);
       M.lr_mult = (float)(c.muon_lr_scale * c.moonlight_coef * sqrt((double)M.l));
+      pmaps.resize(2 * (size_t)(mat_index + 1));
+      M.tma = (c.ns_kernel == MA_NS_TCGEN05 && !(c.reserved[0] & 4) &&
+               tc_encode_param_maps(&pmaps[2 * (size_t)mat_index], M))
+                  ? 1
+                  : 0;
       M.tile_begin = (int)tiles.size();
       for (int r0 = 0; r0 < M.m; r0 += kMomTile)
         for (int c0 = 0; c0 < M.n; c0 += kMomTile) tiles.push_back(MomTile{mat_index, r0, c0, 0});
@@ -441,6 +451,9 @@ ma_status build_plan(muon_adamw* h) {
                              cudaMemcpyHostToDevice, h->s0));
   if (!mats.empty())
     CUDA_TRY(cudaMemcpyAsync(h->d_mats, mats.data(), mats.size() * sizeof(MuonMat), cudaMemcpyHostToDevice, h->s0));
+  if (!pmaps.empty())
+    CUDA_TRY(cudaMemcpyAsync(h->d_pmaps, pmaps.data(), pmaps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice,
+                             h->s0));
   if (!tiles.empty())
     CUDA_TRY(cudaMemcpyAsync(h->d_tiles, tiles.data(), tiles.size() * sizeof(MomTile), cudaMemcpyHostToDevice, h->s0));
   CUDA_TRY(cudaStreamSynchronize(h->s0));
@@ -464,6 +477,7 @@ ma_status build_plan(muon_adamw* h) {
         p.nmat = (int)B.params.size();
         p.mats = h->d_mats + B.mat0;
         p.rscale = h->d_rscale + B.mat0;
+        p.pmaps = h->d_pmaps + 2 * (size_t)B.mat0;
         p.first = it == 0;
         p.last = it == steps - 1;
         if (kind == NS_GRAM) {

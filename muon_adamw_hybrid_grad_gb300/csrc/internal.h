@@ -53,6 +53,7 @@ struct MuonMat {        // one Muon matrix (device-visible metadata)
   int32_t tile_begin;   // momentum tiles [tile_begin, tile_end) in the tile list
   int32_t tile_end;
   float lr_mult;        // muon_lr_scale * moonlight * sqrt(max(m, n))
+  int32_t tma;          // 1 if p (and shadow) have TMA maps: the last iteration moves them by TMA
 };
 
 struct MomTile {
@@ -102,6 +103,7 @@ struct NsProblem {
   uint16_t* out;        // GRAM: A; POLY: B; UPDATE: X'
   const MuonMat* mats;  // this bucket's matrices
   const float* rscale;  // per matrix 1 / (||update||_F + eps), same indexing
+  const CUtensorMap* pmaps;  // per matrix [2]: p (fp32) and shadow (bf16) maps, same indexing
   int32_t kind;
   int32_t S, L;
   int32_t M, N, K;
@@ -152,6 +154,10 @@ struct TcLaunch {
   int32_t stall_test;   // test hook: CTA 0's producer issues no loads (its waits then run out)
   int32_t pad;
 };
+// TMA maps of one parameter for the last iteration's write-back: maps[0] the
+// fp32 master, maps[1] the bf16 shadow (unused without one); 32 x 32 boxes.
+// False (and M.tma stays 0) when the layout does not allow TMA.
+bool tc_encode_param_maps(CUtensorMap* maps, const MuonMat& M);
 // Whether a problem can run in CTA pairs (its row blocks pair up).
 bool ns_tc_pairable(const NsProblem& p);
 // Encode the tensor maps of `tp` and count its work units for cluster size cl (host).

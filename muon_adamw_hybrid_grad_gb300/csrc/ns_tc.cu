@@ -40,7 +40,6 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int BN_MAX = 256;
-constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;      // 16 KB
 constexpr int B_STAGE = BN_MAX * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
@@ -48,8 +47,25 @@ constexpr int EPI_WARPS = 8;  // two warps per TMEM lane quarter, splitting the 
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int EPI_STAGE_WORDS = 32 * 16;  // one 32x32 bf16 block per warp (2 KiB)
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + EPI_WARPS * EPI_STAGE_WORDS * 4;
+constexpr int PBLOCK_BYTES = 32 * 32 * 4;  // one 32x32 fp32 parameter block
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Shared-memory layout (offsets from the 1024-byte aligned base). The last
+// iteration's variant (APPLY) trades one operand stage for two parameter
+// blocks per epilogue warp, into which p is fetched by TMA ahead of use.
+//   [stages][APPLY: 2 fp32 blocks per epilogue warp][bf16 block per epilogue warp][mbarriers, TMEM slot, flag]
+template <bool APPLY>
+struct Smem {
+  static constexpr int STAGES = APPLY ? 3 : 4;
+  static constexpr size_t PBUF = (size_t)STAGES * STAGE_BYTES;
+  static constexpr size_t SB = PBUF + (APPLY ? (size_t)EPI_WARPS * 2 * PBLOCK_BYTES : 0);
+  static constexpr size_t BARS = SB + (size_t)EPI_WARPS * EPI_STAGE_WORDS * 4;
+  // full[S], empty[S], tmem full[2], tmem empty[2], drain, APPLY: parameter blocks [2 per epilogue warp]
+  static constexpr int NBARS = 2 * STAGES + 5 + (APPLY ? 2 * EPI_WARPS : 0);
+  static constexpr size_t BYTES = 1024 + BARS + 256;
+  static_assert(NBARS * 8 + 8 <= 256, "barrier area");
+  static_assert(BYTES <= 232448, "shared memory per CTA");
+};
 
 // error codes written to the device flag
 constexpr int kErrWaitProducer = 0x101;
@@ -126,6 +142,20 @@ __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtens
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
       : "memory");
 }
+
+// Bulk tensor store of a shared-memory box (elements outside the tensor are
+// not written), tracked in this thread's bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until every bulk store this thread committed has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Generic-proxy writes to shared memory become visible to the TMA (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -408,18 +438,218 @@ __device__ __forceinline__ void epilogue_block(const NsProblem& pb, const NsEpiA
   }
 }
 
+// Last-iteration update of one 32x32 block straight from registers, for
+// parameters without TMA maps (unaligned rows or fewer than 32 of either
+// side): lane l holds canonical row row0 + l, columns col0..col0+31. Tall
+// parameters are read and written along their rows, so that the lanes'
+// addresses are contiguous; the others one element per lane-row.
+__device__ __forceinline__ void apply_block_direct(const MuonMat& M, const NsEpiArgs& ep, float rs, int row0,
+                                                   int col0, uint32_t taddr, int lane) {
+  uint32_t r[32];
+  tmem_ld_32x32b_x32(taddr, r);
+  tmem_ld_wait();
+  const int gi = row0 + lane;
+  const int cnt = M.l - col0 < 32 ? M.l - col0 : 32;
+  if (gi >= M.s || cnt <= 0) return;
+  const float lrm = ep.lr * M.lr_mult;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    if (e < cnt) {
+      const size_t po = M.transposed ? (size_t)(col0 + e) * M.n + gi : (size_t)gi * M.n + col0 + e;
+      const float q = fmaf(M.p[po], ep.decay, -lrm * (__uint_as_float(r[e]) * rs));
+      M.p[po] = q;
+      if (M.shadow) M.shadow[po] = ns_f2bf(q);
+    }
+  }
+}
+
+// Epilogue of the last Newton-Schulz iteration:
+//   p <- p (1 - lr wd) - lr_eff O,  O = B X read from TMEM and never stored.
+// For a matrix with TMA maps, each epilogue warp owns two 4 KiB fp32 block
+// buffers and its 2 KiB bf16 tile. When a tile starts (while its main loop
+// still runs) the warp fetches the parameter blocks of its first two 32x32
+// blocks by TMA; block k+1 is fetched as block k starts, into the buffer that
+// block k-1's stores have left. A block is updated in place in shared memory
+// and leaves through TMA stores of p and of its bf16 shadow. Elements outside
+// the parameter read as zero and are not written (the store clips them).
+// Blocks sit in shared memory in the 128-byte (fp32) and 64-byte (bf16)
+// swizzle layouts: the 16-byte chunk q of row r is at q ^ (r & 7), resp.
+// q ^ ((r >> 1) & 3), which keeps both the row-per-lane accesses (parameter
+// row = TMEM lane) and the column-per-lane ones (tall parameters, parameter
+// column = TMEM lane) free of bank conflicts. Matrices without maps take
+// epilogue_block.
+template <int CL>
+__device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem, size_t pbuf_off, size_t sb_off,
+                                               uint32_t pbar_base, uint32_t tmem_base, uint32_t tfull0,
+                                               uint32_t tempty0, volatile int* abort_flag, int warp, int lane,
+                                               uint32_t crank, int unit0, int nunits) {
+  const int w8 = warp - 2;
+  const int quarter = warp & 3;
+  const int half = w8 >> 2;
+  uint8_t* const pb = smem + pbuf_off + (size_t)w8 * 2 * PBLOCK_BYTES;
+  const uint32_t pb_s = smem_u32(pb);
+  uint8_t* const shb = smem + sb_off + (size_t)w8 * EPI_STAGE_WORDS * 4;
+  const uint32_t shb_s = smem_u32(shb);
+  const uint32_t bar0 = pbar_base + 16u * (uint32_t)w8;
+  const NsEpiArgs& ep = L.epi;
+  uint32_t ph = 0;    // bit b: parity of the next completion of buffer b
+  uint32_t pend = 0;  // bit b: a load into buffer b is in flight
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  for (int g = unit0; g < L.total_tiles; g += nunits) {
+    const TileCoord c = decode_tile(L, g);
+    const TcProblem& P = L.prob[c.prob];
+    const MuonMat& M = P.p.mats[c.mat];
+    const int row0 = (c.ti * CL + (int)crank) * BM + quarter * 32;
+    const int nb = P.bn / 64;                       // blocks of this warp in the tile
+    const int colw = c.tj * P.bn + 32 * half;       // canonical column of block 0; block k at +64k
+    const bool tma = M.tma != 0;
+    const bool tr = M.transposed != 0;
+    const bool has_shadow = M.shadow != nullptr;
+    const int s = M.s, l = M.l;
+    const CUtensorMap* maps = P.p.pmaps + 2 * c.mat;
+    if (tma) {
+      if (lane == 0) {
+        bulk_wait_read_all();  // the previous tile's stores have left both buffers
+        for (int k = 0; k < 2 && k < nb; ++k) {
+          const int cc = colw + 64 * k;
+          if (row0 < s && cc < l) {
+            mbar_expect_tx(bar0 + 8 * k, PBLOCK_BYTES);
+            tma_load_2d(pb_s + k * PBLOCK_BYTES, maps, tr ? row0 : cc, tr ? cc : row0, bar0 + 8 * k);
+          }
+        }
+      }
+      for (int k = 0; k < 2 && k < nb; ++k)
+        if (row0 < s && colw + 64 * k < l) pend |= 1u << k;
+      __syncwarp();
+    }
+    const bool got = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, L.err, kErrWaitEpilogue);
+    if (!__all_sync(0xffffffffu, got)) break;
+    tc_fence_after();
+    const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN_MAX);
+    bool ok = true;
+    for (int k = 0; k < nb; ++k) {
+      const int c0 = 32 * half + 64 * k;
+      const int cc = c.tj * P.bn + c0;
+      if (!tma) {
+        apply_block_direct(M, ep, P.p.first ? P.p.rscale[c.mat] : 1.f, row0, cc, tbase + (uint32_t)c0, lane);
+        continue;
+      }
+      if (k >= 1) {
+        const int cn = cc + 64;
+        const bool next = k + 1 < nb && row0 < s && cn < l;
+        if (lane == 0) {
+          bulk_wait_read_all();  // block k-1's stores have read its buffer and the bf16 tile
+          if (next) {
+            const int b = (k + 1) & 1;
+            mbar_expect_tx(bar0 + 8 * b, PBLOCK_BYTES);
+            tma_load_2d(pb_s + b * PBLOCK_BYTES, maps, tr ? row0 : cn, tr ? cn : row0, bar0 + 8 * b);
+          }
+        }
+        if (next) pend |= 1u << ((k + 1) & 1);
+        __syncwarp();
+      }
+      if (!(row0 < s && cc < l)) continue;
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tbase + (uint32_t)c0, r);
+      tmem_ld_wait();
+      const int b = k & 1;
+      const bool in = mbar_wait(bar0 + 8 * b, (ph >> b) & 1u, abort_flag, L.err, kErrWaitEpilogue);
+      if (!__all_sync(0xffffffffu, in)) {
+        ok = false;
+        break;
+      }
+      ph ^= 1u << b;
+      pend &= ~(1u << b);
+      const float rs = P.p.first ? P.p.rscale[c.mat] : 1.f;
+      const float lrm = ep.lr * M.lr_mult;
+      float o[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]) * rs;
+      uint8_t* const buf = pb + b * PBLOCK_BYTES;
+      if (!tr) {
+        // lane = parameter row row0 + lane; TMEM column e = parameter column cc + e
+        float4* const prow = reinterpret_cast<float4*>(buf + lane * 128);
+        uint4* const srow = reinterpret_cast<uint4*>(shb + lane * 64);
+#pragma unroll
+        for (int q = 0; q < 8; q += 2) {
+          float4 v0 = prow[q ^ (lane & 7)];
+          float4 v1 = prow[(q + 1) ^ (lane & 7)];
+          v0.x = fmaf(v0.x, ep.decay, -lrm * o[4 * q + 0]);
+          v0.y = fmaf(v0.y, ep.decay, -lrm * o[4 * q + 1]);
+          v0.z = fmaf(v0.z, ep.decay, -lrm * o[4 * q + 2]);
+          v0.w = fmaf(v0.w, ep.decay, -lrm * o[4 * q + 3]);
+          v1.x = fmaf(v1.x, ep.decay, -lrm * o[4 * q + 4]);
+          v1.y = fmaf(v1.y, ep.decay, -lrm * o[4 * q + 5]);
+          v1.z = fmaf(v1.z, ep.decay, -lrm * o[4 * q + 6]);
+          v1.w = fmaf(v1.w, ep.decay, -lrm * o[4 * q + 7]);
+          prow[q ^ (lane & 7)] = v0;
+          prow[(q + 1) ^ (lane & 7)] = v1;
+          if (has_shadow)
+            srow[(q >> 1) ^ ((lane >> 1) & 3)] = make_uint4(pack_bf16x2(v0.x, v0.y), pack_bf16x2(v0.z, v0.w),
+                                                            pack_bf16x2(v1.x, v1.y), pack_bf16x2(v1.z, v1.w));
+        }
+      } else {
+        // lane = parameter column row0 + lane; TMEM column e = parameter row cc + e
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float* const a = reinterpret_cast<float*>(buf + e * 128 + ((((lane >> 2) ^ (e & 7))) << 4) + (lane & 3) * 4);
+          const float q = fmaf(*a, ep.decay, -lrm * o[e]);
+          *a = q;
+          if (has_shadow)
+            *reinterpret_cast<uint16_t*>(shb + e * 64 + ((((lane >> 3) ^ ((e >> 1) & 3))) << 4) + (lane & 7) * 2) =
+                ns_f2bf(q);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int x = tr ? row0 : cc, y = tr ? cc : row0;
+        tma_store_2d(maps, pb_s + b * PBLOCK_BYTES, x, y);
+        if (has_shadow) tma_store_2d(maps + 1, shb_s, x, y);
+        bulk_commit();
+      }
+    }
+    if (!ok) break;
+    tc_fence_before();
+    mbar_arrive(tempty0 + 8 * acc);
+    if (++acc == 2) {
+      acc = 0;
+      acc_phase ^= 1u;
+    }
+  }
+  // Drain: the stores have read shared memory and loads still in flight
+  // (after an abort) have landed before the CTA may leave.
+  if (lane == 0) bulk_wait_read_all();
+  for (int b = 0; b < 2; ++b) {
+    if ((pend >> b) & 1u) {
+      const uint64_t t0 = global_timer();
+      while (!mbar_try_wait(bar0 + 8 * b, (ph >> b) & 1u)) {
+        if (global_timer() - t0 > kWaitLimitNs) {
+          atomicCAS(L.err, 0, kErrWaitEpilogue);
+          break;
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
 // CL = 1: one CTA per work unit. CL = 2: a cluster of two CTAs per unit of
 // two adjacent 128-row blocks that share the right-hand operand tile; each CTA
 // loads half of that tile and multicasts it into both CTAs' shared memory,
 // which cuts the L2 -> SM operand traffic per CTA from 48 KB to 32 KB per
 // k-block. The stage-release barrier then counts the MMA commits of both CTAs.
-template <int CL>
+template <int CL, bool APPLY>
 __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant__ TcLaunch L) {
+  using SM = Smem<APPLY>;
+  constexpr int STAGES = SM::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * STAGE_BYTES);
-  // bars[0..S): full, [S..2S): empty, [2S..2S+2): tmem full, [2S+2..2S+4): tmem empty, [2S+4]: drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::BARS);
+  // bars[0..S): full, [S..2S): empty, [2S..2S+2): tmem full, [2S+2..2S+4): tmem empty, [2S+4]: drain,
+  // APPLY: [2S+5 + 2w + b): parameter block b of epilogue warp w
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + SM::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -444,6 +674,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       mbar_init(tempty0 + 8 * a, EPI_WARPS * 32);
     }
     mbar_init(drain, 1);
+    for (int i = 2 * STAGES + 5; i < SM::NBARS; ++i) mbar_init(smem_u32(bars + i), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -590,11 +821,15 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
         }
       }
     }
+  } else if (APPLY) {
+    // ---------------- epilogue of the last iteration ----------------
+    apply_epilogue<CL>(L, smem, SM::PBUF, SM::SB, smem_u32(bars + 2 * STAGES + 5), tmem_base, tfull0, tempty0,
+                       abort_flag, warp, lane, crank, unit0, nunits);
   } else {
     // ---------------- epilogue ----------------
     const int quarter = warp & 3;      // TMEM lanes 32*quarter .. 32*quarter+31
     const int half = (warp - 2) >> 2;  // which alternate 32-column blocks
-    uint32_t* sb = reinterpret_cast<uint32_t*>(smem + (size_t)STAGES * STAGE_BYTES + 256) + (warp - 2) * EPI_STAGE_WORDS;
+    uint32_t* sb = reinterpret_cast<uint32_t*>(smem + SM::SB) + (warp - 2) * EPI_STAGE_WORDS;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int g = unit0; g < L.total_tiles; g += nunits) {
@@ -644,6 +879,19 @@ EncodeTiledFn get_encode_fn() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
   }
   return fn;
+}
+
+// cuTensorMapEncodeTiled of a row-major 2-D tensor.
+CUresult encode_rowmajor(CUtensorMap* tm, CUtensorMapDataType dt, size_t esize, const void* base, uint64_t cols,
+                         uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_SUPPORTED;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * esize};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 bool encode_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
@@ -708,13 +956,33 @@ bool tc_encode_problem(TcProblem& tp, int cl, char* errbuf, size_t errlen) {
   return true;
 }
 
-size_t ns_tc_smem_bytes() { return SMEM_BYTES; }
+bool tc_encode_param_maps(CUtensorMap* maps, const MuonMat& M) {
+  memset(maps, 0, 2 * sizeof(CUtensorMap));
+  const bool shadow = M.shadow != nullptr;
+  // row strides and base addresses on 16-byte boundaries; at least one full box per dimension
+  if (M.m < 32 || M.n < 32 || M.n % (shadow ? 8 : 4) != 0) return false;
+  if (reinterpret_cast<uintptr_t>(M.p) % 16 != 0 || (shadow && reinterpret_cast<uintptr_t>(M.shadow) % 16 != 0))
+    return false;
+  if (encode_rowmajor(&maps[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M.p, (uint64_t)M.n, (uint64_t)M.m, 32, 32,
+                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    return false;
+  if (shadow && encode_rowmajor(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M.shadow, (uint64_t)M.n,
+                                (uint64_t)M.m, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
+    return false;
+  return true;
+}
 
-cudaError_t ns_tc_prepare(int* max_pairs) {
-  cudaError_t e = cudaFuncSetAttribute(ns_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(ns_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-  if (e != cudaSuccess) return e;
+size_t ns_tc_smem_bytes() { return Smem<true>::BYTES > Smem<false>::BYTES ? Smem<true>::BYTES : Smem<false>::BYTES; }
+
+namespace {
+template <int CL, bool APPLY>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(ns_tc_kernel<CL, APPLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)Smem<APPLY>::BYTES);
+}
+
+template <bool APPLY>
+cudaError_t max_pairs_of(int* n) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -723,21 +991,16 @@ cudaError_t ns_tc_prepare(int* max_pairs) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Smem<APPLY>::BYTES;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, ns_tc_kernel<2>, &cfg);
-  if (e != cudaSuccess) return e;
-  *max_pairs = n;
-  return cudaSuccess;
+  return cudaOccupancyMaxActiveClusters(n, ns_tc_kernel<2, APPLY>, &cfg);
 }
 
-cudaError_t launch_ns_tc(const TcLaunch& L, int grid_units, cudaStream_t st) {
-  if (grid_units > L.total_tiles) grid_units = L.total_tiles;
-  if (grid_units <= 0) return cudaSuccess;
+template <bool APPLY>
+cudaError_t launch_variant(const TcLaunch& L, int grid_units, cudaStream_t st) {
   if (L.cl == 1) {
-    ns_tc_kernel<1><<<grid_units, THREADS, SMEM_BYTES, st>>>(L);
+    ns_tc_kernel<1, APPLY><<<grid_units, THREADS, Smem<APPLY>::BYTES, st>>>(L);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -748,11 +1011,33 @@ cudaError_t launch_ns_tc(const TcLaunch& L, int grid_units, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * grid_units, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Smem<APPLY>::BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, ns_tc_kernel<2>, L);
+  return cudaLaunchKernelEx(&cfg, ns_tc_kernel<2, APPLY>, L);
+}
+}  // namespace
+
+cudaError_t ns_tc_prepare(int* max_pairs) {
+  cudaError_t e;
+  if ((e = set_smem_attr<1, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<2, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<1, true>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<2, true>()) != cudaSuccess) return e;
+  int a = 0, b = 0;
+  if ((e = max_pairs_of<false>(&a)) != cudaSuccess) return e;
+  if ((e = max_pairs_of<true>(&b)) != cudaSuccess) return e;
+  *max_pairs = a < b ? a : b;
+  return cudaSuccess;
+}
+
+cudaError_t launch_ns_tc(const TcLaunch& L, int grid_units, cudaStream_t st) {
+  if (grid_units > L.total_tiles) grid_units = L.total_tiles;
+  if (grid_units <= 0) return cudaSuccess;
+  // every problem of a launch is the same product of the same iteration
+  const bool apply = L.prob[0].p.kind == NS_UPDATE && L.prob[0].p.last;
+  return apply ? launch_variant<true>(L, grid_units, st) : launch_variant<false>(L, grid_units, st);
 }
 
 }  // namespace ma

@@ -208,6 +208,39 @@ def test_tcgen05_matches_simt_kernel(mx):
             assert relative_frobenius(res[0][i], res[1][i]) < 5e-3, t.name
 
 
+@pytest.mark.parametrize("policy", ["bf16_mixed", "fp32_mixed"])
+def test_tma_writeback_matches_register_writeback(mx, policy):
+    """The last iteration's parameter update leaves through TMA for aligned
+    parameters and from registers otherwise (cross-check switch bit 2 forces
+    the latter). Both evaluate the same fp32 expression on the same
+    accumulator, so parameters and shadows agree bit for bit, including
+    blocks cut by the parameter's edges in both orientations."""
+    shapes = [(200, 136), (136, 200), (256, 1024), (1024, 256), (96, 1000), (1000, 72), (33, 64), (640, 384)]
+    t = [TensorSpec(f"model.action_expert.layers.{k}.mlp.w{k}.weight", sh) for k, sh in enumerate(shapes)]
+    t.append(TensorSpec("model.vlm.ln.weight", (64,)))
+    w = workloads.custom_workload("edges", t, policy=policy, steps=2)
+    masters = workloads.master_weights(w)
+    outs = []
+    for reserved in ([0], [4]):
+        gpu = GpuSide(w, masters, config={"reserved": reserved})
+        try:
+            for st in (1, 2):
+                gpu.load_grads(workloads.gradients(w, st))
+                gpu.step(w.lr)
+            outs.append(([gpu.param(i) for i in range(len(t))],
+                         [None if x is None else x.float().cpu().numpy() for x in gpu.S]))
+        finally:
+            gpu.close()
+    (pa, sa), (pb, sb) = outs
+    for i in range(len(t)):
+        assert np.array_equal(pa[i], pb[i]), t[i].name
+        if sa[i] is not None:
+            assert np.array_equal(sa[i], sb[i]), t[i].name
+    # and the TMA path itself is right against the oracle
+    r = run_parity(w)
+    assert r["worst_o"] <= O_TOL
+
+
 def test_checkpoint_roundtrip_bitwise(mx):
     """get_state/set_state/set_step resume: a restored optimizer continues
     bit for bit like the original."""
