@@ -135,6 +135,7 @@ constexpr int kTcMaxProblems = 4;
 struct TcProblem {
   CUtensorMap tmP;      // K-major loads of P, box {64, 128}
   CUtensorMap tmQ;      // GRAM/POLY: K-major box {64, 128}; UPDATE: MN-major box {64, 64}
+  CUtensorMap tmO;      // stores of the output, box {32, 32}
   NsProblem p;
   int32_t bn;           // N tile: 128 or 256
   int32_t tiles_m;      // M / 128

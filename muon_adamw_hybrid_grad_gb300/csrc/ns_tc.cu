@@ -42,24 +42,31 @@ constexpr int BK = 64;
 constexpr int BN_MAX = 256;
 constexpr int A_STAGE = BM * BK * 2;      // 16 KB
 constexpr int B_STAGE = BN_MAX * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int EPI_WARPS = 8;  // two warps per TMEM lane quarter, splitting the columns
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int EPI_STAGE_WORDS = 32 * 16;  // one 32x32 bf16 block per warp (2 KiB)
 constexpr int PBLOCK_BYTES = 32 * 32 * 4;  // one 32x32 fp32 parameter block
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
-// Shared-memory layout (offsets from the 1024-byte aligned base). The last
-// iteration's variant (APPLY) trades one operand stage for two parameter
+// Shared-memory layout (offsets from the 1024-byte aligned base). A stage
+// holds one 64-wide k-block of both operands: for a CTA that runs its own
+// MMAs, its 128 rows of the left operand and the whole right-hand tile; for a
+// CTA pair running one M = 256 MMA (PAIR), each CTA's own 128 rows and its
+// half of the right-hand tile, so a stage is two thirds of the bytes and the
+// ring deepens from 4 to 6 stages (the main loop is bound by TMA latency,
+// not by bandwidth). The
+// last iteration's variant (APPLY) trades operand stages for two parameter
 // blocks per epilogue warp, into which p is fetched by TMA ahead of use.
-//   [stages][APPLY: 2 fp32 blocks per epilogue warp][bf16 block per epilogue warp][mbarriers, TMEM slot, flag]
-template <bool APPLY>
+//   [stages][APPLY: 2 fp32 blocks per epilogue warp][bf16 tiles per epilogue warp][mbarriers, TMEM slot, flag]
+template <bool PAIR, bool APPLY>
 struct Smem {
-  static constexpr int STAGES = APPLY ? 3 : 4;
-  static constexpr size_t PBUF = (size_t)STAGES * STAGE_BYTES;
+  static constexpr int STAGE = A_STAGE + (PAIR ? B_STAGE / 2 : B_STAGE);
+  static constexpr int STAGES = PAIR ? (APPLY ? 4 : 6) : (APPLY ? 3 : 4);
+  static constexpr size_t PBUF = (size_t)STAGES * STAGE;
   static constexpr size_t SB = PBUF + (APPLY ? (size_t)EPI_WARPS * 2 * PBLOCK_BYTES : 0);
-  static constexpr size_t BARS = SB + (size_t)EPI_WARPS * EPI_STAGE_WORDS * 4;
+  // bf16 tiles per epilogue warp: APPLY the shadow tile; otherwise a row tile and a column tile
+  static constexpr size_t SB_PER_WARP = APPLY ? 2048 : 4096;
+  static constexpr size_t BARS = SB + (size_t)EPI_WARPS * SB_PER_WARP;
   // full[S], empty[S], tmem full[2], tmem empty[2], drain, APPLY: parameter blocks [2 per epilogue warp]
   static constexpr int NBARS = 2 * STAGES + 5 + (APPLY ? 2 * EPI_WARPS : 0);
   static constexpr size_t BYTES = 1024 + BARS + 256;
@@ -94,27 +101,38 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// CLUSTER: acquire at cluster scope (arrivals from the other CTA of a pair).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (CLUSTER)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
 // Wait until the phase of parity `parity` of `bar` has completed. Returns
 // false if the CTA is aborting or the wait ran past the limit (then the
 // abort flag and the device error code are set).
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
-                                       int code) {
-  if (mbar_try_wait(bar, parity)) return true;
+template <bool CLUSTER = false>
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, int code) {
+  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = global_timer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
       if (global_timer() - t0 > kWaitLimitNs) {
@@ -131,15 +149,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
       : "memory");
 }
 
@@ -171,27 +180,106 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// tcgen05 operations of one CTA (CL = 1) or of a CTA pair (CL = 2: one MMA of
+// M = 256 issued by the even CTA covers both CTAs' operands and accumulators).
+template <int CL>
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if constexpr (CL == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
+// Arrive on `bar` (this CTA) once this thread's prior MMAs have completed.
+template <int CL>
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+  if constexpr (CL == 1)
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Arrive (when this thread's prior MMAs complete) on the mbarrier at the same
-// shared-memory offset in every CTA of `cta_mask`.
+// The same, on the mbarrier at the same shared-memory offset in every CTA of
+// `cta_mask` (MMAs of this CTA alone).
 __device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
                    bar),
                "h"(cta_mask)
                : "memory");
+}
+
+// The same for the MMAs of a CTA pair, on both CTAs' mbarriers.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+template <int CL>
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  if constexpr (CL == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  } else {
+    // one warp of each CTA of the pair, collectively: the same columns in both
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+}
+
+template <int CL>
+__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t ncols) {
+  if constexpr (CL == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols) : "memory");
+}
+
+// Address of this CTA's shared-memory location `addr` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of any CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// TMA load of one box into the same shared-memory offset of every CTA in
+// `cta_mask`, completing on the mbarrier at the same offset in each.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar,
+                                                      uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier of the pair's other CTA (cluster address `bar`).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -223,15 +311,15 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, ui
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulate, bf16 A and B,
-// A K-major, B K-major or MN-major, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_bf16(int n, bool b_mn_major) {
+// A K-major, B K-major or MN-major, M = m (128, or 256 for a CTA pair), N = n.
+__device__ __forceinline__ uint32_t idesc_bf16(int m, int n, bool b_mn_major) {
   uint32_t d = 0;
   d |= 1u << 4;   // D format: f32
   d |= 1u << 7;   // A format: bf16
   d |= 1u << 10;  // B format: bf16
   if (b_mn_major) d |= 1u << 16;
   d |= (uint32_t)(n >> 3) << 17;
-  d |= (uint32_t)(BM >> 4) << 24;
+  d |= (uint32_t)(m >> 4) << 24;
   return d;
 }
 
@@ -278,42 +366,39 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)ns_f2bf(lo) | ((uint32_t)ns_f2bf(hi) << 16);
 }
 
-// Epilogue of one 32x32 block of the accumulator: rows row0..row0+31 (this
-// warp's TMEM lane quarter; lane l holds row row0 + l), columns
-// col0..col0+31 of matrix `mat`. Values are computed in registers in that
-// one-row-per-lane layout. Row-major stores go through the warp's 2 KiB
-// shared tile `sb16` as bf16 (four 16-byte stores and loads per lane; the
-// 16-byte chunk q of row r sits at chunk q ^ ((r >> 1) & 3), which keeps
-// both directions free of bank conflicts) and leave as 16-byte vectors of
-// which four lanes cover 64 contiguous bytes of a row. The mirrored half of
-// the symmetric products and the write-back into tall (transposed)
-// parameters are stored straight from registers: there the lanes' addresses
-// are contiguous. Only the b A term of B and the last iteration's
-// parameters are read from memory, and those loads are issued before TMEM is
-// read so that their latency overlaps it.
-__device__ __forceinline__ void epilogue_block(const NsProblem& pb, const NsEpiArgs& ep, int mat, int row0, int col0,
-                                               uint32_t taddr, uint32_t* sb16, int lane) {
+// Epilogue of one 32x32 block of the accumulator for A = X X^T,
+// B = a I + b A + c A A and the iterations' X' = B X (the last iteration has
+// its own epilogue): rows row0..row0+31 (this warp's TMEM lane quarter; lane
+// l holds row row0 + l), columns col0..col0+31 of matrix `mat`. Values are
+// computed in registers, written as bf16 into the warp's 2 KiB row tile `rt`
+// in the 64-byte swizzle layout (the 16-byte chunk q of row r at
+// q ^ ((r >> 1) & 3)) and leave with one TMA store, so that no global store
+// passes through the load/store units the operand feed shares. The
+// symmetric products store only blocks on or below the diagonal: a block
+// below it also leaves transposed, from the column tile that follows `rt`,
+// at the mirrored position; a block on it is completed to a symmetric block
+// in `rt` (upper half taken from the lower one) before its store, so every
+// element is written exactly once. Elements outside the matrix are stored as
+// zero (the workspaces' padding stays zero). Only the b A term of B is read
+// from memory, issued before TMEM is read so that its latency overlaps it.
+__device__ __forceinline__ void epilogue_block(const NsProblem& pb, const CUtensorMap* tmo, const NsEpiArgs& ep,
+                                               int mat, int row0, int col0, uint32_t taddr, uint8_t* rt, int lane) {
   const MuonMat& M = pb.mats[mat];
   const int s = M.s;
-  const int gi = row0 + lane;
   const bool update = pb.kind == NS_UPDATE;
-  const bool apply = update && pb.last;
+  const int lim = update ? M.l : s;          // valid columns
+  if (row0 >= s || col0 >= lim) return;      // padding only: never written
+  if (!update && col0 >= row0 + 32) return;  // above the diagonal: the mirror of a lower block
+  const int gi = row0 + lane;
   uint4 preA[4];
-  float4 preP[8];
   if (pb.kind == NS_POLY) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) preA[q] = make_uint4(0u, 0u, 0u, 0u);
-    if (gi < s && col0 <= gi) {  // A is stored in full (mirrored); padding is zero
+    if (gi < s) {  // A is stored in full (mirrored); padding is zero
       const uint4* ap = reinterpret_cast<const uint4*>(pb.aux + (size_t)mat * pb.S * pb.S + (size_t)gi * pb.S + col0);
 #pragma unroll
       for (int q = 0; q < 4; ++q) preA[q] = __ldg(ap + q);
     }
-  }
-  const bool pfull = apply && !M.transposed && gi < s && col0 + 32 <= M.l && M.pvec;
-  if (pfull) {
-    const float4* pp = reinterpret_cast<const float4*>(M.p + (size_t)gi * M.n + col0);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) preP[q] = pp[q];
   }
   uint32_t r[32];
   tmem_ld_32x32b_x32(taddr, r);
@@ -335,106 +420,56 @@ __device__ __forceinline__ void epilogue_block(const NsProblem& pb, const NsEpiA
       o[e] = fmaf(ep.c, __uint_as_float(r[e]), fmaf(ep.b, a, col0 + e == gi ? ep.a : 0.f));
     }
   }
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (gi >= s || col0 + e >= lim) o[e] = 0.f;
 
-  if (apply) {
-    // last Newton-Schulz iteration: p <- p (1 - lr wd) - lr_eff O, O never stored
-    const float lrm = ep.lr * M.lr_mult;
-    const int l = M.l;
-    if (M.transposed) {
-      // canonical row gi = parameter column; canonical column = parameter row
-      const int cnt = l - col0 < 32 ? l - col0 : 32;
-      if (gi < s && cnt > 0) {
-        float pv[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (e < cnt) pv[e] = M.p[(size_t)(col0 + e) * M.n + gi];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if (e < cnt) {
-            const size_t po = (size_t)(col0 + e) * M.n + gi;
-            const float q = fmaf(pv[e], ep.decay, -lrm * o[e]);
-            M.p[po] = q;
-            if (M.shadow) M.shadow[po] = ns_f2bf(q);
-          }
-        }
-      }
-    } else if (pfull) {
-      float4* pp = reinterpret_cast<float4*>(M.p + (size_t)gi * M.n + col0);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 v = preP[q];
-        v.x = fmaf(v.x, ep.decay, -lrm * o[4 * q + 0]);
-        v.y = fmaf(v.y, ep.decay, -lrm * o[4 * q + 1]);
-        v.z = fmaf(v.z, ep.decay, -lrm * o[4 * q + 2]);
-        v.w = fmaf(v.w, ep.decay, -lrm * o[4 * q + 3]);
-        pp[q] = v;
-        preP[q] = v;
-      }
-      if (M.shadow) {
-        uint4* sp = reinterpret_cast<uint4*>(M.shadow + (size_t)gi * M.n + col0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          w.x = pack_bf16x2(preP[2 * q].x, preP[2 * q].y);
-          w.y = pack_bf16x2(preP[2 * q].z, preP[2 * q].w);
-          w.z = pack_bf16x2(preP[2 * q + 1].x, preP[2 * q + 1].y);
-          w.w = pack_bf16x2(preP[2 * q + 1].z, preP[2 * q + 1].w);
-          sp[q] = w;
-        }
-      }
-    } else if (gi < s) {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        if (col0 + e < l) {
-          const size_t po = (size_t)gi * M.n + col0 + e;
-          const float q = fmaf(M.p[po], ep.decay, -lrm * o[e]);
-          M.p[po] = q;
-          if (M.shadow) M.shadow[po] = ns_f2bf(q);
-        }
-      }
-    }
-    return;
-  }
-
-  // bf16 row-major stores, staged through shared memory
-  const int ld = update ? pb.L : pb.S;
-  const size_t mbase = (size_t)mat * pb.S * ld;
-  const int lim = update ? M.l : s;  // valid columns
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    w.x = pack_bf16x2(o[8 * q + 0], o[8 * q + 1]);
-    w.y = pack_bf16x2(o[8 * q + 2], o[8 * q + 3]);
-    w.z = pack_bf16x2(o[8 * q + 4], o[8 * q + 5]);
-    w.w = pack_bf16x2(o[8 * q + 6], o[8 * q + 7]);
-    reinterpret_cast<uint4*>(sb16 + lane * 16)[q ^ ((lane >> 1) & 3)] = w;
-  }
+  uint8_t* const ct = rt + 2048;
+  if (lane == 0) bulk_wait_read_all();  // the previous block's stores have read both tiles
   __syncwarp();
+  uint4* const rrow = reinterpret_cast<uint4*>(rt + lane * 64);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int rr = (lane >> 2) + 8 * k, q = lane & 3;
-    const int gr = row0 + rr, gj = col0 + 8 * q;
-    const uint4 w = reinterpret_cast<const uint4*>(sb16 + rr * 16)[q ^ ((rr >> 1) & 3)];
-    const int hi = update ? lim : (gr + 1 < lim ? gr + 1 : lim);  // sym: columns j <= i only
-    if (gr < s && gj < hi) {
-      uint16_t* dst = pb.out + mbase + (size_t)gr * ld + gj;
-      if (gj + 8 <= hi) {
-        *reinterpret_cast<uint4*>(dst) = w;
-      } else {
-        for (int e = 0; e < 8 && gj + e < hi; ++e) {
-          const uint32_t u = u4_get(w, e >> 1);
-          dst[e] = (uint16_t)((e & 1) ? (u >> 16) : u);
-        }
-      }
-    }
-  }
-  __syncwarp();
-  if (!update && gi < s) {
-    // mirror: out[j][i] = out[i][j] for j < i; lanes hold consecutive i
-    uint16_t* col = pb.out + mbase + gi;
+  for (int q = 0; q < 4; ++q)
+    rrow[q ^ ((lane >> 1) & 3)] = make_uint4(pack_bf16x2(o[8 * q + 0], o[8 * q + 1]), pack_bf16x2(o[8 * q + 2], o[8 * q + 3]),
+                                             pack_bf16x2(o[8 * q + 4], o[8 * q + 5]), pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
+  // blocks are 32-aligned: one meets the diagonal iff col0 == row0
+  const bool diag = !update && col0 == row0;
+  const bool below = !update && col0 + 32 <= row0;
+  if (diag) {
+    __syncwarp();
+    // (row e, column lane) for e < lane <- (row lane, column e)
 #pragma unroll
     for (int e = 0; e < 32; ++e)
-      if (col0 + e < gi) col[(size_t)(col0 + e) * pb.S] = ns_f2bf(o[e]);
+      if (e < lane)
+        *reinterpret_cast<uint16_t*>(rt + e * 64 + (((lane >> 3) ^ ((e >> 1) & 3)) << 4) + (lane & 7) * 2) =
+            ns_f2bf(o[e]);
+  } else if (below) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      *reinterpret_cast<uint16_t*>(ct + e * 64 + (((lane >> 3) ^ ((e >> 1) & 3)) << 4) + (lane & 7) * 2) =
+          ns_f2bf(o[e]);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    const int y = mat * pb.S;
+    tma_store_2d(tmo, smem_u32(rt), col0, y + row0);
+    if (below) tma_store_2d(tmo, smem_u32(ct), row0, y + col0);
+    bulk_commit();
+  }
+}
+
+// An epilogue warp is done reading an accumulator from TMEM: one arrival per
+// warp on the MMA issuer's barrier (the leader's, for a CTA pair).
+template <bool PAIR>
+__device__ __forceinline__ void release_accumulator(uint32_t tempty, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) {
+    if (PAIR)
+      mbar_arrive_cluster(mapa_shared(tempty, 0));
+    else
+      mbar_arrive(tempty);
   }
 }
 
@@ -478,7 +513,7 @@ __device__ __forceinline__ void apply_block_direct(const MuonMat& M, const NsEpi
 // row = TMEM lane) and the column-per-lane ones (tall parameters, parameter
 // column = TMEM lane) free of bank conflicts. Matrices without maps take
 // epilogue_block.
-template <int CL>
+template <int CL, bool PAIR>
 __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem, size_t pbuf_off, size_t sb_off,
                                                uint32_t pbar_base, uint32_t tmem_base, uint32_t tfull0,
                                                uint32_t tempty0, volatile int* abort_flag, int warp, int lane,
@@ -488,7 +523,7 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
   const int half = w8 >> 2;
   uint8_t* const pb = smem + pbuf_off + (size_t)w8 * 2 * PBLOCK_BYTES;
   const uint32_t pb_s = smem_u32(pb);
-  uint8_t* const shb = smem + sb_off + (size_t)w8 * EPI_STAGE_WORDS * 4;
+  uint8_t* const shb = smem + sb_off + (size_t)w8 * Smem<PAIR, true>::SB_PER_WARP;
   const uint32_t shb_s = smem_u32(shb);
   const uint32_t bar0 = pbar_base + 16u * (uint32_t)w8;
   const NsEpiArgs& ep = L.epi;
@@ -611,8 +646,7 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
       }
     }
     if (!ok) break;
-    tc_fence_before();
-    mbar_arrive(tempty0 + 8 * acc);
+    release_accumulator<PAIR>(tempty0 + 8 * acc, lane);
     if (++acc == 2) {
       acc = 0;
       acc_phase ^= 1u;
@@ -635,14 +669,28 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
   __syncwarp();
 }
 
-// CL = 1: one CTA per work unit. CL = 2: a cluster of two CTAs per unit of
-// two adjacent 128-row blocks that share the right-hand operand tile; each CTA
-// loads half of that tile and multicasts it into both CTAs' shared memory,
-// which cuts the L2 -> SM operand traffic per CTA from 48 KB to 32 KB per
-// k-block. The stage-release barrier then counts the MMA commits of both CTAs.
-template <int CL, bool APPLY>
+// CL = 1: one CTA per work unit. CL = 2: a cluster of two CTAs (a CTA pair)
+// per unit of two adjacent 128-row blocks that share the right-hand operand
+// tile, in one of two ways:
+//   PAIR: the pair runs tcgen05.mma.cta_group::2 with M = 256. The even CTA
+//     (leader) issues every MMA, which reads each CTA's own 128 rows of the
+//     left operand and each CTA's half of the right-hand tile from that CTA's
+//     shared memory and accumulates into each CTA's own TMEM. Both CTAs load
+//     their parts by TMA; the odd CTA's copies complete on the leader's full
+//     barrier, whose expected byte count covers both. The leader's commits
+//     release each stage and each accumulator in both CTAs; both CTAs'
+//     epilogue warps release the accumulator on the leader's barrier. Used
+//     where the right-hand operand is K-major (X X^T, A A) and for the last
+//     iteration.
+//   otherwise: each CTA runs its own M = 128 MMAs; each loads half of the
+//     shared right-hand tile and multicasts it into both CTAs, and a stage is
+//     free once both CTAs' MMAs have read it. Used for X' = B X, whose
+//     MN-major right-hand operand ran slower through the paired MMA.
+template <int CL, bool APPLY, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant__ TcLaunch L) {
-  using SM = Smem<APPLY>;
+  static_assert(!PAIR || CL == 2, "a paired MMA needs a CTA pair");
+  constexpr int G = PAIR ? 2 : 1;  // tcgen05 cta_group
+  using SM = Smem<PAIR, APPLY>;
   constexpr int STAGES = SM::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -660,18 +708,22 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
   const uint32_t tempty0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
   const uint32_t crank = CL == 2 ? cluster_ctarank() : 0u;
-  const int unit0 = blockIdx.x / CL;   // this cluster's first work unit
-  const int nunits = gridDim.x / CL;   // clusters in the grid
+  const bool leader = crank == 0;
+  const bool issues_mma = !PAIR || leader;
+  const int unit0 = blockIdx.x / CL;  // this cluster's first work unit
+  const int nunits = gridDim.x / CL;  // clusters in the grid
   const uint16_t mc_mask = (uint16_t)((1u << CL) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, CL);  // one MMA commit per CTA of the cluster
+      mbar_init(full0 + 8 * s, 1);  // one producer arrival + the bytes of every copy
+      // one commit from each CTA whose MMAs read the stage
+      mbar_init(empty0 + 8 * s, PAIR ? 1 : CL);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, EPI_WARPS * 32);
+      // one arrival per epilogue warp of each CTA whose TMEM the MMAs write
+      mbar_init(tempty0 + 8 * a, (PAIR ? 2 : 1) * EPI_WARPS);
     }
     mbar_init(drain, 1);
     for (int i = 2 * STAGES + 5; i < SM::NBARS; ++i) mbar_init(smem_u32(bars + i), 1);
@@ -679,21 +731,16 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
+  if (warp == 1) tmem_alloc<G>(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
-  if (CL == 2) cluster_sync();  // the peer's barriers exist before any multicast reaches them
+  if (CL == 2) cluster_sync();  // the peer's barriers exist before any copy or commit reaches them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer (every CTA) ----------------
       for (int p = 0; p < L.nprob; ++p) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L.prob[p].tmP)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L.prob[p].tmQ)) : "memory");
@@ -710,30 +757,41 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
         const int kblocks = P.p.K / BK;
         const int rowP = c.mat * P.p.M + (c.ti * CL + (int)crank) * BM;
         const bool sym = P.p.kind != NS_UPDATE;
-        const uint32_t tx = (uint32_t)(A_STAGE + P.bn * BK * 2);
-        // right-hand operand boxes: 128 rows each (K-major) or 64 columns each (MN-major);
-        // with CL = 2 this CTA loads its half of them and multicasts
-        const int nbox = sym ? P.bn / BM : P.bn / 64;
-        const int box0 = (int)crank * (nbox / CL), box1 = box0 + nbox / CL;
+        // this CTA's part of the right-hand tile: columns [n0, n0 + bn / CL) of the
+        // column block, in boxes of 128 rows (K-major) or 64 columns (MN-major);
+        // PAIR keeps it here, otherwise it is multicast into both CTAs at its
+        // offset in the tile
+        const int nown = P.bn / CL;
+        const int n0 = c.tj * P.bn + (int)crank * nown;
+        const int nbox = sym ? nown / BM : nown / 64;
+        const uint32_t own_off = PAIR ? 0u : (uint32_t)crank * (uint32_t)nown * BK * 2u;
+        // bytes landing in this CTA per stage: its left rows + its (PAIR) or the whole right tile
+        const uint32_t tx = (uint32_t)(A_STAGE + (PAIR ? nown : P.bn) * BK * 2);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, L.err, kErrWaitProducer)) {
             ok = false;
             break;
           }
           const uint32_t fb = full0 + 8 * stage;
-          mbar_expect_tx(fb, tx);
-          const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+          const uint32_t sa = smem_u32(smem + (size_t)stage * SM::STAGE);
           const uint32_t sb = sa + A_STAGE;
-          tma_load_2d(sa, &P.tmP, kb * BK, rowP, fb);
-          for (int q = box0; q < box1; ++q) {
+          if (issues_mma) {
+            mbar_expect_tx(fb, (PAIR ? 2u : 1u) * tx);  // PAIR: both CTAs' copies complete here
+            tma_load_2d(sa, &P.tmP, kb * BK, rowP, fb);
+          } else {
+            tma_load_2d_pair(sa, &P.tmP, kb * BK, rowP, mapa_shared(fb, 0));
+          }
+          for (int q = 0; q < nbox; ++q) {
             // sym: rows (column block) of the same matrix, K-major; update: X, MN-major
-            const uint32_t dst = sb + q * (sym ? BM * BK * 2 : 64 * BK * 2);
-            const int x = sym ? kb * BK : c.tj * P.bn + q * 64;
-            const int y = sym ? c.mat * P.p.N + c.tj * P.bn + q * BM : c.mat * P.p.K + kb * BK;
-            if (CL == 1)
-              tma_load_2d(dst, &P.tmQ, x, y, fb);
-            else
+            const uint32_t dst = sb + own_off + q * (sym ? BM * BK * 2 : 64 * BK * 2);
+            const int x = sym ? kb * BK : n0 + q * 64;
+            const int y = sym ? c.mat * P.p.N + n0 + q * BM : c.mat * P.p.K + kb * BK;
+            if (PAIR && !leader)
+              tma_load_2d_pair(dst, &P.tmQ, x, y, mapa_shared(fb, 0));
+            else if (CL == 2 && !PAIR)
               tma_load_2d_multicast(dst, &P.tmQ, x, y, fb, mc_mask);
+            else
+              tma_load_2d(dst, &P.tmQ, x, y, fb);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -742,8 +800,11 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
           }
         }
       }
-      // Drain: wait for the copies of the most recent ring lap to land.
-      const int pending = issued < STAGES ? issued : STAGES;
+      // Drain: wait for the copies of the most recent ring lap to land. With
+      // PAIR the leader's full barriers count both CTAs' copies; the odd CTA's
+      // own copies are also covered by the leader's MMA drain (they are read
+      // by its MMAs) and by the closing cluster barrier.
+      const int pending = issues_mma ? (issued < STAGES ? issued : STAGES) : 0;
       int s = stage;
       uint32_t ph = phase;
       for (int i = 0; i < pending; ++i) {
@@ -751,7 +812,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
           s = STAGES - 1;
           ph ^= 1u;
         }
-        // full[s] completes phase `ph` when that copy lands; a dedicated
+        // full[s] completes phase `ph` when those copies land; a dedicated
         // bound keeps this loop finite even when the CTA is aborting.
         const uint64_t t0 = global_timer();
         while (!mbar_try_wait(full0 + 8 * s, ph)) {
@@ -763,8 +824,8 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    if (lane == 0 && issues_mma) {
+      // ---------------- MMA issuer (PAIR: the leader only) ----------------
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -775,10 +836,11 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
         const TcProblem& P = L.prob[c.prob];
         const int kblocks = P.p.K / BK;
         const bool sym = P.p.kind != NS_UPDATE;
-        const uint32_t idesc = idesc_bf16(P.bn, !sym);
+        const uint32_t idesc = idesc_bf16(G * BM, P.bn, !sym);
         const uint32_t lbo_mn = L.mn_swap ? 1024u : 64u * BK * 2u;
         const uint32_t sbo_mn = L.mn_swap ? 64u * BK * 2u : 1024u;
-        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, L.err, kErrWaitMma)) break;
+        // the epilogues (PAIR: of both CTAs) have released this accumulator
+        if (!mbar_wait<PAIR>(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, L.err, kErrWaitMma)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN_MAX);
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -787,32 +849,37 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+          const uint32_t sa = smem_u32(smem + (size_t)stage * SM::STAGE);
           const uint32_t sb = sa + A_STAGE;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = sdesc(sa + kk * 32, 16, 1024);
             const uint64_t bd = sym ? sdesc(sb + kk * 32, 16, 1024) : sdesc(sb + kk * 16 * 128, lbo_mn, sbo_mn);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16<G>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          if (CL == 1)
-            umma_commit(empty0 + 8 * stage);
+          if (PAIR)
+            umma_commit_pair(empty0 + 8 * stage);  // both CTAs' parts of this stage are free
+          else if (CL == 2)
+            umma_commit_multicast(empty0 + 8 * stage, mc_mask);  // this CTA no longer reads either copy
           else
-            umma_commit_multicast(empty0 + 8 * stage, mc_mask);  // both CTAs' copies of this stage are free
+            umma_commit<1>(empty0 + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(tfull0 + 8 * acc);
+        if (PAIR)
+          umma_commit_pair(tfull0 + 8 * acc);
+        else
+          umma_commit<1>(tfull0 + 8 * acc);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // Drain: every MMA issued above completes before TMEM is released.
-      umma_commit(drain);
+      umma_commit<G>(drain);
       const uint64_t t0 = global_timer();
       while (!mbar_try_wait(drain, 0)) {
         if (global_timer() - t0 > kWaitLimitNs) {
@@ -823,13 +890,13 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
     }
   } else if (APPLY) {
     // ---------------- epilogue of the last iteration ----------------
-    apply_epilogue<CL>(L, smem, SM::PBUF, SM::SB, smem_u32(bars + 2 * STAGES + 5), tmem_base, tfull0, tempty0,
+    apply_epilogue<CL, PAIR>(L, smem, SM::PBUF, SM::SB, smem_u32(bars + 2 * STAGES + 5), tmem_base, tfull0, tempty0,
                        abort_flag, warp, lane, crank, unit0, nunits);
   } else {
     // ---------------- epilogue ----------------
     const int quarter = warp & 3;      // TMEM lanes 32*quarter .. 32*quarter+31
     const int half = (warp - 2) >> 2;  // which alternate 32-column blocks
-    uint32_t* sb = reinterpret_cast<uint32_t*>(smem + SM::SB) + (warp - 2) * EPI_STAGE_WORDS;
+    uint8_t* const rt = smem + SM::SB + (size_t)(warp - 2) * SM::SB_PER_WARP;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int g = unit0; g < L.total_tiles; g += nunits) {
@@ -842,25 +909,24 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN_MAX);
       const int row0 = (c.ti * CL + (int)crank) * BM + quarter * 32;
       for (int c0 = 32 * half; c0 < P.bn; c0 += 64)
-        epilogue_block(P.p, L.epi, c.mat, row0, c.tj * P.bn + c0, tbase + (uint32_t)c0, sb, lane);
-      tc_fence_before();
-      mbar_arrive(tempty0 + 8 * acc);
+        epilogue_block(P.p, &P.tmO, L.epi, c.mat, row0, c.tj * P.bn + c0, tbase + (uint32_t)c0, rt, lane);
+      release_accumulator<PAIR>(tempty0 + 8 * acc, lane);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait_read_all();  // the stores have read shared memory before the CTA may leave
+    __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
-  // Neither CTA of a pair leaves while the other may still multicast into its
-  // shared memory or arrive on its barriers.
+  // Neither CTA of a pair leaves while the other may still read its shared
+  // memory or TMEM, or arrive on its barriers.
   if (CL == 2) cluster_sync();
   tc_fence_after();
-  if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
-  }
+  if (warp == 1) tmem_dealloc<G>(tmem_base, TMEM_COLS);
 }
 
 // ---- host side ----
@@ -944,6 +1010,12 @@ bool tc_encode_problem(TcProblem& tp, int cl, char* errbuf, size_t errlen) {
   tp.tiles_per_mat =
       p.kind == NS_UPDATE ? units_m * tp.tiles_n : ns_tc_num_tiles_sym(units_m, BM * cl, tp.bn);
   const uint64_t nm = (uint64_t)p.nmat;
+  // Output: [nmat * S] rows x (UPDATE: L, else S) cols, 32 x 32 bf16 blocks, 64-byte swizzle.
+  if (encode_rowmajor(&tp.tmO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, (uint64_t)(p.kind == NS_UPDATE ? p.L : p.S),
+                      nm * p.S, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS) {
+    snprintf(errbuf, errlen, "cuTensorMapEncodeTiled failed for the output of a %dx%d bucket", p.S, p.L);
+    return false;
+  }
   // Left operand: [nmat * M] rows x K cols, K-major tiles of 128 x 64.
   if (!encode_2d(&tp.tmP, p.P, (uint64_t)p.K, nm * p.M, BK, BM, errbuf, errlen)) return false;
   if (p.kind == NS_UPDATE) {
@@ -972,16 +1044,22 @@ bool tc_encode_param_maps(CUtensorMap* maps, const MuonMat& M) {
   return true;
 }
 
-size_t ns_tc_smem_bytes() { return Smem<true>::BYTES > Smem<false>::BYTES ? Smem<true>::BYTES : Smem<false>::BYTES; }
-
-namespace {
-template <int CL, bool APPLY>
-cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(ns_tc_kernel<CL, APPLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)Smem<APPLY>::BYTES);
+size_t ns_tc_smem_bytes() {
+  size_t m = Smem<false, false>::BYTES;
+  if (Smem<false, true>::BYTES > m) m = Smem<false, true>::BYTES;
+  if (Smem<true, false>::BYTES > m) m = Smem<true, false>::BYTES;
+  if (Smem<true, true>::BYTES > m) m = Smem<true, true>::BYTES;
+  return m;
 }
 
-template <bool APPLY>
+namespace {
+template <int CL, bool APPLY, bool PAIR>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(ns_tc_kernel<CL, APPLY, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)Smem<PAIR, APPLY>::BYTES);
+}
+
+template <bool APPLY, bool PAIR>
 cudaError_t max_pairs_of(int* n) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -991,18 +1069,14 @@ cudaError_t max_pairs_of(int* n) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Smem<APPLY>::BYTES;
+  cfg.dynamicSmemBytes = Smem<PAIR, APPLY>::BYTES;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, ns_tc_kernel<2, APPLY>, &cfg);
+  return cudaOccupancyMaxActiveClusters(n, ns_tc_kernel<2, APPLY, PAIR>, &cfg);
 }
 
-template <bool APPLY>
-cudaError_t launch_variant(const TcLaunch& L, int grid_units, cudaStream_t st) {
-  if (L.cl == 1) {
-    ns_tc_kernel<1, APPLY><<<grid_units, THREADS, Smem<APPLY>::BYTES, st>>>(L);
-    return cudaGetLastError();
-  }
+template <bool APPLY, bool PAIR>
+cudaError_t launch_pair(const TcLaunch& L, int grid_units, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1011,24 +1085,27 @@ cudaError_t launch_variant(const TcLaunch& L, int grid_units, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * grid_units, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Smem<APPLY>::BYTES;
+  cfg.dynamicSmemBytes = Smem<PAIR, APPLY>::BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, ns_tc_kernel<2, APPLY>, L);
+  return cudaLaunchKernelEx(&cfg, ns_tc_kernel<2, APPLY, PAIR>, L);
 }
 }  // namespace
 
 cudaError_t ns_tc_prepare(int* max_pairs) {
   cudaError_t e;
-  if ((e = set_smem_attr<1, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<2, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<1, true>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<2, true>()) != cudaSuccess) return e;
-  int a = 0, b = 0;
-  if ((e = max_pairs_of<false>(&a)) != cudaSuccess) return e;
-  if ((e = max_pairs_of<true>(&b)) != cudaSuccess) return e;
-  *max_pairs = a < b ? a : b;
+  if ((e = set_smem_attr<1, false, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<1, true, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<2, false, true>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<2, false, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<2, true, true>()) != cudaSuccess) return e;
+  int a = 0, b = 0, c = 0;
+  if ((e = max_pairs_of<false, true>(&a)) != cudaSuccess) return e;
+  if ((e = max_pairs_of<false, false>(&b)) != cudaSuccess) return e;
+  if ((e = max_pairs_of<true, true>(&c)) != cudaSuccess) return e;
+  int m = a < b ? a : b;
+  *max_pairs = m < c ? m : c;
   return cudaSuccess;
 }
 
@@ -1036,8 +1113,18 @@ cudaError_t launch_ns_tc(const TcLaunch& L, int grid_units, cudaStream_t st) {
   if (grid_units > L.total_tiles) grid_units = L.total_tiles;
   if (grid_units <= 0) return cudaSuccess;
   // every problem of a launch is the same product of the same iteration
-  const bool apply = L.prob[0].p.kind == NS_UPDATE && L.prob[0].p.last;
-  return apply ? launch_variant<true>(L, grid_units, st) : launch_variant<false>(L, grid_units, st);
+  const bool update = L.prob[0].p.kind == NS_UPDATE;
+  const bool apply = update && L.prob[0].p.last;
+  if (L.cl == 1) {
+    if (apply)
+      ns_tc_kernel<1, true, false><<<grid_units, THREADS, Smem<false, true>::BYTES, st>>>(L);
+    else
+      ns_tc_kernel<1, false, false><<<grid_units, THREADS, Smem<false, false>::BYTES, st>>>(L);
+    return cudaGetLastError();
+  }
+  if (apply) return launch_pair<true, true>(L, grid_units, st);
+  if (update) return launch_pair<false, false>(L, grid_units, st);
+  return launch_pair<false, true>(L, grid_units, st);
 }
 
 }  // namespace ma
