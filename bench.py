@@ -43,12 +43,13 @@ STREAM_KINDS = ("grad_norm", "momentum", "adamw")
 
 
 # DRAM bytes per ns_tc_kernel launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# capture of the 6-layer case of this workload (profiles/ns_tc_kernel_expert1024x6.md: one launch of
-# each product), scaled to the 16-layer h1024 workload by the matrices processed (16/6) and averaged
-# over the three products. It describes only the kernel sources it was measured on: any change to
-# them makes it null until it is measured again.
-NS_TRAFFIC = {"sources_sha256": "7275095b701724277b8aa633dbe433eca812e2060ea7c295e76a60b0d0bdd941",
-              "bytes_per_launch": 760909824, "workload": "h1024"}
+# capture of the 6-layer case of this workload (the ns_tc_kernel summary in profiles/: one launch of
+# each product of a middle iteration and the last iteration's launch), averaged over a step's 15
+# launches (5 X X^T, 5 A A, 4 B X, 1 last) and scaled to the 16-layer h1024 workload by the matrices
+# processed (16/6: each launch reads its operands once and writes its output once). It describes only
+# the kernel sources it was measured on: any change to them makes it null until it is measured again.
+NS_TRAFFIC = {"sources_sha256": "928b62ef6b51bccb0a49348c10c36eec69e51d34998fce29e9cd96958509f67a",
+              "bytes_per_launch": 897413939, "workload": "h1024"}
 NS_SOURCES = ("ns_tc.cu", "ns_epilogue.cuh", "internal.h")
 
 
