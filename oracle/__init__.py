@@ -21,8 +21,10 @@ U diag(phi^5(sigma)) V^T, the quintic's singular-value band, the polar factor,
 transpose and scale invariance, rank-1 closed forms of the full Muon update,
 closed-form AdamW trajectories (t = 1 sign step, constant gradient, zero
 gradient, unrolled EMAs), hand-computed clip factors and lr scalings, the
-schedule's closed-form points and the routing table. No function here is
-"parity unpinned".
+schedule's closed-form points and the routing table; the variants (exponential-
+average momentum, coefficient schedules, per-parameter lr / weight-decay
+multipliers, the bias/norm decay exemption) against unrolled sums, composed
+SVD closed forms and hand-solved steps. No function here is "parity unpinned".
 """
 from .hybrid import (  # noqa: F401
     DEFAULTS,
@@ -36,6 +38,7 @@ from .hybrid import (  # noqa: F401
     clip_coefficient,
     nesterov_momentum,
     zeropower_newton_schulz5,
+    decay_exempt,
     muon_lr,
     muon_apply,
     adamw_update,

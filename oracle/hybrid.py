@@ -42,6 +42,12 @@ DEFAULTS: Dict[str, object] = {
     "weight_decay": 0.1,
     "muon_weight_decay": 0.1,
     "clip_eps": 1e-6,
+    # Variants off by default (the page's step uses none of them): the
+    # exponential-average form of the momentum, a per-iteration coefficient
+    # schedule, and no weight decay on biases and normalisation weights.
+    "muon_momentum_form": "sgd",
+    "ns_schedule": None,
+    "adam_decay_exempt_bias_norm": False,
 }
 
 READINGS = {
@@ -58,6 +64,12 @@ READINGS = {
     "clip": "coef = min(1, max_norm/(total+1e-6)) over both groups' gradients, before either update; "
             "a NaN norm gives a NaN coefficient, an infinite norm gives 0",
     "schedule": "HF cosine_with_min_lr, num_cycles 0.5, lr = base*(min + (1-min)*0.5*(1+cos(pi*p)))",
+    "momentum_form_ema": "variant: buf = mu*buf + (1-mu)*g; update = (1-mu)*g + mu*buf (Nesterov) or buf",
+    "ns_schedule": "variant: iteration i uses its own (a_i, b_i, c_i) in the same three products",
+    "param_options": "per parameter, like a PyTorch parameter group: lr_i = lr*lr_scale and "
+                     "wd_i = wd*wd_scale, used in both the step and the decoupled decay",
+    "decay_exempt": "variant: an AdamW parameter whose lower-cased name ends with 'bias' or contains "
+                    "'norm' has wd_scale 0 unless set explicitly",
 }
 
 
@@ -129,14 +141,26 @@ def clip_coefficient(total: float, max_norm: float, eps: float = 1e-6) -> float:
 # Muon -- OpenDM article, 核心揭秘一 / Muon 的工作原理 and 关键超参默认值
 # ---------------------------------------------------------------------------
 
-def nesterov_momentum(buf: np.ndarray, g: np.ndarray, mu: float, nesterov: bool = True):
+def nesterov_momentum(buf: np.ndarray, g: np.ndarray, mu: float, nesterov: bool = True,
+                      form: str = "sgd"):
     """Momentum buffer update and the update direction fed to Newton-Schulz.
 
-    buf <- mu * buf + g; the Nesterov look-ahead direction is g + mu * buf.
-    Returns (new_buf, direction).
+    form "sgd" (the step's reading of muon_nesterov): buf <- mu * buf + g,
+    and the Nesterov look-ahead direction is g + mu * buf.
+    form "ema" (a variant): the buffer is an exponential average,
+    buf <- mu * buf + (1 - mu) * g, and the look-ahead direction is
+    (1 - mu) * g + mu * buf.
+    Without Nesterov the direction is the buffer itself. Returns
+    (new_buf, direction).
     """
-    new_buf = mu * buf + g
-    direction = g + mu * new_buf if nesterov else new_buf.copy()
+    if form == "sgd":
+        w = 1.0
+    elif form == "ema":
+        w = 1.0 - mu
+    else:
+        raise ValueError(f"unknown momentum form {form!r}")
+    new_buf = mu * buf + w * g
+    direction = w * g + mu * new_buf if nesterov else new_buf.copy()
     return new_buf, direction
 
 
@@ -148,20 +172,36 @@ def zeropower_newton_schulz5(G: np.ndarray, steps: int = 5,
     Works on the short side: a tall matrix is transposed first and the
     result transposed back. The matrix is scaled to unit Frobenius norm, then
     each iteration forms A = X X^T, B = b A + c A A and X <- a X + B X.
+    ``coefficients`` is one (a, b, c) used in every iteration, or a sequence
+    of ``steps`` triples, the i-th used in iteration i (a schedule).
     """
-    a, b, c = coefficients
+    coeffs = np.asarray(coefficients, dtype=np.float64)
+    if coeffs.ndim == 1:
+        schedule = [tuple(coeffs)] * steps
+    else:
+        if coeffs.shape != (steps, 3):
+            raise ValueError(f"a schedule needs {steps} triples, got shape {coeffs.shape}")
+        schedule = [tuple(row) for row in coeffs]
     X = np.array(G, dtype=np.float64)
     tall = X.shape[0] > X.shape[1]
     if tall:
         X = X.T
     X = X / (np.linalg.norm(X) + eps)
-    for _ in range(steps):
+    for a, b, c in schedule:
         A = X @ X.T
         B = b * A + c * (A @ A)
         X = a * X + B @ X
     if tall:
         X = X.T
     return X
+
+
+def decay_exempt(name: str) -> bool:
+    """Biases and normalisation weights take no weight decay when the
+    exemption variant is on (the convention of HF Trainer's selection of
+    decay parameters; the defaults table lists one weight_decay for all)."""
+    low = name.lower()
+    return low.endswith("bias") or "norm" in low
 
 
 def muon_lr(lr: float, rows: int, cols: int, muon_lr_scale: float = 1.0,
@@ -226,7 +266,7 @@ class HybridOracle:
 
     def __init__(self, names: Sequence[str], shapes: Sequence[Sequence[int]],
                  frozen: Optional[Sequence[bool]] = None, *, optim: str = "muon_adamw",
-                 **overrides):
+                 param_options: Optional[Dict[int, Sequence[float]]] = None, **overrides):
         cfg = dict(DEFAULTS)
         cfg.update(overrides)
         self.cfg = cfg
@@ -235,6 +275,15 @@ class HybridOracle:
         fz = list(frozen) if frozen is not None else [False] * len(self.names)
         self.groups = [route(n, len(s), frozen=f, optim=optim)
                        for n, s, f in zip(self.names, self.shapes, fz)]
+        # per parameter (lr_scale, wd_scale): explicit options win over the exemption rule
+        self.options = []
+        for i, (n, grp) in enumerate(zip(self.names, self.groups)):
+            ls, ws = 1.0, 1.0
+            if cfg["adam_decay_exempt_bias_norm"] and grp == GROUP_ADAMW and decay_exempt(n):
+                ws = 0.0
+            if param_options and i in param_options:
+                ls, ws = (float(x) for x in param_options[i])
+            self.options.append((ls, ws))
         self.t = 0
         self.buf: Dict[int, np.ndarray] = {}
         self.m: Dict[int, np.ndarray] = {}
@@ -257,26 +306,29 @@ class HybridOracle:
         active = [i for i, g in enumerate(self.groups) if g != GROUP_FROZEN]
         total = global_grad_norm([grads[i] for i in active])
         coef = clip_coefficient(total, float(cfg["max_grad_norm"]), float(cfg["clip_eps"]))
-        a_b_c = tuple(cfg["ns_coefficients"])
+        a_b_c = cfg["ns_schedule"] if cfg["ns_schedule"] is not None else tuple(cfg["ns_coefficients"])
         beta1, beta2 = cfg["adam_betas"]
         out_O: Dict[int, np.ndarray] = {}
         for i in active:
             g = coef * np.asarray(grads[i], dtype=np.float64)
+            ls, ws = self.options[i]
+            lr_i = lr * ls
             if self.groups[i] == GROUP_MUON:
                 self.buf[i], direction = nesterov_momentum(
-                    self.buf[i], g, float(cfg["muon_momentum"]), bool(cfg["muon_nesterov"]))
+                    self.buf[i], g, float(cfg["muon_momentum"]), bool(cfg["muon_nesterov"]),
+                    str(cfg["muon_momentum_form"]))
                 if muon_indices is not None and i not in muon_indices:
                     continue
                 O = zeropower_newton_schulz5(direction, int(cfg["muon_ns_steps"]), a_b_c,
                                              float(cfg["ns_eps"]))
                 rows, cols = self.shapes[i]
-                lr_eff = muon_lr(lr, rows, cols, float(cfg["muon_lr_scale"]),
+                lr_eff = muon_lr(lr_i, rows, cols, float(cfg["muon_lr_scale"]),
                                  float(cfg["muon_moonlight_coefficient"]))
-                params[i][...] = muon_apply(params[i], O, lr, float(cfg["muon_weight_decay"]), lr_eff)
+                params[i][...] = muon_apply(params[i], O, lr_i, float(cfg["muon_weight_decay"]) * ws, lr_eff)
                 out_O[i] = O
             else:
-                p, m, v = adamw_update(params[i], g, self.m[i], self.v[i], t, lr, float(beta1),
-                                       float(beta2), float(cfg["adam_eps"]), float(cfg["weight_decay"]))
+                p, m, v = adamw_update(params[i], g, self.m[i], self.v[i], t, lr_i, float(beta1),
+                                       float(beta2), float(cfg["adam_eps"]), float(cfg["weight_decay"]) * ws)
                 params[i][...] = p
                 self.m[i], self.v[i] = m, v
         return {"total": total, "coef": coef, "O": out_O, "t": t}
