@@ -70,6 +70,16 @@ typedef enum { MA_BF16_MIXED = 0, MA_FP32_MIXED = 1 } ma_precision;           /*
 typedef enum { MA_GROUP_AUTO = 0, MA_GROUP_MUON = 1, MA_GROUP_ADAMW = 2, MA_GROUP_FROZEN = 3 } ma_group;
 typedef enum { MA_DT_F32 = 0, MA_DT_BF16 = 1 } ma_dtype;
 typedef enum { MA_NS_TCGEN05 = 0, MA_NS_SIMT = 1 } ma_ns_kernel;
+/* Form of the Muon momentum. SGD (the step's reading of muon_nesterov):
+ * buf <- mu buf + g, update g + mu buf. EMA (a variant): buf <- mu buf +
+ * (1 - mu) g, update (1 - mu) g + mu buf. Without Nesterov the update is buf. */
+typedef enum { MA_MOMENTUM_SGD = 0, MA_MOMENTUM_EMA = 1 } ma_momentum_form;
+
+/* Longest per-iteration coefficient schedule (ns_schedule_len <= this). */
+#define MA_NS_SCHEDULE_MAX 16
+/* Distinct (lr_scale, weight_decay_scale) pairs over all parameters,
+ * including the default (1, 1) (see muon_adamw_set_param_options). */
+#define MA_MAX_OPTION_GROUPS 8
 
 /* Optimizer configuration. Fill with muon_adamw_config_init(), then edit.
  * Defaults (article section in brackets):
@@ -95,8 +105,18 @@ typedef struct {
    * exchanges the strides of the MN-major operand descriptor (a wrong layout
    * that parity must catch); bit 1 runs every Newton-Schulz product without
    * CTA pairs; bit 2 writes the last iteration's parameters from registers
-   * instead of through TMA. reserved[1..6] must be 0. */
-  int32_t reserved[7];
+   * instead of through TMA. reserved[1..3] must be 0. */
+  int32_t reserved[4];
+  int32_t muon_momentum_form;          /* ma_momentum_form; default MA_MOMENTUM_SGD */
+  /* 1: AdamW parameters whose lower-cased name ends with "bias" or contains
+   * "norm" take no weight decay (the HF Trainer convention), unless
+   * muon_adamw_set_param_options sets them. Default 0: one weight_decay for
+   * all, as the article's defaults table lists it. */
+  int32_t adam_decay_exempt_bias_norm;
+  /* 0: every Newton-Schulz iteration uses (ns_a, ns_b, ns_c). Otherwise it
+   * must equal ns_steps (<= MA_NS_SCHEDULE_MAX) and iteration i uses
+   * ns_schedule[i] = {a, b, c}. */
+  int32_t ns_schedule_len;
   /* Real-valued settings are doubles (like Python floats); the kernels get
    * fp32 values derived from them on the host, e.g. 1 - adam_beta2 is formed
    * in double before rounding, so 0.999 yields exactly fp32(0.001). */
@@ -109,6 +129,7 @@ typedef struct {
   double adam_beta1, adam_beta2, adam_eps, adam_weight_decay;
   double max_grad_norm;
   double clip_eps;
+  double ns_schedule[MA_NS_SCHEDULE_MAX][3];
 } muon_adamw_config;
 
 /* Per-kernel timing collected while profiling is on (see muon_adamw_set_profiling).
@@ -192,6 +213,20 @@ MA_API ma_status muon_adamw_register_param(muon_adamw_t* h, const char* name, in
                                     float* param_fp32, const void* grad, int grad_dtype,
                                     void* param_bf16_shadow, int group_override, int* assigned,
                                     int* index_out);
+
+/* Per-parameter multipliers, like a PyTorch parameter group: parameter
+ * `index` (registration order) steps with lr * lr_scale, and its decoupled
+ * weight decay is weight_decay * weight_decay_scale with that lr. For AdamW:
+ * p <- p (1 - lr ls wd ws) - (lr ls / bc1) m / (sqrt(v / bc2) + eps); for a
+ * Muon matrix: p <- p (1 - lr ls muon_wd ws) - lr ls muon_lr_scale 0.2
+ * sqrt(max(m, n)) O. Default (1, 1); an explicit call overrides
+ * adam_decay_exempt_bias_norm for that parameter. Call before the first step.
+ * Errors: MA_ERR_ARG (NULL handle, index out of range, a scale negative or
+ * not finite), MA_ERR_STATE (after the first step, or a frozen parameter),
+ * MA_ERR_UNSUPPORTED (more than MA_MAX_OPTION_GROUPS distinct pairs; the
+ * exemption rule's pairs count too and are checked at the first step). */
+MA_API ma_status muon_adamw_set_param_options(muon_adamw_t* h, int index, double lr_scale,
+                                              double weight_decay_scale);
 
 /* One optimizer step with base learning rate `lr` (the caller applies its
  * schedule, stepped once per optimizer step). The first call freezes the

@@ -44,6 +44,10 @@ MA_DT_F32 = 0
 MA_DT_BF16 = 1
 MA_NS_TCGEN05 = 0
 MA_NS_SIMT = 1
+MA_MOMENTUM_SGD = 0
+MA_MOMENTUM_EMA = 1
+MA_NS_SCHEDULE_MAX = 16
+MA_MAX_OPTION_GROUPS = 8
 
 KERNEL_KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "adamw", "ns_apply")
 MA_K_COUNT = len(KERNEL_KINDS)
@@ -57,7 +61,10 @@ class MuonAdamWConfig(ctypes.Structure):
         ("muon_nesterov", ctypes.c_int32),
         ("ns_steps", ctypes.c_int32),
         ("ns_kernel", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 7),
+        ("reserved", ctypes.c_int32 * 4),
+        ("muon_momentum_form", ctypes.c_int32),
+        ("adam_decay_exempt_bias_norm", ctypes.c_int32),
+        ("ns_schedule_len", ctypes.c_int32),
         ("muon_momentum", ctypes.c_double),
         ("ns_a", ctypes.c_double),
         ("ns_b", ctypes.c_double),
@@ -72,6 +79,7 @@ class MuonAdamWConfig(ctypes.Structure):
         ("adam_weight_decay", ctypes.c_double),
         ("max_grad_norm", ctypes.c_double),
         ("clip_eps", ctypes.c_double),
+        ("ns_schedule", (ctypes.c_double * 3) * MA_NS_SCHEDULE_MAX),
     ]
 
 
@@ -126,6 +134,7 @@ _SIGNATURES = {
     "muon_adamw_step": (ctypes.c_int, [_P, ctypes.c_double, ctypes.POINTER(ctypes.c_float)]),
     "muon_adamw_sync": (ctypes.c_int, [_P]),
     "muon_adamw_test_arm_stall": (ctypes.c_int, [_P]),
+    "muon_adamw_set_param_options": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_double, ctypes.c_double]),
     "muon_adamw_get_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),
     "muon_adamw_set_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),
     "muon_adamw_get_step": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int64)]),
@@ -218,6 +227,11 @@ def muon_adamw_step(h: int, lr: float, want_norm: bool = False) -> Optional[floa
 
 def muon_adamw_sync(h: int) -> None:
     _check(load_library().muon_adamw_sync(_P(h)))
+
+
+def muon_adamw_set_param_options(h: int, index: int, lr_scale: float, weight_decay_scale: float) -> None:
+    _check(load_library().muon_adamw_set_param_options(_P(h), int(index), float(lr_scale),
+                                                       float(weight_decay_scale)))
 
 
 def muon_adamw_test_arm_stall(h: int) -> None:
@@ -314,6 +328,18 @@ class MuonAdamW:
                 for i, x in enumerate(v):
                     cfg.reserved[i] = int(x)
                 continue
+            if k == "ns_schedule":
+                # a list of (a, b, c) per iteration, or None for the constant triple
+                rows = [] if v is None else [tuple(float(x) for x in r) for r in v]
+                if len(rows) > MA_NS_SCHEDULE_MAX or any(len(r) != 3 for r in rows):
+                    raise ValueError(f"ns_schedule: at most {MA_NS_SCHEDULE_MAX} triples")
+                cfg.ns_schedule_len = len(rows)
+                for i, r in enumerate(rows):
+                    for j in range(3):
+                        cfg.ns_schedule[i][j] = r[j]
+                continue
+            if k == "muon_momentum_form" and isinstance(v, str):
+                v = {"sgd": MA_MOMENTUM_SGD, "ema": MA_MOMENTUM_EMA}[v]
             if not hasattr(cfg, k):
                 raise TypeError(f"unknown config field {k!r}")
             setattr(cfg, k, v)
@@ -349,6 +375,9 @@ class MuonAdamW:
         except Exception:
             self.close()
             raise
+
+    def set_param_options(self, index: int, lr_scale: float = 1.0, weight_decay_scale: float = 1.0) -> None:
+        muon_adamw_set_param_options(self.handle, index, lr_scale, weight_decay_scale)
 
     def step(self, lr: float, want_norm: bool = False):
         return muon_adamw_step(self.handle, lr, want_norm)

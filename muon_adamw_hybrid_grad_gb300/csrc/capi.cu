@@ -11,6 +11,7 @@
 // Everything on the device runs in the kernels of stream_kernels.cu, ns_tc.cu
 // (and the ns_simt.cu cross-check); this file plans, allocates and launches.
 #include <cuda_runtime.h>
+#include <ctype.h>
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -94,6 +95,9 @@ struct Param {
   int group = MA_GROUP_ADAMW;
   float* st0 = nullptr;  // Muon buf or AdamW m
   float* st1 = nullptr;  // AdamW v
+  double lr_scale = 1.0, wd_scale = 1.0;  // per-parameter multipliers
+  bool options_set = false;               // set explicitly (wins over the exemption rule)
+  int og = 0;                             // option group (index into the per-step tables)
 };
 
 struct Bucket {
@@ -127,6 +131,7 @@ struct muon_adamw {
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   std::vector<Param> params;
   bool planned = false;
+  std::vector<std::pair<double, double>> option_groups;  // (lr_scale, wd_scale); [0] = (1, 1)
   int64_t t = 0;
 
   // arena
@@ -210,6 +215,14 @@ ma_status fold_profile(muon_adamw* h) {
   }
   h->prof_pending.clear();
   return MA_OK;
+}
+
+// Biases and normalisation weights (HF Trainer's decay-exemption convention).
+bool decay_exempt_name(const std::string& name) {
+  std::string low(name);
+  for (char& ch : low) ch = (char)tolower((unsigned char)ch);
+  const bool bias = low.size() >= 4 && low.compare(low.size() - 4, 4, "bias") == 0;
+  return bias || low.find("norm") != std::string::npos;
 }
 
 ma_status check_device_flag(muon_adamw* h) {
@@ -375,6 +388,25 @@ ma_status build_plan(muon_adamw* h) {
       norm_chunks.push_back(gc);
     }
   }
+  // option groups: distinct (lr_scale, wd_scale) pairs, group 0 = (1, 1)
+  h->option_groups.assign(1, {1.0, 1.0});
+  for (Param& p : h->params) {
+    if (p.group == MA_GROUP_FROZEN) continue;
+    if (!p.options_set) {
+      p.lr_scale = 1.0;
+      p.wd_scale = (c.adam_decay_exempt_bias_norm && p.group == MA_GROUP_ADAMW && decay_exempt_name(p.name)) ? 0.0 : 1.0;
+    }
+    const std::pair<double, double> key{p.lr_scale, p.wd_scale};
+    size_t gi = 0;
+    while (gi < h->option_groups.size() && h->option_groups[gi] != key) ++gi;
+    if (gi == h->option_groups.size()) {
+      if ((int)gi == kMaxOptionGroups)
+        return fail(MA_ERR_UNSUPPORTED, "more than %d distinct (lr_scale, weight_decay_scale) pairs",
+                    kMaxOptionGroups);
+      h->option_groups.push_back(key);
+    }
+    p.og = (int)gi;
+  }
   for (int pi : h->adam_params) {
     const Param& p = h->params[pi];
     const size_t es = p.gdtype == MA_DT_BF16 ? 2 : 4;
@@ -392,6 +424,8 @@ ma_status build_plan(muon_adamw* h) {
       const uintptr_t pa = reinterpret_cast<uintptr_t>(a.p), ga = reinterpret_cast<uintptr_t>(a.g),
                       sa = reinterpret_cast<uintptr_t>(a.shadow);
       a.vec = (pa % 16 == 0) && (ga % (a.gdtype == DT_BF16 ? 8 : 16) == 0) && (sa % 8 == 0);
+      a.group = p.og;
+      a.pad = 0;
       adam_chunks.push_back(a);
     }
   }
@@ -420,7 +454,8 @@ ma_status build_plan(muon_adamw* h) {
       M.vec = (M.n % 8 == 0) && (reinterpret_cast<uintptr_t>(p.g) % 16 == 0);
       M.pvec = (M.n % 8 == 0) && (reinterpret_cast<uintptr_t>(p.p) % 16 == 0) &&
                (reinterpret_cast<uintptr_t>(p.shadow) % 16 == 0);
-      M.lr_mult = (float)(c.muon_lr_scale * c.moonlight_coef * sqrt((double)M.l));
+      M.lr_mult = (float)(p.lr_scale * c.muon_lr_scale * c.moonlight_coef * sqrt((double)M.l));
+      M.group = p.og;
       pmaps.resize(2 * (size_t)(mat_index + 1));
       M.tma = (c.ns_kernel == MA_NS_TCGEN05 && !(c.reserved[0] & 4) &&
                tc_encode_param_maps(&pmaps[2 * (size_t)mat_index], M))
@@ -549,13 +584,23 @@ ma_status build_plan(muon_adamw* h) {
   return MA_OK;
 }
 
-void set_epi(NsEpiArgs& e, const muon_adamw_config& c, double lr) {
-  e.a = (float)c.ns_a;
-  e.b = (float)c.ns_b;
-  e.c = (float)c.ns_c;
-  e.decay = (float)(1.0 - lr * c.muon_weight_decay);
+// Epilogue scalars of Newton-Schulz iteration `it`: its coefficients (the
+// schedule's, if one is set) and, per option group, the decoupled decay
+// 1 - lr * lr_scale * muon_wd * wd_scale (formed in double, rounded once).
+void set_epi(NsEpiArgs& e, const muon_adamw_config& c, const std::vector<std::pair<double, double>>& groups,
+             double lr, int it) {
+  const bool sched = c.ns_schedule_len > 0;
+  e.a = (float)(sched ? c.ns_schedule[it][0] : c.ns_a);
+  e.b = (float)(sched ? c.ns_schedule[it][1] : c.ns_b);
+  e.c = (float)(sched ? c.ns_schedule[it][2] : c.ns_c);
   e.lr = (float)lr;
+  for (int g = 0; g < kMaxOptionGroups; ++g) {
+    const double ls = g < (int)groups.size() ? groups[g].first : 1.0;
+    const double ws = g < (int)groups.size() ? groups[g].second : 1.0;
+    e.decay[g] = (float)(1.0 - lr * ls * c.muon_weight_decay * ws);
+  }
 }
+
 
 ma_status valid_config(const muon_adamw_config* c) {
   if (c->mode != MA_MODE_MUON_ADAMW && c->mode != MA_MODE_ADAMW_ONLY) return fail(MA_ERR_ARG, "bad mode %d", c->mode);
@@ -563,6 +608,19 @@ ma_status valid_config(const muon_adamw_config* c) {
     return fail(MA_ERR_ARG, "bad precision %d", c->precision);
   if (c->ns_steps < 1 || c->ns_steps > 64) return fail(MA_ERR_ARG, "ns_steps must be in [1, 64]");
   if (c->ns_kernel != MA_NS_TCGEN05 && c->ns_kernel != MA_NS_SIMT) return fail(MA_ERR_ARG, "bad ns_kernel");
+  if (c->muon_momentum_form != MA_MOMENTUM_SGD && c->muon_momentum_form != MA_MOMENTUM_EMA)
+    return fail(MA_ERR_ARG, "bad muon_momentum_form %d", c->muon_momentum_form);
+  if (c->adam_decay_exempt_bias_norm != 0 && c->adam_decay_exempt_bias_norm != 1)
+    return fail(MA_ERR_ARG, "adam_decay_exempt_bias_norm must be 0 or 1");
+  if (c->ns_schedule_len != 0) {
+    if (c->ns_schedule_len != c->ns_steps || c->ns_schedule_len > MA_NS_SCHEDULE_MAX)
+      return fail(MA_ERR_ARG, "ns_schedule_len must be 0 or equal ns_steps (<= %d)", MA_NS_SCHEDULE_MAX);
+    for (int i = 0; i < c->ns_schedule_len; ++i)
+      for (int k = 0; k < 3; ++k)
+        if (!isfinite(c->ns_schedule[i][k])) return fail(MA_ERR_ARG, "non-finite ns_schedule entry");
+  }
+  for (int i = 1; i < 4; ++i)
+    if (c->reserved[i] != 0) return fail(MA_ERR_ARG, "reserved[%d] must be 0", i);
   if (!(c->adam_beta1 >= 0.0 && c->adam_beta1 < 1.0) || !(c->adam_beta2 >= 0.0 && c->adam_beta2 < 1.0))
     return fail(MA_ERR_ARG, "betas must lie in [0, 1)");
   if (!(c->adam_eps >= 0.0) || !(c->ns_eps >= 0.0) || !(c->clip_eps >= 0.0)) return fail(MA_ERR_ARG, "eps < 0");
@@ -729,16 +787,21 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
     a.omb1 = (float)(1.0 - c.adam_beta1);
     a.omb2 = (float)(1.0 - c.adam_beta2);
     a.eps = (float)c.adam_eps;
-    a.decay = (float)(1.0 - lr * c.adam_weight_decay);
     const double bc1 = 1.0 - pow(c.adam_beta1, t), bc2 = 1.0 - pow(c.adam_beta2, t);
-    a.step_size = (float)(lr / bc1);
+    for (int g = 0; g < kMaxOptionGroups; ++g) {
+      const double ls = g < (int)h->option_groups.size() ? h->option_groups[g].first : 1.0;
+      const double ws = g < (int)h->option_groups.size() ? h->option_groups[g].second : 1.0;
+      a.decay[g] = (float)(1.0 - lr * ls * c.adam_weight_decay * ws);
+      a.step_size[g] = (float)(lr * ls / bc1);
+    }
     a.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
     timed(h, MA_K_ADAMW, h->s1, h->bytes_adam,
           [&] { launch_adamw(h->d_adam_chunks, h->n_adam_chunks, h->d_scalars, a, h->adam_grid, h->s1); });
   }
 
   if (h->n_mats > 0) {
-    MomArgs ma_{(float)c.muon_momentum, c.muon_nesterov};
+    MomArgs ma_{(float)c.muon_momentum, c.muon_nesterov,
+                c.muon_momentum_form == MA_MOMENTUM_EMA ? (float)(1.0 - c.muon_momentum) : 1.0f};
     timed(h, MA_K_MOMENTUM, h->s0, h->bytes_mom, [&] {
       launch_muon_momentum(h->d_tiles, h->n_tiles, h->d_mats, h->d_scalars, ma_, h->d_tile_partials, h->mom_grid,
                            h->s0);
@@ -746,9 +809,9 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
     timed(h, MA_K_NS_PREP, h->s0, (double)h->n_tiles * 4,
           [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, (float)c.ns_eps, h->d_rscale, h->s0); });
     NsEpiArgs epi;
-    set_epi(epi, c, lr);
     const double units[3] = {h->unit_gram, h->unit_poly, h->unit_update};
     for (int it = 0; it < c.ns_steps; ++it) {
+      set_epi(epi, c, h->option_groups, lr, it);
       for (int kind = 0; kind < 3; ++kind) {
         if (c.ns_kernel == MA_NS_TCGEN05) {
           for (TcLaunch& L : h->tc[kind][it]) {
@@ -782,6 +845,35 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
     ma_status st = check_device_flag(h);
     if (st != MA_OK) return st;
   }
+  return ok();
+}
+
+ma_status muon_adamw_set_param_options(muon_adamw_t* h, int index, double lr_scale, double weight_decay_scale) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  if (index < 0 || index >= (int)h->params.size()) return fail(MA_ERR_ARG, "bad parameter index %d", index);
+  if (!(lr_scale >= 0.0) || !isfinite(lr_scale) || !(weight_decay_scale >= 0.0) || !isfinite(weight_decay_scale))
+    return fail(MA_ERR_ARG, "scales must be finite and >= 0");
+  if (h->planned) return fail(MA_ERR_STATE, "set_param_options after the first step (plan is frozen)");
+  Param& p = h->params[index];
+  if (p.group == MA_GROUP_FROZEN) return fail(MA_ERR_STATE, "parameter %d is frozen", index);
+  // count the distinct explicit pairs with this one (the rule's pairs are checked at the first step)
+  std::vector<std::pair<double, double>> seen{{1.0, 1.0}};
+  for (size_t i = 0; i < h->params.size(); ++i) {
+    const Param& q = h->params[i];
+    std::pair<double, double> key;
+    if ((int)i == index)
+      key = {lr_scale, weight_decay_scale};
+    else if (q.options_set && q.group != MA_GROUP_FROZEN)
+      key = {q.lr_scale, q.wd_scale};
+    else
+      continue;
+    if (std::find(seen.begin(), seen.end(), key) == seen.end()) seen.push_back(key);
+  }
+  if ((int)seen.size() > kMaxOptionGroups)
+    return fail(MA_ERR_UNSUPPORTED, "more than %d distinct (lr_scale, weight_decay_scale) pairs", kMaxOptionGroups);
+  p.lr_scale = lr_scale;
+  p.wd_scale = weight_decay_scale;
+  p.options_set = true;
   return ok();
 }
 

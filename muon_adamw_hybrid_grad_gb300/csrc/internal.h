@@ -35,6 +35,8 @@ struct AdamChunk {      // one slice of one AdamW parameter
   int64_t n;
   int32_t gdtype;
   int32_t vec;          // 1 if every pointer allows 4-wide vector access
+  int32_t group;        // option group: index into AdamArgs' per-group decay and step size
+  int32_t pad;
 };
 
 struct MuonMat {        // one Muon matrix (device-visible metadata)
@@ -54,6 +56,7 @@ struct MuonMat {        // one Muon matrix (device-visible metadata)
   int32_t tile_end;
   float lr_mult;        // muon_lr_scale * moonlight * sqrt(max(m, n))
   int32_t tma;          // 1 if p (and shadow) have TMA maps: the last iteration moves them by TMA
+  int32_t group;        // option group: index into NsEpiArgs::decay
 };
 
 struct MomTile {
@@ -68,24 +71,29 @@ struct StepScalars {    // written on the device each step
   float pad0, pad1;
 };
 
+// Distinct (lr_scale, weight_decay_scale) pairs of the parameters, group 0
+// being (1, 1); each chunk or matrix names its group.
+constexpr int kMaxOptionGroups = 8;
+
 struct AdamArgs {
   float beta1, beta2, omb1, omb2, eps;
-  float decay;          // 1 - lr * wd
-  float step_size;      // lr / (1 - beta1^t)
-  float inv_sqrt_bc2;   // 1 / sqrt(1 - beta2^t)
+  float inv_sqrt_bc2;                // 1 / sqrt(1 - beta2^t)
+  float decay[kMaxOptionGroups];     // 1 - lr * lr_scale * wd * wd_scale
+  float step_size[kMaxOptionGroups]; // lr * lr_scale / (1 - beta1^t)
 };
 
 struct MomArgs {
   float mu;
   int32_t nesterov;
+  float gscale;         // weight of the clipped gradient: 1, or 1 - mu for the exponential-average form
 };
 
 enum NsKind : int32_t { NS_GRAM = 0, NS_POLY = 1, NS_UPDATE = 2 };
 
 struct NsEpiArgs {
-  float a, b, c;
-  float decay;          // 1 - lr * muon_wd
+  float a, b, c;                 // this iteration's coefficients
   float lr;
+  float decay[kMaxOptionGroups]; // 1 - lr * lr_scale * muon_wd * wd_scale
 };
 
 // One grouped GEMM problem: all same-shape matrices of one bucket. The

@@ -487,11 +487,12 @@ __device__ __forceinline__ void apply_block_direct(const MuonMat& M, const NsEpi
   const int cnt = M.l - col0 < 32 ? M.l - col0 : 32;
   if (gi >= M.s || cnt <= 0) return;
   const float lrm = ep.lr * M.lr_mult;
+  const float dec = ep.decay[M.group];
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     if (e < cnt) {
       const size_t po = M.transposed ? (size_t)(col0 + e) * M.n + gi : (size_t)gi * M.n + col0 + e;
-      const float q = fmaf(M.p[po], ep.decay, -lrm * (__uint_as_float(r[e]) * rs));
+      const float q = fmaf(M.p[po], dec, -lrm * (__uint_as_float(r[e]) * rs));
       M.p[po] = q;
       if (M.shadow) M.shadow[po] = ns_f2bf(q);
     }
@@ -598,6 +599,7 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
       pend &= ~(1u << b);
       const float rs = P.p.first ? P.p.rscale[c.mat] : 1.f;
       const float lrm = ep.lr * M.lr_mult;
+      const float dec = ep.decay[M.group];
       float o[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]) * rs;
@@ -610,14 +612,14 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
         for (int q = 0; q < 8; q += 2) {
           float4 v0 = prow[q ^ (lane & 7)];
           float4 v1 = prow[(q + 1) ^ (lane & 7)];
-          v0.x = fmaf(v0.x, ep.decay, -lrm * o[4 * q + 0]);
-          v0.y = fmaf(v0.y, ep.decay, -lrm * o[4 * q + 1]);
-          v0.z = fmaf(v0.z, ep.decay, -lrm * o[4 * q + 2]);
-          v0.w = fmaf(v0.w, ep.decay, -lrm * o[4 * q + 3]);
-          v1.x = fmaf(v1.x, ep.decay, -lrm * o[4 * q + 4]);
-          v1.y = fmaf(v1.y, ep.decay, -lrm * o[4 * q + 5]);
-          v1.z = fmaf(v1.z, ep.decay, -lrm * o[4 * q + 6]);
-          v1.w = fmaf(v1.w, ep.decay, -lrm * o[4 * q + 7]);
+          v0.x = fmaf(v0.x, dec, -lrm * o[4 * q + 0]);
+          v0.y = fmaf(v0.y, dec, -lrm * o[4 * q + 1]);
+          v0.z = fmaf(v0.z, dec, -lrm * o[4 * q + 2]);
+          v0.w = fmaf(v0.w, dec, -lrm * o[4 * q + 3]);
+          v1.x = fmaf(v1.x, dec, -lrm * o[4 * q + 4]);
+          v1.y = fmaf(v1.y, dec, -lrm * o[4 * q + 5]);
+          v1.z = fmaf(v1.z, dec, -lrm * o[4 * q + 6]);
+          v1.w = fmaf(v1.w, dec, -lrm * o[4 * q + 7]);
           prow[q ^ (lane & 7)] = v0;
           prow[(q + 1) ^ (lane & 7)] = v1;
           if (has_shadow)
@@ -629,7 +631,7 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           float* const a = reinterpret_cast<float*>(buf + e * 128 + ((((lane >> 2) ^ (e & 7))) << 4) + (lane & 3) * 4);
-          const float q = fmaf(*a, ep.decay, -lrm * o[e]);
+          const float q = fmaf(*a, dec, -lrm * o[e]);
           *a = q;
           if (has_shadow)
             *reinterpret_cast<uint16_t*>(shb + e * 64 + ((((lane >> 3) ^ ((e >> 1) & 3))) << 4) + (lane & 7) * 2) =

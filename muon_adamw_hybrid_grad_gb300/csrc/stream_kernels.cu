@@ -183,8 +183,9 @@ __global__ void __launch_bounds__(kClipThreads) clip_finalize_kernel(const float
 // ---------------------------------------------------------------------------
 // Muon momentum + canonical bf16 pack.
 // One 64x64 tile of one parameter per iteration; 256 threads, each owns an
-// 8-wide column group of two rows. buf <- mu*buf + coef*g; the update
-// (Nesterov: coef*g + mu*buf) goes to X in bf16. Wide matrices (X = update)
+// 8-wide column group of two rows. buf <- mu*buf + w*coef*g; the update
+// (Nesterov: w*coef*g + mu*buf) goes to X in bf16; w = 1, or 1 - mu for the
+// exponential-average form of the momentum. Wide matrices (X = update)
 // are written straight from registers, 16 bytes per thread, with no block
 // barrier. Tall matrices (X = update^T) go through a shared-memory tile,
 // double-buffered so that one barrier per tile suffices. Sum of squares of
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kMomThreads) muon_momentum_kernel(const MomTil
                                                                     const StepScalars* __restrict__ sc, MomArgs args,
                                                                     float* __restrict__ tile_partials) {
   __shared__ __align__(16) uint16_t su[2][kMomTile][kMomTile + 8];
-  const float coef = sc->coef;
+  const float coef = sc->coef * args.gscale;
   const float mu = args.mu;
   const int cg = threadIdx.x & 7;   // column group (8 columns)
   const int rr = threadIdx.x >> 3;  // row 0..31
@@ -334,19 +335,22 @@ __global__ void __launch_bounds__(kPrepThreads) ns_prep_kernel(const MuonMat* __
 // ---------------------------------------------------------------------------
 constexpr int kAdamThreads = 256;
 
-__device__ __forceinline__ void adam_one(float& p, float& m, float& v, float g, float coef, const AdamArgs& a) {
+__device__ __forceinline__ void adam_one(float& p, float& m, float& v, float g, float coef, const AdamArgs& a,
+                                         float decay, float step_size) {
   const float gh = coef * g;
   m = fmaf(a.beta1, m, a.omb1 * gh);
   v = fmaf(a.beta2, v, a.omb2 * gh * gh);
   const float denom = fmaf(sqrtf(v), a.inv_sqrt_bc2, a.eps);
-  p = fmaf(p, a.decay, -a.step_size * (m / denom));
+  p = fmaf(p, decay, -step_size * (m / denom));
 }
 
 __global__ void __launch_bounds__(kAdamThreads) adamw_kernel(const AdamChunk* __restrict__ chunks, int nchunks,
-                                                             const StepScalars* __restrict__ sc, AdamArgs a) {
+                                                             const StepScalars* __restrict__ sc,
+                                                             const __grid_constant__ AdamArgs a) {
   const float coef = sc->coef;
   for (int c = blockIdx.x; c < nchunks; c += gridDim.x) {
     const AdamChunk ch = chunks[c];
+    const float decay = a.decay[ch.group], step_size = a.step_size[ch.group];
     const int64_t nv = ch.vec ? ch.n / 4 : 0;
     float4* pv = reinterpret_cast<float4*>(ch.p);
     float4* mv = reinterpret_cast<float4*>(ch.m);
@@ -364,10 +368,10 @@ __global__ void __launch_bounds__(kAdamThreads) adamw_kernel(const AdamChunk* __
         const float4 w = __ldg(reinterpret_cast<const float4*>(ch.g) + i);
         g[0] = w.x; g[1] = w.y; g[2] = w.z; g[3] = w.w;
       }
-      adam_one(p.x, m.x, v.x, g[0], coef, a);
-      adam_one(p.y, m.y, v.y, g[1], coef, a);
-      adam_one(p.z, m.z, v.z, g[2], coef, a);
-      adam_one(p.w, m.w, v.w, g[3], coef, a);
+      adam_one(p.x, m.x, v.x, g[0], coef, a, decay, step_size);
+      adam_one(p.y, m.y, v.y, g[1], coef, a, decay, step_size);
+      adam_one(p.z, m.z, v.z, g[2], coef, a, decay, step_size);
+      adam_one(p.w, m.w, v.w, g[3], coef, a, decay, step_size);
       pv[i] = p;
       mv[i] = m;
       vv[i] = v;
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__(kAdamThreads) adamw_kernel(const AdamChunk* __
       float p = ch.p[j], m = ch.m[j], v = ch.v[j];
       const float g = ch.gdtype == DT_BF16 ? bf2f(static_cast<const uint16_t*>(ch.g)[j])
                                             : static_cast<const float*>(ch.g)[j];
-      adam_one(p, m, v, g, coef, a);
+      adam_one(p, m, v, g, coef, a, decay, step_size);
       ch.p[j] = p;
       ch.m[j] = m;
       ch.v[j] = v;

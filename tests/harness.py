@@ -103,24 +103,28 @@ def relative_frobenius(got: np.ndarray, want: np.ndarray) -> float:
 def run_parity(w: workloads.Workload, *, steps: Optional[int] = None, config: Optional[dict] = None,
                oracle_overrides: Optional[dict] = None, muon_sample: Optional[Sequence[int]] = None,
                grad_scale: float = 1.0, lr: Optional[float] = None, check_states: bool = True,
-               optim: str = "muon_adamw") -> Dict[str, object]:
+               optim: str = "muon_adamw",
+               param_options: Optional[Dict[int, Sequence[float]]] = None) -> Dict[str, object]:
     """Run ``steps`` optimizer steps on both sides and assert parity.
 
     ``muon_sample``: Muon parameter indices whose Newton-Schulz output is
     checked (all when None). Every AdamW/momentum element is checked when
-    ``check_states`` is set.
+    ``check_states`` is set. ``param_options``: {index: (lr_scale,
+    weight_decay_scale)} given to both sides.
     """
     steps = steps or w.steps
     lr = w.lr if lr is None else lr
     masters = workloads.master_weights(w)
     gpu = GpuSide(w, masters, config=config)
     try:
+        for i, (ls, ws) in (param_options or {}).items():
+            gpu.opt.set_param_options(i, ls, ws)
         cfg = gpu.opt.cfg
         names = [t.name for t in w.tensors]
         shapes = [t.shape for t in w.tensors]
         frozen = [t.frozen for t in w.tensors]
         ov = dict(oracle_overrides or {})
-        orc = oracle.HybridOracle(names, shapes, frozen, optim=optim, **ov)
+        orc = oracle.HybridOracle(names, shapes, frozen, optim=optim, param_options=param_options, **ov)
         groups = orc.groups
         assert groups == gpu.opt.groups, "routing differs between the C ABI and the oracle"
         muon_idx = [i for i, g in enumerate(groups) if g == "muon"]
@@ -143,7 +147,6 @@ def run_parity(w: workloads.Workload, *, steps: Optional[int] = None, config: Op
                 f"step {step}: norm {total_gpu} vs {res['total']}"
             coef = res["coef"]
             # --- Muon: momentum (all elements) and O (sampled) ---
-            decay = _f32(1.0 - lr * cfg.muon_weight_decay)
             for i in muon_idx:
                 ghat = np.abs(coef * grads[i].astype(np.float64))
                 sum_abs_g[i] = sum_abs_g.get(i, 0.0) + ghat
@@ -153,7 +156,9 @@ def run_parity(w: workloads.Workload, *, steps: Optional[int] = None, config: Op
                                   np.abs(orc.buf[i]) + sum_abs_g[i])
             for i in sample:
                 m_, n_ = shapes[i]
-                lr_mult = _f32(cfg.muon_lr_scale * cfg.moonlight_coef * math.sqrt(max(m_, n_)))
+                ls, ws = orc.options[i]
+                decay = _f32(1.0 - lr * ls * cfg.muon_weight_decay * ws)
+                lr_mult = _f32(ls * cfg.muon_lr_scale * cfg.moonlight_coef * math.sqrt(max(m_, n_)))
                 after = gpu.param(i).astype(np.float64)
                 O_gpu = (before[i].astype(np.float64) * decay - after) / (_f32(lr) * lr_mult)
                 err = relative_frobenius(O_gpu, res["O"][i])
@@ -178,7 +183,7 @@ def run_parity(w: workloads.Workload, *, steps: Optional[int] = None, config: Op
                     compare_state(f"step {step} m[{names[i]}]", m_gpu, orc.m[i], np.abs(orc.m[i]) + sum_abs_g[i])
                     compare_state(f"step {step} v[{names[i]}]", v_gpu, orc.v[i], np.abs(orc.v[i]) + ghat * ghat)
                     p_gpu = gpu.param(i)
-                    upd = lr * t * 10.0
+                    upd = lr * max(1.0, orc.options[i][0]) * t * 10.0
                     compare_state(f"step {step} p[{names[i]}]", p_gpu, orc_p[i],
                                   np.abs(adam_before[i]) + np.abs(orc_p[i]) + upd)
                     if gpu.S[i] is not None:

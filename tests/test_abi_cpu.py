@@ -160,3 +160,49 @@ def test_binding_fails_loudly_without_library(monkeypatch, mx):
 
 def test_version(mx):
     assert "sm_103a" in mx.muon_adamw_version()
+
+
+def test_config_struct_matches_c_layout(mx):
+    """config_init zero-fills the C struct and then sets fields: with canary
+    bytes around the Python mirror, every byte of the mirror is rewritten
+    (the C struct is not shorter) and none beyond it (not longer)."""
+    import ctypes
+
+    n = ctypes.sizeof(mx.MuonAdamWConfig)
+    buf = (ctypes.c_ubyte * (n + 64))(*([0xAB] * (n + 64)))
+    mx.load_library().muon_adamw_config_init(ctypes.cast(buf, ctypes.POINTER(mx.MuonAdamWConfig)))
+    assert all(b == 0xAB for b in bytes(buf)[n:]), "C config struct is larger than the Python mirror"
+    cfg = mx.MuonAdamWConfig.from_buffer_copy(bytes(buf)[:n])
+    assert bytes(cfg.ns_schedule[mx.MA_NS_SCHEDULE_MAX - 1]) == bytes(24), "C config struct is shorter"
+    assert cfg.ns_steps == 5 and cfg.clip_eps == 1e-6
+    assert cfg.muon_momentum_form == mx.MA_MOMENTUM_SGD
+    assert cfg.adam_decay_exempt_bias_norm == 0 and cfg.ns_schedule_len == 0
+
+
+@pytest.mark.parametrize("field,value", [
+    ("muon_momentum_form", 2),
+    ("adam_decay_exempt_bias_norm", 3),
+    ("ns_schedule_len", 4),          # != ns_steps
+    ("ns_schedule_len", 17),
+    ("reserved1", 1),
+    ("schedule_nan", 0),
+])
+def test_invalid_variant_config_is_rejected(mx, field, value):
+    import ctypes
+
+    c = mx.muon_adamw_config_init()
+    if field == "reserved1":
+        c.reserved[1] = value
+    elif field == "schedule_nan":
+        c.ns_schedule_len = 5
+        c.ns_schedule[2][1] = float("nan")
+    else:
+        setattr(c, field, value)
+    h = ctypes.c_void_p()
+    st = mx.load_library().muon_adamw_create(ctypes.byref(c), None, ctypes.byref(h))
+    assert st == mx.MA_ERR_ARG, mx.muon_adamw_last_error()
+    assert not h.value
+
+
+def test_set_param_options_null_handle(mx):
+    assert mx.load_library().muon_adamw_set_param_options(None, 0, 1.0, 1.0) == mx.MA_ERR_ARG

@@ -349,6 +349,68 @@ def test_profiling_counts_launches(mx):
         gpu.close()
 
 
+# a schedule: the standard triple three times, then two polishing steps with
+# phi(1) = 1 (the last one also has phi'(1) = 0)
+SCHEDULE = [(3.4445, -4.7750, 2.0315)] * 3 + [(3.0, -3.2, 1.2), (1.875, -1.25, 0.375)]
+
+
+@pytest.mark.parametrize("ns_kernel", KERNELS, ids=lambda k: KNAMES[k])
+def test_ema_momentum_and_coefficient_schedule(mx, ns_kernel):
+    w = workloads.get_workload("tiny")
+    w = workloads.custom_workload("tiny", w.tensors, policy="bf16_mixed", steps=3)
+    r = run_parity(w, config={"ns_kernel": ns_kernel, "muon_momentum_form": "ema", "ns_schedule": SCHEDULE},
+                   oracle_overrides={"muon_momentum_form": "ema", "ns_schedule": SCHEDULE})
+    assert r["worst_o"] <= O_TOL
+
+
+def _options_workload():
+    t = [TensorSpec("model.action_expert.layers.0.mlp.up_proj.weight", (512, 256)),
+         TensorSpec("model.action_expert.layers.0.mlp.down_proj.weight", (256, 512)),
+         TensorSpec("model.action_expert.layers.0.self_attn.q_proj.weight", (256, 256)),
+         TensorSpec("model.action_expert.layers.0.self_attn.q_proj.bias", (256,)),
+         TensorSpec("model.action_expert.layers.0.input_layernorm.weight", (256,)),
+         TensorSpec("model.vlm.proj.weight", (96, 200)),
+         TensorSpec("model.vlm.proj.bias", (200,)),
+         TensorSpec("model.vlm.final_norm.weight", (200,))]
+    return workloads.custom_workload("options", t, policy="bf16_mixed", steps=3)
+
+
+def test_param_options_and_decay_exemption(mx):
+    """Per-parameter (lr_scale, weight_decay_scale) on Muon and AdamW
+    parameters, the bias/norm exemption rule, and an explicit option that
+    overrides the rule (the q_proj bias)."""
+    w = _options_workload()
+    opts = {0: (2.0, 0.0), 2: (0.5, 3.0), 3: (1.0, 1.0), 5: (3.0, 0.5)}
+    r = run_parity(w, config={"adam_decay_exempt_bias_norm": 1},
+                   oracle_overrides={"adam_decay_exempt_bias_norm": True}, param_options=opts)
+    assert r["worst_o"] <= O_TOL
+
+
+def test_param_options_errors(mx):
+    w = _options_workload()
+    gpu = GpuSide(w, workloads.master_weights(w))
+    try:
+        opt = gpu.opt
+        for bad in ((99, 1.0, 1.0), (0, -1.0, 1.0), (0, 1.0, float("inf")), (0, float("nan"), 1.0)):
+            with pytest.raises(mx.MuonAdamWError) as ei:
+                opt.set_param_options(*bad)
+            assert ei.value.status == mx.MA_ERR_ARG
+        # seven more distinct pairs fill the table of eight; the next one is refused
+        for i in range(7):
+            opt.set_param_options(i, 2.0 + i, 1.0)
+        with pytest.raises(mx.MuonAdamWError) as ei:
+            opt.set_param_options(7, 9.0, 1.0)
+        assert ei.value.status == mx.MA_ERR_UNSUPPORTED
+        opt.set_param_options(7, 1.0, 1.0)   # the default pair is always available
+        gpu.load_grads(workloads.gradients(w, 1))
+        gpu.step(w.lr)
+        with pytest.raises(mx.MuonAdamWError) as ei:
+            opt.set_param_options(0, 1.0, 1.0)
+        assert ei.value.status == mx.MA_ERR_STATE
+    finally:
+        gpu.close()
+
+
 def test_bounded_wait_runs_out_and_reports(mx):
     """Failure path without a fault: the armed test hook starves one CTA of
     its operand loads, its bounded mbarrier wait runs out (2 s), and the step
