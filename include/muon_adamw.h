@@ -244,6 +244,18 @@ MA_API ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_ou
  * MA_ERR_DEVICE_CHECK if a bounded in-kernel wait ran out. */
 MA_API ma_status muon_adamw_sync(muon_adamw_t* h);
 
+/* Record `cuda_event` (a cudaEvent_t created by the caller) so that it
+ * completes once the latest step no longer reads any gradient: after the
+ * gradient norm, the Muon momentum pass and the AdamW pass (the Newton-Schulz
+ * chain that follows reads none). From then on the caller may overwrite the
+ * gradient buffers, e.g. with the next step's gradients, while the step's
+ * Newton-Schulz products still run. The event is recorded on a library
+ * stream that only waits for those passes, so neither of the step's streams
+ * is held back. The article has no counterpart (its optimizer owns no
+ * gradient buffers). Errors: MA_ERR_ARG (NULL handle or event), MA_ERR_STATE
+ * (no step taken yet), MA_ERR_CUDA. */
+MA_API ma_status muon_adamw_record_grads_consumed(muon_adamw_t* h, void* cuda_event);
+
 /* Test hook for the failure path, not for production use. Arms a one-shot
  * stall: in the next step's first Newton-Schulz launch, one CTA issues no
  * operand loads, so its MMA warp's bounded wait (2 s) runs out. The kernel

@@ -134,6 +134,7 @@ _SIGNATURES = {
     "muon_adamw_step": (ctypes.c_int, [_P, ctypes.c_double, ctypes.POINTER(ctypes.c_float)]),
     "muon_adamw_sync": (ctypes.c_int, [_P]),
     "muon_adamw_test_arm_stall": (ctypes.c_int, [_P]),
+    "muon_adamw_record_grads_consumed": (ctypes.c_int, [_P, _P]),
     "muon_adamw_set_param_options": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_double, ctypes.c_double]),
     "muon_adamw_get_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),
     "muon_adamw_set_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),
@@ -232,6 +233,10 @@ def muon_adamw_sync(h: int) -> None:
 def muon_adamw_set_param_options(h: int, index: int, lr_scale: float, weight_decay_scale: float) -> None:
     _check(load_library().muon_adamw_set_param_options(_P(h), int(index), float(lr_scale),
                                                        float(weight_decay_scale)))
+
+
+def muon_adamw_record_grads_consumed(h: int, cuda_event: int) -> None:
+    _check(load_library().muon_adamw_record_grads_consumed(_P(h), _P(cuda_event)))
 
 
 def muon_adamw_test_arm_stall(h: int) -> None:
@@ -375,6 +380,17 @@ class MuonAdamW:
         except Exception:
             self.close()
             raise
+
+    def record_grads_consumed(self, event=None):
+        """A torch.cuda.Event that completes once the latest step has read
+        every gradient (the gradient buffers may then be overwritten)."""
+        import torch
+
+        ev = event if event is not None else torch.cuda.Event()
+        if not ev.cuda_event:
+            ev.record()  # torch creates the underlying CUDA event on its first record
+        muon_adamw_record_grads_consumed(self.handle, ev.cuda_event)
+        return ev
 
     def set_param_options(self, index: int, lr_scale: float = 1.0, weight_decay_scale: float = 1.0) -> None:
         muon_adamw_set_param_options(self.handle, index, lr_scale, weight_decay_scale)

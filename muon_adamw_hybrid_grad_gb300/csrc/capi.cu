@@ -128,7 +128,10 @@ struct muon_adamw {
   bool stall_test = false;    // one-shot test hook armed by muon_adamw_test_arm_stall
   cudaStream_t s0 = nullptr;  // caller's stream
   cudaStream_t s1 = nullptr;  // AdamW stream (library-owned)
+  cudaStream_t s2 = nullptr;  // joins the gradient readers for muon_adamw_record_grads_consumed
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_g0 = nullptr, ev_g1 = nullptr;  // last gradient reader of the latest step on s0 / s1
+  bool g1_valid = false;                          // the latest step read gradients on s1
   std::vector<Param> params;
   bool planned = false;
   std::vector<std::pair<double, double>> option_groups;  // (lr_scale, wd_scale); [0] = (1, 1)
@@ -691,8 +694,11 @@ ma_status muon_adamw_create(const muon_adamw_config* cfg, void* cuda_stream, muo
   h->num_sms = prop.multiProcessorCount;
   h->s0 = static_cast<cudaStream_t>(cuda_stream);
   cudaError_t e = cudaStreamCreateWithFlags(&h->s1, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->s2, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_g0, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_g1, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     muon_adamw_destroy(h);
     return fail(MA_ERR_CUDA, "stream/event creation failed: %s", cudaGetErrorString(e));
@@ -797,7 +803,10 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
     a.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
     timed(h, MA_K_ADAMW, h->s1, h->bytes_adam,
           [&] { launch_adamw(h->d_adam_chunks, h->n_adam_chunks, h->d_scalars, a, h->adam_grid, h->s1); });
+    CUDA_TRY(cudaEventRecord(h->ev_g1, h->s1));
   }
+  h->g1_valid = have_adam;
+  if (h->n_mats == 0) CUDA_TRY(cudaEventRecord(h->ev_g0, h->s0));  // the norm pass was the last reader on s0
 
   if (h->n_mats > 0) {
     MomArgs ma_{(float)c.muon_momentum, c.muon_nesterov,
@@ -806,6 +815,7 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
       launch_muon_momentum(h->d_tiles, h->n_tiles, h->d_mats, h->d_scalars, ma_, h->d_tile_partials, h->mom_grid,
                            h->s0);
     });
+    CUDA_TRY(cudaEventRecord(h->ev_g0, h->s0));  // the last kernel on s0 that reads gradients
     timed(h, MA_K_NS_PREP, h->s0, (double)h->n_tiles * 4,
           [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, (float)c.ns_eps, h->d_rscale, h->s0); });
     NsEpiArgs epi;
@@ -845,6 +855,16 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
     ma_status st = check_device_flag(h);
     if (st != MA_OK) return st;
   }
+  return ok();
+}
+
+ma_status muon_adamw_record_grads_consumed(muon_adamw_t* h, void* cuda_event) {
+  if (!h || !cuda_event) return fail(MA_ERR_ARG, "NULL handle or event");
+  if (!h->planned || h->t == 0) return fail(MA_ERR_STATE, "no step taken yet");
+  CUDA_TRY(cudaSetDevice(h->device));
+  CUDA_TRY(cudaStreamWaitEvent(h->s2, h->ev_g0, 0));
+  if (h->g1_valid) CUDA_TRY(cudaStreamWaitEvent(h->s2, h->ev_g1, 0));
+  CUDA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(cuda_event), h->s2));
   return ok();
 }
 
@@ -1031,7 +1051,10 @@ ma_status muon_adamw_destroy(muon_adamw_t* h) {
   if (h->arena) cudaFree(h->arena);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->ev_g0) cudaEventDestroy(h->ev_g0);
+  if (h->ev_g1) cudaEventDestroy(h->ev_g1);
   if (h->s1) cudaStreamDestroy(h->s1);
+  if (h->s2) cudaStreamDestroy(h->s2);
   delete h;
   return ok();
 }

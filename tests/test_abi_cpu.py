@@ -206,3 +206,8 @@ def test_invalid_variant_config_is_rejected(mx, field, value):
 
 def test_set_param_options_null_handle(mx):
     assert mx.load_library().muon_adamw_set_param_options(None, 0, 1.0, 1.0) == mx.MA_ERR_ARG
+
+
+def test_record_grads_consumed_argument_errors(mx):
+    lib = mx.load_library()
+    assert lib.muon_adamw_record_grads_consumed(None, None) == mx.MA_ERR_ARG

@@ -411,6 +411,43 @@ def test_param_options_errors(mx):
         gpu.close()
 
 
+def test_grads_consumed_event_allows_overwriting_gradients(mx):
+    """Gradient buffers overwritten on another stream as soon as the event of
+    muon_adamw_record_grads_consumed completes leave that step's result bit
+    for bit unchanged; the event is refused before the first step."""
+    import torch
+
+    w = _options_workload()
+    masters = workloads.master_weights(w)
+    g1 = workloads.gradients(w, 1)
+    ref = GpuSide(w, masters)
+    try:
+        ref.load_grads(g1)
+        ref.step(w.lr)
+        want = [ref.param(i) for i in range(len(w.tensors))]
+    finally:
+        ref.close()
+    gpu = GpuSide(w, masters)
+    try:
+        with pytest.raises(mx.MuonAdamWError) as ei:
+            gpu.opt.record_grads_consumed()
+        assert ei.value.status == mx.MA_ERR_STATE
+        gpu.load_grads(g1)
+        side = torch.cuda.Stream()
+        gpu.opt.step(w.lr)
+        ev = gpu.opt.record_grads_consumed()
+        side.wait_event(ev)
+        with torch.cuda.stream(side):
+            for g in gpu.G:
+                if g is not None:
+                    g.fill_(1e6)
+        torch.cuda.synchronize()
+        for i in range(len(w.tensors)):
+            assert np.array_equal(gpu.param(i), want[i]), w.tensors[i].name
+    finally:
+        gpu.close()
+
+
 def test_bounded_wait_runs_out_and_reports(mx):
     """Failure path without a fault: the armed test hook starves one CTA of
     its operand loads, its bounded mbarrier wait runs out (2 s), and the step
