@@ -296,15 +296,18 @@ class HybridOracle:
                 self.v[i] = np.zeros(shp, dtype=np.float64)
 
     def step(self, params: List[np.ndarray], grads: List[Optional[np.ndarray]], lr: float,
-             muon_indices: Optional[Sequence[int]] = None) -> dict:
+             muon_indices: Optional[Sequence[int]] = None, total_override: Optional[float] = None) -> dict:
         """One optimizer step. ``muon_indices`` limits the (expensive) Muon
         orthogonalisation to a subset; the other Muon matrices still get their
-        momentum update but no parameter update (used for sampled checks)."""
+        momentum update but no parameter update (used for sampled checks).
+        ``total_override``: the global gradient norm when this oracle holds
+        only a sample of a model's parameters (computed by ``global_grad_norm``
+        over every gradient of the model); the clip coefficient follows from it."""
         cfg = self.cfg
         self.t += 1
         t = self.t
         active = [i for i, g in enumerate(self.groups) if g != GROUP_FROZEN]
-        total = global_grad_norm([grads[i] for i in active])
+        total = global_grad_norm([grads[i] for i in active]) if total_override is None else float(total_override)
         coef = clip_coefficient(total, float(cfg["max_grad_norm"]), float(cfg["clip_eps"]))
         a_b_c = cfg["ns_schedule"] if cfg["ns_schedule"] is not None else tuple(cfg["ns_coefficients"])
         beta1, beta2 = cfg["adam_betas"]

@@ -198,3 +198,123 @@ def run_parity(w: workloads.Workload, *, steps: Optional[int] = None, config: Op
         return {"worst_o": worst_o, "steps": steps, "groups": groups}
     finally:
         gpu.close()
+
+
+def _batches(idx: Sequence[int], size: int = 16):
+    idx = list(idx)
+    for k in range(0, len(idx), size):
+        yield idx[k:k + size]
+
+
+def run_parity_sampled(w: workloads.Workload, sample: Sequence[int], *, steps: int = 1,
+                       o_sample: Optional[Sequence[int]] = None, lr: Optional[float] = None,
+                       config: Optional[dict] = None) -> Dict[str, object]:
+    """A whole workload on the GPU, the oracle on a sample of its tensors.
+
+    Every master and gradient comes from the seeded generators (in batches,
+    uploaded as they are made, so that full-size workloads fit in host
+    memory). The expected global norm is ``oracle.global_grad_norm`` over
+    every gradient of the model; an oracle over the sampled tensors steps
+    with that norm (``total_override``). Compared each step: the norm, and
+    for every sampled tensor its optimizer state and parameters at the
+    tolerances of ``run_parity``; O of the Muon matrices in ``o_sample``
+    (default: every sampled Muon matrix); frozen tensors stay unwritten.
+    """
+    import torch
+
+    import muon_adamw_hybrid_grad_gb300 as mx
+
+    lr = w.lr if lr is None else lr
+    dev = torch.device("cuda")
+    gdt = torch.bfloat16 if w.grad_dtype == "bf16" else torch.float32
+    n = len(w.tensors)
+    sample = sorted(set(sample))
+    P: List = [None] * n
+    G: List = [None] * n
+    S: List = [None] * n
+    m0: Dict[int, np.ndarray] = {}
+    for batch in _batches(range(n)):
+        for i, m in zip(batch, workloads.master_weights(w, batch)):
+            t = w.tensors[i]
+            P[i] = torch.from_numpy(m).to(dev)
+            if not t.frozen:
+                G[i] = torch.zeros(t.shape, dtype=gdt, device=dev)
+                if w.policy == "bf16_mixed":
+                    S[i] = torch.zeros(t.shape, dtype=torch.bfloat16, device=dev)
+            if i in sample or t.frozen:
+                m0[i] = m
+    entries = [(t.name, P[i], G[i], S[i], mx.MA_GROUP_FROZEN if t.frozen else None)
+               for i, t in enumerate(w.tensors)]
+    cfg_kw = dict(config or {})
+    cfg_kw.setdefault("precision", mx.MA_BF16_MIXED if w.policy == "bf16_mixed" else mx.MA_FP32_MIXED)
+    opt = mx.MuonAdamW(entries, **cfg_kw)
+    try:
+        cfg = opt.cfg
+        names = [w.tensors[i].name for i in sample]
+        shapes = [w.tensors[i].shape for i in sample]
+        frozen = [w.tensors[i].frozen for i in sample]
+        orc = oracle.HybridOracle(names, shapes, frozen)
+        for k, i in enumerate(sample):
+            assert orc.groups[k] == opt.groups[i], f"routing of {names[k]} differs"
+        local = {i: k for k, i in enumerate(sample)}
+        o_idx = [i for i in (sample if o_sample is None else o_sample) if opt.groups[i] == "muon"]
+        orc_p = [m0[i].astype(np.float64) for i in sample]
+        sum_abs_g: Dict[int, np.ndarray] = {}
+        worst_o = 0.0
+        for step in range(1, steps + 1):
+            sq = 0.0
+            gs: Dict[int, np.ndarray] = {}
+            for batch in _batches(range(n)):
+                for i, g in zip(batch, workloads.gradients(w, step, batch)):
+                    if g is None:
+                        continue
+                    G[i].copy_(torch.from_numpy(g).to(dev).to(gdt))
+                    sq += float(np.sum(np.square(g, dtype=np.float64)))
+                    if i in local:
+                        gs[i] = g
+            total = math.sqrt(sq)
+            before = {i: P[i].cpu().numpy() for i in o_idx}
+            adam_before = {i: orc_p[local[i]].copy() for i in sample if opt.groups[i] == "adamw"}
+            total_gpu = opt.step(lr, want_norm=True)
+            grads_local = [gs.get(i) for i in sample]
+            res = orc.step(orc_p, grads_local, lr, muon_indices=[local[i] for i in o_idx], total_override=total)
+            assert math.isclose(total_gpu, total, rel_tol=NORM_TOL), f"step {step}: norm {total_gpu} vs {total}"
+            coef = res["coef"]
+            for i in sample:
+                k = local[i]
+                grp = opt.groups[i]
+                if grp == "frozen":
+                    continue
+                ghat = np.abs(coef * gs[i].astype(np.float64))
+                sum_abs_g[i] = sum_abs_g.get(i, 0.0) + ghat
+                if grp == "muon":
+                    compare_state(f"step {step} buf[{names[k]}]", opt.state(i, 0).numpy(), orc.buf[k],
+                                  np.abs(orc.buf[k]) + sum_abs_g[i])
+                else:
+                    compare_state(f"step {step} m[{names[k]}]", opt.state(i, 0).numpy(), orc.m[k],
+                                  np.abs(orc.m[k]) + sum_abs_g[i])
+                    compare_state(f"step {step} v[{names[k]}]", opt.state(i, 1).numpy(), orc.v[k],
+                                  np.abs(orc.v[k]) + ghat * ghat)
+                    p_gpu = P[i].cpu().numpy()
+                    compare_state(f"step {step} p[{names[k]}]", p_gpu, orc_p[k],
+                                  np.abs(adam_before[i]) + np.abs(orc_p[k]) + lr * res["t"] * 10.0)
+                    if S[i] is not None:
+                        assert np.array_equal(S[i].float().cpu().numpy(), workloads.bf16_round(p_gpu))
+            for i in o_idx:
+                k = local[i]
+                m_, n_ = w.tensors[i].shape
+                decay = _f32(1.0 - lr * cfg.muon_weight_decay)
+                lr_mult = _f32(cfg.muon_lr_scale * cfg.moonlight_coef * math.sqrt(max(m_, n_)))
+                after = P[i].cpu().numpy().astype(np.float64)
+                O_gpu = (before[i].astype(np.float64) * decay - after) / (_f32(lr) * lr_mult)
+                err = relative_frobenius(O_gpu, res["O"][k])
+                worst_o = max(worst_o, err)
+                assert err <= O_TOL, f"step {step} {names[k]} {(m_, n_)}: O rel. Frobenius error {err:.3e}"
+                if S[i] is not None:
+                    assert np.array_equal(S[i].float().cpu().numpy(), workloads.bf16_round(after.astype(np.float32)))
+            for i, t in enumerate(w.tensors):
+                if t.frozen:
+                    assert torch.equal(P[i], torch.from_numpy(m0[i]).to(dev)), f"frozen {t.name} was modified"
+        return {"worst_o": worst_o, "steps": steps, "o_checked": len(o_idx)}
+    finally:
+        opt.close()

@@ -212,3 +212,25 @@ def test_planted_option_mistakes_are_caught():
     assert not math.isclose(right, wrong, rel_tol=1e-9)
     # exempting by substring "bias" would exempt 'biased_gate'
     assert "bias" in "model.vlm.biased_gate.weight" and not oracle.decay_exempt("model.vlm.biased_gate.weight")
+
+
+def test_total_override_sets_the_clip_coefficient():
+    # a sampled oracle takes the model's global norm from outside: with its own
+    # norm nothing changes; with a larger one the momentum is the gradient times
+    # max_norm / (total + 1e-6) (first step: buf = coef * g)
+    names = ["model.action_expert.layers.0.mlp.w.weight", "model.vlm.ln.weight"]
+    shapes = [(6, 8), (5,)]
+    rng = np.random.default_rng(31)
+    g = [rng.standard_normal((6, 8)), rng.standard_normal(5)]
+    own = math.sqrt(sum(float(np.sum(x * x)) for x in g))
+    a = oracle.HybridOracle(names, shapes)
+    b = oracle.HybridOracle(names, shapes)
+    pa = [np.zeros((6, 8)), np.ones(5)]
+    pb = [x.copy() for x in pa]
+    ra = a.step(pa, g, LR)
+    rb = b.step(pb, g, LR, total_override=own)
+    assert ra["coef"] == rb["coef"] and all(np.array_equal(x, y) for x, y in zip(pa, pb))
+    c = oracle.HybridOracle(names, shapes)
+    rc = c.step([np.zeros((6, 8)), np.ones(5)], g, LR, total_override=1000.0)
+    assert rc["total"] == 1000.0 and rc["coef"] == pytest.approx(1.0 / (1000.0 + 1e-6), rel=1e-15)
+    assert np.allclose(c.buf[0], g[0] / (1000.0 + 1e-6), rtol=1e-15)

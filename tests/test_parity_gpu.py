@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import workloads
-from harness import O_TOL, GpuSide, relative_frobenius, run_parity
+from harness import O_TOL, GpuSide, relative_frobenius, run_parity, run_parity_sampled
 from workloads import TensorSpec
 
 pytestmark = pytest.mark.gpu
@@ -85,6 +85,51 @@ def test_h1024_full_size_sampled(mx):
     w = workloads.get_workload("h1024")
     per_layer = 7
     sample = [layer * per_layer + k for layer in (0, 8, 15) for k in (0, 4, 6)]
+    r = run_parity(w, steps=2, muon_sample=sample)
+    assert r["worst_o"] <= O_TOL
+
+
+def _layer_sample(w, layers, per_layer=7, extra=()):
+    """Indices of the matrices of the given expert layers plus ``extra``."""
+    return [layer * per_layer + k for layer in layers for k in range(per_layer)] + list(extra)
+
+
+def test_h2048_full_size_sampled(mx):
+    """The 2048-hidden expert at full size (24 layers, 1.61 G Muon elements,
+    fp32 masters): the norm over every gradient; momentum, parameters and O of
+    every matrix of layers 0 and 23 (2048x2048, 8192x2048, 2048x8192); AdamW
+    state of layer 0's norms and biases."""
+    w = workloads.get_workload("h2048")
+    vec0 = 24 * 7  # first vector tensor (layer 0's input_layernorm)
+    sample = _layer_sample(w, (0, 23), extra=range(vec0, vec0 + 5))
+    o_sample = [0, 4, 6, 23 * 7, 23 * 7 + 4, 23 * 7 + 6]
+    r = run_parity_sampled(w, sample, steps=2, o_sample=o_sample)
+    assert r["o_checked"] == 6 and r["worst_o"] <= O_TOL
+
+
+def test_full_vla_full_size_sampled(mx):
+    """The full VLA workload at full size (1.61 G Muon + 1.69 G AdamW elements,
+    a frozen 151936x2048 embedding), lr from the cosine schedule at step 1000:
+    the norm over every gradient; one expert layer (O of its 2048x2048 and
+    8192x2048 matrices), one language-model layer (AdamW, every shape) and one
+    vision block sampled; the frozen embedding unwritten."""
+    w = workloads.get_workload("full_vla")
+    names = [t.name for t in w.tensors]
+    emb = names.index("model.vlm.embed_tokens.weight")
+    lm0 = names.index("model.vlm.language_model.layers.0.self_attn.q_proj.weight")
+    vis = names.index("model.vlm.vision_tower.blocks.0.proj.weight")
+    sample = _layer_sample(w, (11,)) + list(range(lm0, lm0 + 9)) + [vis]
+    lr = w.lr * mx.muon_adamw_cosine_with_min_lr(1000, 2000, 0, 0.1)
+    r = run_parity_sampled(w, sample, steps=1, o_sample=[11 * 7, 11 * 7 + 4], lr=lr)
+    assert r["o_checked"] == 2 and r["worst_o"] <= O_TOL
+    assert w.tensors[emb].frozen
+
+
+def test_many_small_full_size(mx):
+    """The many-small workload at full size (768 matrices of 128x512 and
+    512x128, 4096 AdamW vectors): every state element and O of 64 matrices."""
+    w = workloads.get_workload("many_small")
+    sample = list(range(0, 512, 16)) + list(range(512, 768, 8))
     r = run_parity(w, steps=2, muon_sample=sample)
     assert r["worst_o"] <= O_TOL
 
