@@ -244,6 +244,18 @@ MA_API ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_ou
  * MA_ERR_DEVICE_CHECK if a bounded in-kernel wait ran out. */
 MA_API ma_status muon_adamw_sync(muon_adamw_t* h);
 
+/* Run each step's Newton-Schulz chain (the Frobenius scales and the 3 x
+ * ns_steps products, most of a step's launches) as a captured CUDA graph
+ * (enable = 1, the default) or as direct launches (0). The graph is captured
+ * at the first step that can use it and replayed from then on: the plan never
+ * changes after the first step and the lr- and step-dependent scalars are read
+ * from HBM (one small host-to-device copy per step). The gradient passes (norm,
+ * clip, momentum, AdamW) stay direct launches, so the events of
+ * muon_adamw_record_grads_consumed keep their meaning. Direct launches are
+ * used while profiling is on, with MA_NS_SIMT, and if a capture ever fails.
+ * Results are bitwise the same either way. Errors: MA_ERR_ARG (NULL handle). */
+MA_API ma_status muon_adamw_set_graph_mode(muon_adamw_t* h, int enable);
+
 /* Record `cuda_event` (a cudaEvent_t created by the caller) so that it
  * completes once the latest step no longer reads any gradient: after the
  * gradient norm, the Muon momentum pass and the AdamW pass (the Newton-Schulz

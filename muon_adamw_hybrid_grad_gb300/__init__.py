@@ -135,6 +135,7 @@ _SIGNATURES = {
     "muon_adamw_sync": (ctypes.c_int, [_P]),
     "muon_adamw_test_arm_stall": (ctypes.c_int, [_P]),
     "muon_adamw_record_grads_consumed": (ctypes.c_int, [_P, _P]),
+    "muon_adamw_set_graph_mode": (ctypes.c_int, [_P, ctypes.c_int]),
     "muon_adamw_set_param_options": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_double, ctypes.c_double]),
     "muon_adamw_get_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),
     "muon_adamw_set_state": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P]),
@@ -233,6 +234,10 @@ def muon_adamw_sync(h: int) -> None:
 def muon_adamw_set_param_options(h: int, index: int, lr_scale: float, weight_decay_scale: float) -> None:
     _check(load_library().muon_adamw_set_param_options(_P(h), int(index), float(lr_scale),
                                                        float(weight_decay_scale)))
+
+
+def muon_adamw_set_graph_mode(h: int, enable: bool) -> None:
+    _check(load_library().muon_adamw_set_graph_mode(_P(h), 1 if enable else 0))
 
 
 def muon_adamw_record_grads_consumed(h: int, cuda_event: int) -> None:

@@ -132,6 +132,12 @@ struct muon_adamw {
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   cudaEvent_t ev_g0 = nullptr, ev_g1 = nullptr;  // last gradient reader of the latest step on s0 / s1
   bool g1_valid = false;                          // the latest step read gradients on s1
+  StepParams* d_step = nullptr;                   // this step's scalars (arena)
+  StepParams* h_step = nullptr;                   // two pinned host slots, alternating per step
+  cudaEvent_t ev_slot[2] = {nullptr, nullptr};    // a slot's copy has been read
+  bool graph_mode = true;                         // run steps as captured CUDA graphs
+  bool graph_broken = false;                      // capture failed: direct launches from now on
+  cudaGraphExec_t gexec = nullptr;                // the captured Newton-Schulz chain
   std::vector<Param> params;
   bool planned = false;
   std::vector<std::pair<double, double>> option_groups;  // (lr_scale, wd_scale); [0] = (1, 1)
@@ -332,6 +338,8 @@ ma_status build_plan(muon_adamw* h) {
   off += al(n_mats * sizeof(float));
   const size_t off_scalars = off;
   off += al(sizeof(StepScalars));
+  const size_t off_step = off;
+  off += al(sizeof(StepParams));
   const size_t off_err = off;
   off += al(sizeof(int));
   h->arena_bytes = off;
@@ -363,6 +371,7 @@ ma_status build_plan(muon_adamw* h) {
   h->d_tile_partials = reinterpret_cast<float*>(base + off_tile_part);
   h->d_rscale = reinterpret_cast<float*>(base + off_rscale);
   h->d_scalars = reinterpret_cast<StepScalars*>(base + off_scalars);
+  h->d_step = reinterpret_cast<StepParams*>(base + off_step);
   h->d_err = reinterpret_cast<int*>(base + off_err);
 
   // --- host tables with device pointers ---
@@ -587,22 +596,14 @@ ma_status build_plan(muon_adamw* h) {
   return MA_OK;
 }
 
-// Epilogue scalars of Newton-Schulz iteration `it`: its coefficients (the
-// schedule's, if one is set) and, per option group, the decoupled decay
-// 1 - lr * lr_scale * muon_wd * wd_scale (formed in double, rounded once).
-void set_epi(NsEpiArgs& e, const muon_adamw_config& c, const std::vector<std::pair<double, double>>& groups,
-             double lr, int it) {
+// Coefficients of Newton-Schulz iteration `it` (the schedule's, if one is set).
+void set_epi_coefficients(NsEpiArgs& e, const muon_adamw_config& c, int it) {
   const bool sched = c.ns_schedule_len > 0;
   e.a = (float)(sched ? c.ns_schedule[it][0] : c.ns_a);
   e.b = (float)(sched ? c.ns_schedule[it][1] : c.ns_b);
   e.c = (float)(sched ? c.ns_schedule[it][2] : c.ns_c);
-  e.lr = (float)lr;
-  for (int g = 0; g < kMaxOptionGroups; ++g) {
-    const double ls = g < (int)groups.size() ? groups[g].first : 1.0;
-    const double ws = g < (int)groups.size() ? groups[g].second : 1.0;
-    e.decay[g] = (float)(1.0 - lr * ls * c.muon_weight_decay * ws);
-  }
 }
+
 
 
 ma_status valid_config(const muon_adamw_config* c) {
@@ -634,6 +635,123 @@ ma_status valid_config(const muon_adamw_config* c) {
 }
 
 }  // namespace
+
+// The scalars of one step (lr and step count dependent), formed in double and
+// rounded once, as the kernels use them.
+static void fill_step_params(muon_adamw* h, double lr, StepParams* sp) {
+  const muon_adamw_config& c = h->cfg;
+  const double t = (double)h->t;
+  const double bc1 = 1.0 - pow(c.adam_beta1, t), bc2 = 1.0 - pow(c.adam_beta2, t);
+  memset(sp, 0, sizeof *sp);
+  for (int g = 0; g < kMaxOptionGroups; ++g) {
+    const double ls = g < (int)h->option_groups.size() ? h->option_groups[g].first : 1.0;
+    const double ws = g < (int)h->option_groups.size() ? h->option_groups[g].second : 1.0;
+    sp->adam_decay[g] = (float)(1.0 - lr * ls * c.adam_weight_decay * ws);
+    sp->adam_step[g] = (float)(lr * ls / bc1);
+    sp->ns_decay[g] = (float)(1.0 - lr * ls * c.muon_weight_decay * ws);
+  }
+  sp->adam_inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
+  sp->ns_lr = (float)lr;
+}
+
+// The launches of one step that read gradients, in order: the norm pass and
+// clip on s0; AdamW forked onto s1; the momentum pass on s0. Each stream then
+// records its grads-consumed event. The per-step scalars are read from
+// h->d_step.
+static ma_status enqueue_gradient_passes(muon_adamw* h) {
+  const muon_adamw_config& c = h->cfg;
+  if (h->n_norm_chunks > 0) {
+    timed(h, MA_K_GRAD_NORM, h->s0, h->bytes_norm,
+          [&] { launch_grad_sumsq(h->d_norm_chunks, h->n_norm_chunks, h->d_norm_partials, h->norm_grid, h->s0); });
+  } else {
+    CUDA_TRY(cudaMemsetAsync(h->d_norm_partials, 0, sizeof(float), h->s0));
+  }
+  timed(h, MA_K_CLIP, h->s0, (double)h->norm_grid * 4, [&] {
+    launch_clip_finalize(h->d_norm_partials, h->n_norm_chunks > 0 ? h->norm_grid : 1, (float)c.max_grad_norm,
+                         (float)c.clip_eps, h->d_scalars, h->s0);
+  });
+  const bool have_adam = h->n_adam_chunks > 0;
+  if (have_adam) {
+    CUDA_TRY(cudaEventRecord(h->ev_fork, h->s0));
+    CUDA_TRY(cudaStreamWaitEvent(h->s1, h->ev_fork, 0));
+    AdamArgs a;
+    a.beta1 = (float)c.adam_beta1;
+    a.beta2 = (float)c.adam_beta2;
+    a.omb1 = (float)(1.0 - c.adam_beta1);
+    a.omb2 = (float)(1.0 - c.adam_beta2);
+    a.eps = (float)c.adam_eps;
+    a.sp = h->d_step;
+    timed(h, MA_K_ADAMW, h->s1, h->bytes_adam,
+          [&] { launch_adamw(h->d_adam_chunks, h->n_adam_chunks, h->d_scalars, a, h->adam_grid, h->s1); });
+    CUDA_TRY(cudaEventRecord(h->ev_g1, h->s1));
+  }
+  h->g1_valid = have_adam;
+  if (h->n_mats > 0) {
+    MomArgs ma_{(float)c.muon_momentum, c.muon_nesterov,
+                c.muon_momentum_form == MA_MOMENTUM_EMA ? (float)(1.0 - c.muon_momentum) : 1.0f};
+    timed(h, MA_K_MOMENTUM, h->s0, h->bytes_mom, [&] {
+      launch_muon_momentum(h->d_tiles, h->n_tiles, h->d_mats, h->d_scalars, ma_, h->d_tile_partials, h->mom_grid,
+                           h->s0);
+    });
+  }
+  CUDA_TRY(cudaEventRecord(h->ev_g0, h->s0));  // the last kernel on s0 that reads gradients is done
+  return MA_OK;
+}
+
+// The Newton-Schulz part of a step on s0: the Frobenius scales, then every
+// product of every iteration. It reads no gradient and nothing that changes
+// from step to step except h->d_step, so it can be captured once.
+static ma_status enqueue_newton_schulz(muon_adamw* h) {
+  const muon_adamw_config& c = h->cfg;
+  if (h->n_mats == 0) return MA_OK;
+  timed(h, MA_K_NS_PREP, h->s0, (double)h->n_tiles * 4,
+        [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, (float)c.ns_eps, h->d_rscale, h->s0); });
+  NsEpiArgs epi;
+  epi.sp = h->d_step;
+  const double units[3] = {h->unit_gram, h->unit_poly, h->unit_update};
+  for (int it = 0; it < c.ns_steps; ++it) {
+    set_epi_coefficients(epi, c, it);
+    for (int kind = 0; kind < 3; ++kind) {
+      if (c.ns_kernel == MA_NS_TCGEN05) {
+        for (TcLaunch& L : h->tc[kind][it]) {
+          L.epi = epi;
+          L.stall_test = h->stall_test ? 1 : 0;
+          h->stall_test = false;  // one launch only
+          const int grid_units = L.cl == 2 ? h->max_pairs : h->num_sms;
+          const int pk = (kind == NS_UPDATE && it == c.ns_steps - 1) ? MA_K_NS_APPLY : MA_K_NS_GRAM + kind;
+          timed(h, pk, h->s0, units[kind] / h->tc[kind][it].size(), [&] { launch_ns_tc(L, grid_units, h->s0); });
+        }
+      } else {
+        const int pk = (kind == NS_UPDATE && it == c.ns_steps - 1) ? MA_K_NS_APPLY : MA_K_NS_GRAM + kind;
+        timed(h, pk, h->s0, units[kind], [&] {
+          for (const NsProblem& p : h->simt[kind][it]) launch_ns_simt(p, epi, h->s0);
+        });
+      }
+    }
+  }
+  return MA_OK;
+}
+
+// Capture the Newton-Schulz part as a CUDA graph (the plan's pointers and
+// launch shapes never change after the first step, and the step's scalars are
+// read from HBM). Any failure leaves the handle on direct launches.
+static void capture_newton_schulz_graph(muon_adamw* h) {
+  cudaGraph_t g = nullptr;
+  if (cudaStreamBeginCapture(h->s0, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    h->graph_broken = true;
+    return;
+  }
+  const bool good = enqueue_newton_schulz(h) == MA_OK;
+  const cudaError_t e = cudaStreamEndCapture(h->s0, &g);
+  if (!good || e != cudaSuccess || !g || cudaGraphInstantiate(&h->gexec, g, 0) != cudaSuccess) {
+    h->gexec = nullptr;
+    h->graph_broken = true;
+  }
+  if (g) cudaGraphDestroy(g);
+  cudaGetLastError();  // a failed capture leaves no sticky error behind
+  clear_last_error();
+}
 
 extern "C" {
 
@@ -699,6 +817,9 @@ ma_status muon_adamw_create(const muon_adamw_config* cfg, void* cuda_stream, muo
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_g0, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_g1, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_slot[0], cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_slot[1], cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaHostAlloc(&h->h_step, 2 * sizeof(StepParams), cudaHostAllocDefault);
   if (e != cudaSuccess) {
     muon_adamw_destroy(h);
     return fail(MA_ERR_CUDA, "stream/event creation failed: %s", cudaGetErrorString(e));
@@ -770,78 +891,26 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
   }
   const muon_adamw_config& c = h->cfg;
   h->t += 1;
-  const double t = (double)h->t;
-
-  if (h->n_norm_chunks > 0) {
-    timed(h, MA_K_GRAD_NORM, h->s0, h->bytes_norm,
-          [&] { launch_grad_sumsq(h->d_norm_chunks, h->n_norm_chunks, h->d_norm_partials, h->norm_grid, h->s0); });
+  // the step's scalars go through one of two pinned slots; the slot's
+  // previous copy (two steps ago) has been read before it is rewritten
+  const int slot = (int)(h->t & 1);
+  CUDA_TRY(cudaEventSynchronize(h->ev_slot[slot]));
+  fill_step_params(h, lr, &h->h_step[slot]);
+  CUDA_TRY(cudaMemcpyAsync(h->d_step, &h->h_step[slot], sizeof(StepParams), cudaMemcpyHostToDevice, h->s0));
+  CUDA_TRY(cudaEventRecord(h->ev_slot[slot], h->s0));
+  ma_status st = enqueue_gradient_passes(h);
+  if (st != MA_OK) return st;
+  // the Newton-Schulz chain: one graph launch, or its launches one by one
+  const bool graph = h->graph_mode && !h->graph_broken && !h->profiling && !h->stall_test &&
+                     c.ns_kernel == MA_NS_TCGEN05 && h->n_mats > 0;
+  if (graph && !h->gexec) capture_newton_schulz_graph(h);
+  if (graph && h->gexec) {
+    CUDA_TRY(cudaGraphLaunch(h->gexec, h->s0));
   } else {
-    CUDA_TRY(cudaMemsetAsync(h->d_norm_partials, 0, sizeof(float), h->s0));
+    st = enqueue_newton_schulz(h);
+    if (st != MA_OK) return st;
   }
-  timed(h, MA_K_CLIP, h->s0, (double)h->norm_grid * 4, [&] {
-    launch_clip_finalize(h->d_norm_partials, h->n_norm_chunks > 0 ? h->norm_grid : 1, (float)c.max_grad_norm,
-                         (float)c.clip_eps, h->d_scalars, h->s0);
-  });
-
-  const bool have_adam = h->n_adam_chunks > 0;
-  if (have_adam) {
-    CUDA_TRY(cudaEventRecord(h->ev_fork, h->s0));
-    CUDA_TRY(cudaStreamWaitEvent(h->s1, h->ev_fork, 0));
-    AdamArgs a;
-    a.beta1 = (float)c.adam_beta1;
-    a.beta2 = (float)c.adam_beta2;
-    a.omb1 = (float)(1.0 - c.adam_beta1);
-    a.omb2 = (float)(1.0 - c.adam_beta2);
-    a.eps = (float)c.adam_eps;
-    const double bc1 = 1.0 - pow(c.adam_beta1, t), bc2 = 1.0 - pow(c.adam_beta2, t);
-    for (int g = 0; g < kMaxOptionGroups; ++g) {
-      const double ls = g < (int)h->option_groups.size() ? h->option_groups[g].first : 1.0;
-      const double ws = g < (int)h->option_groups.size() ? h->option_groups[g].second : 1.0;
-      a.decay[g] = (float)(1.0 - lr * ls * c.adam_weight_decay * ws);
-      a.step_size[g] = (float)(lr * ls / bc1);
-    }
-    a.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
-    timed(h, MA_K_ADAMW, h->s1, h->bytes_adam,
-          [&] { launch_adamw(h->d_adam_chunks, h->n_adam_chunks, h->d_scalars, a, h->adam_grid, h->s1); });
-    CUDA_TRY(cudaEventRecord(h->ev_g1, h->s1));
-  }
-  h->g1_valid = have_adam;
-  if (h->n_mats == 0) CUDA_TRY(cudaEventRecord(h->ev_g0, h->s0));  // the norm pass was the last reader on s0
-
-  if (h->n_mats > 0) {
-    MomArgs ma_{(float)c.muon_momentum, c.muon_nesterov,
-                c.muon_momentum_form == MA_MOMENTUM_EMA ? (float)(1.0 - c.muon_momentum) : 1.0f};
-    timed(h, MA_K_MOMENTUM, h->s0, h->bytes_mom, [&] {
-      launch_muon_momentum(h->d_tiles, h->n_tiles, h->d_mats, h->d_scalars, ma_, h->d_tile_partials, h->mom_grid,
-                           h->s0);
-    });
-    CUDA_TRY(cudaEventRecord(h->ev_g0, h->s0));  // the last kernel on s0 that reads gradients
-    timed(h, MA_K_NS_PREP, h->s0, (double)h->n_tiles * 4,
-          [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, (float)c.ns_eps, h->d_rscale, h->s0); });
-    NsEpiArgs epi;
-    const double units[3] = {h->unit_gram, h->unit_poly, h->unit_update};
-    for (int it = 0; it < c.ns_steps; ++it) {
-      set_epi(epi, c, h->option_groups, lr, it);
-      for (int kind = 0; kind < 3; ++kind) {
-        if (c.ns_kernel == MA_NS_TCGEN05) {
-          for (TcLaunch& L : h->tc[kind][it]) {
-            L.epi = epi;
-            L.stall_test = h->stall_test ? 1 : 0;
-            h->stall_test = false;  // one launch only
-            const int grid_units = L.cl == 2 ? h->max_pairs : h->num_sms;
-            const int pk = (kind == NS_UPDATE && it == c.ns_steps - 1) ? MA_K_NS_APPLY : MA_K_NS_GRAM + kind;
-            timed(h, pk, h->s0, units[kind] / h->tc[kind][it].size(), [&] { launch_ns_tc(L, grid_units, h->s0); });
-          }
-        } else {
-          const int pk = (kind == NS_UPDATE && it == c.ns_steps - 1) ? MA_K_NS_APPLY : MA_K_NS_GRAM + kind;
-          timed(h, pk, h->s0, units[kind], [&] {
-            for (const NsProblem& p : h->simt[kind][it]) launch_ns_simt(p, epi, h->s0);
-          });
-        }
-      }
-    }
-  }
-  if (have_adam) {
+  if (h->g1_valid) {
     CUDA_TRY(cudaEventRecord(h->ev_join, h->s1));
     CUDA_TRY(cudaStreamWaitEvent(h->s0, h->ev_join, 0));
   }
@@ -855,6 +924,12 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
     ma_status st = check_device_flag(h);
     if (st != MA_OK) return st;
   }
+  return ok();
+}
+
+ma_status muon_adamw_set_graph_mode(muon_adamw_t* h, int enable) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  h->graph_mode = enable != 0;
   return ok();
 }
 
@@ -1053,6 +1128,10 @@ ma_status muon_adamw_destroy(muon_adamw_t* h) {
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->ev_g0) cudaEventDestroy(h->ev_g0);
   if (h->ev_g1) cudaEventDestroy(h->ev_g1);
+  if (h->gexec) cudaGraphExecDestroy(h->gexec);
+  for (int k = 0; k < 2; ++k)
+    if (h->ev_slot[k]) cudaEventDestroy(h->ev_slot[k]);
+  if (h->h_step) cudaFreeHost(h->h_step);
   if (h->s1) cudaStreamDestroy(h->s1);
   if (h->s2) cudaStreamDestroy(h->s2);
   delete h;

@@ -75,11 +75,22 @@ struct StepScalars {    // written on the device each step
 // being (1, 1); each chunk or matrix names its group.
 constexpr int kMaxOptionGroups = 8;
 
+// Scalars that change every step (they depend on lr and the step count t):
+// one host-to-device copy writes them to HBM at the start of each step and
+// the kernels that need them read them there, so that a captured step graph
+// stays valid from step to step.
+struct StepParams {
+  float adam_decay[kMaxOptionGroups];  // 1 - lr * lr_scale * wd * wd_scale
+  float adam_step[kMaxOptionGroups];   // lr * lr_scale / (1 - beta1^t)
+  float adam_inv_sqrt_bc2;             // 1 / sqrt(1 - beta2^t)
+  float ns_lr;                         // lr
+  float ns_decay[kMaxOptionGroups];    // 1 - lr * lr_scale * muon_wd * wd_scale
+  float pad[2];
+};
+
 struct AdamArgs {
   float beta1, beta2, omb1, omb2, eps;
-  float inv_sqrt_bc2;                // 1 / sqrt(1 - beta2^t)
-  float decay[kMaxOptionGroups];     // 1 - lr * lr_scale * wd * wd_scale
-  float step_size[kMaxOptionGroups]; // lr * lr_scale / (1 - beta1^t)
+  const StepParams* sp;
 };
 
 struct MomArgs {
@@ -91,9 +102,8 @@ struct MomArgs {
 enum NsKind : int32_t { NS_GRAM = 0, NS_POLY = 1, NS_UPDATE = 2 };
 
 struct NsEpiArgs {
-  float a, b, c;                 // this iteration's coefficients
-  float lr;
-  float decay[kMaxOptionGroups]; // 1 - lr * lr_scale * muon_wd * wd_scale
+  float a, b, c;         // this iteration's coefficients
+  const StepParams* sp;  // the last iteration's lr and decays
 };
 
 // One grouped GEMM problem: all same-shape matrices of one bucket. The

@@ -58,7 +58,7 @@ __device__ __forceinline__ void ns_epilogue_element(const NsProblem& pb, const N
   const int pi = M.transposed ? j : i;
   const int pj = M.transposed ? i : j;
   const size_t po = (size_t)pi * M.n + pj;
-  const float p = fmaf(M.p[po], ep.decay[M.group], -(ep.lr * M.lr_mult) * v);
+  const float p = fmaf(M.p[po], ep.sp->ns_decay[M.group], -(ep.sp->ns_lr * M.lr_mult) * v);
   M.p[po] = p;
   if (M.shadow) M.shadow[po] = ns_f2bf(p);
 }

@@ -486,8 +486,8 @@ __device__ __forceinline__ void apply_block_direct(const MuonMat& M, const NsEpi
   const int gi = row0 + lane;
   const int cnt = M.l - col0 < 32 ? M.l - col0 : 32;
   if (gi >= M.s || cnt <= 0) return;
-  const float lrm = ep.lr * M.lr_mult;
-  const float dec = ep.decay[M.group];
+  const float lrm = ep.sp->ns_lr * M.lr_mult;
+  const float dec = ep.sp->ns_decay[M.group];
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     if (e < cnt) {
@@ -598,8 +598,8 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
       ph ^= 1u << b;
       pend &= ~(1u << b);
       const float rs = P.p.first ? P.p.rscale[c.mat] : 1.f;
-      const float lrm = ep.lr * M.lr_mult;
-      const float dec = ep.decay[M.group];
+      const float lrm = ep.sp->ns_lr * M.lr_mult;
+      const float dec = ep.sp->ns_decay[M.group];
       float o[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]) * rs;

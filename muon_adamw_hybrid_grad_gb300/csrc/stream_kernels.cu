@@ -336,11 +336,11 @@ __global__ void __launch_bounds__(kPrepThreads) ns_prep_kernel(const MuonMat* __
 constexpr int kAdamThreads = 256;
 
 __device__ __forceinline__ void adam_one(float& p, float& m, float& v, float g, float coef, const AdamArgs& a,
-                                         float decay, float step_size) {
+                                         float decay, float step_size, float inv_sqrt_bc2) {
   const float gh = coef * g;
   m = fmaf(a.beta1, m, a.omb1 * gh);
   v = fmaf(a.beta2, v, a.omb2 * gh * gh);
-  const float denom = fmaf(sqrtf(v), a.inv_sqrt_bc2, a.eps);
+  const float denom = fmaf(sqrtf(v), inv_sqrt_bc2, a.eps);
   p = fmaf(p, decay, -step_size * (m / denom));
 }
 
@@ -350,7 +350,8 @@ __global__ void __launch_bounds__(kAdamThreads) adamw_kernel(const AdamChunk* __
   const float coef = sc->coef;
   for (int c = blockIdx.x; c < nchunks; c += gridDim.x) {
     const AdamChunk ch = chunks[c];
-    const float decay = a.decay[ch.group], step_size = a.step_size[ch.group];
+    const float decay = a.sp->adam_decay[ch.group], step_size = a.sp->adam_step[ch.group];
+    const float inv_sqrt_bc2 = a.sp->adam_inv_sqrt_bc2;
     const int64_t nv = ch.vec ? ch.n / 4 : 0;
     float4* pv = reinterpret_cast<float4*>(ch.p);
     float4* mv = reinterpret_cast<float4*>(ch.m);
@@ -368,10 +369,10 @@ __global__ void __launch_bounds__(kAdamThreads) adamw_kernel(const AdamChunk* __
         const float4 w = __ldg(reinterpret_cast<const float4*>(ch.g) + i);
         g[0] = w.x; g[1] = w.y; g[2] = w.z; g[3] = w.w;
       }
-      adam_one(p.x, m.x, v.x, g[0], coef, a, decay, step_size);
-      adam_one(p.y, m.y, v.y, g[1], coef, a, decay, step_size);
-      adam_one(p.z, m.z, v.z, g[2], coef, a, decay, step_size);
-      adam_one(p.w, m.w, v.w, g[3], coef, a, decay, step_size);
+      adam_one(p.x, m.x, v.x, g[0], coef, a, decay, step_size, inv_sqrt_bc2);
+      adam_one(p.y, m.y, v.y, g[1], coef, a, decay, step_size, inv_sqrt_bc2);
+      adam_one(p.z, m.z, v.z, g[2], coef, a, decay, step_size, inv_sqrt_bc2);
+      adam_one(p.w, m.w, v.w, g[3], coef, a, decay, step_size, inv_sqrt_bc2);
       pv[i] = p;
       mv[i] = m;
       vv[i] = v;
@@ -386,7 +387,7 @@ __global__ void __launch_bounds__(kAdamThreads) adamw_kernel(const AdamChunk* __
       float p = ch.p[j], m = ch.m[j], v = ch.v[j];
       const float g = ch.gdtype == DT_BF16 ? bf2f(static_cast<const uint16_t*>(ch.g)[j])
                                             : static_cast<const float*>(ch.g)[j];
-      adam_one(p, m, v, g, coef, a, decay, step_size);
+      adam_one(p, m, v, g, coef, a, decay, step_size, inv_sqrt_bc2);
       ch.p[j] = p;
       ch.m[j] = m;
       ch.v[j] = v;

@@ -211,3 +211,7 @@ def test_set_param_options_null_handle(mx):
 def test_record_grads_consumed_argument_errors(mx):
     lib = mx.load_library()
     assert lib.muon_adamw_record_grads_consumed(None, None) == mx.MA_ERR_ARG
+
+
+def test_set_graph_mode_null_handle(mx):
+    assert mx.load_library().muon_adamw_set_graph_mode(None, 1) == mx.MA_ERR_ARG
