@@ -43,13 +43,13 @@ STREAM_KINDS = ("grad_norm", "momentum", "adamw")
 
 
 # DRAM bytes per ns_tc_kernel launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# capture of the 6-layer case of this workload (the ns_tc_kernel summary in profiles/: one launch of
-# each product of a middle iteration and the last iteration's launch), averaged over a step's 15
-# launches (5 X X^T, 5 A A, 4 B X, 1 last) and scaled to the 16-layer h1024 workload by the matrices
-# processed (16/6: each launch reads its operands once and writes its output once). It describes only
-# the kernel sources it was measured on: any change to them makes it null until it is measured again.
-NS_TRAFFIC = {"sources_sha256": "590465411f18b9fb62787a255d2a7b6c489f61948ccbacbd910f596c77b6f1a5",
-              "bytes_per_launch": 894176597, "workload": "h1024"}
+# capture of the 6-layer case of this workload (the ns_tc_kernel summary in profiles/: the 12 launches
+# of iterations 2-5 of one step, averaged per product), weighted over a step's 15 launches (5 X X^T,
+# 5 A A, 4 B X, 1 last) and scaled to the 16-layer h1024 workload by the matrices processed (16/6:
+# each launch reads its operands once and writes its output once). It describes only the kernel
+# sources it was measured on: any change to them makes it null until it is measured again.
+NS_TRAFFIC = {"sources_sha256": "5e79b67f12fd78796db8f46b680c5cc5ebfe537bc9674f4bdae04c8e407464bc",
+              "bytes_per_launch": 887933458, "workload": "h1024"}
 NS_SOURCES = ("ns_tc.cu", "ns_epilogue.cuh", "internal.h")
 
 

@@ -101,11 +101,12 @@ typedef struct {
   int32_t muon_nesterov;
   int32_t ns_steps;
   int32_t ns_kernel;
-  /* reserved[0]: cross-check switches for tests, 0 in normal use. Bit 0
-   * exchanges the strides of the MN-major operand descriptor (a wrong layout
-   * that parity must catch); bit 1 runs every Newton-Schulz product without
-   * CTA pairs; bit 2 writes the last iteration's parameters from registers
-   * instead of through TMA. reserved[1..3] must be 0. */
+  /* reserved[0]: cross-check switches for tests, 0 in normal use; each
+   * selects another correct path, which the tests check against the oracle
+   * (bit 1) or bit for bit against the default (bit 2). Bit 1 runs every
+   * Newton-Schulz product without CTA clusters; bit 2 writes the last
+   * iteration's parameters from registers instead of through TMA. Other bits
+   * and reserved[1..3] must be 0 (MA_ERR_ARG). */
   int32_t reserved[4];
   int32_t muon_momentum_form;          /* ma_momentum_form; default MA_MOMENTUM_SGD */
   /* 1: AdamW parameters whose lower-cased name ends with "bias" or contains

@@ -580,7 +580,6 @@ ma_status build_plan(muon_adamw* h) {
             }
             L.total_tiles = tiles_total;
             L.err = h->d_err;
-            L.mn_swap = (c.reserved[0] & 1) ? 1 : 0;
             L.cl = cl;
             h->tc[kind][it].push_back(L);
           }
@@ -623,6 +622,7 @@ ma_status valid_config(const muon_adamw_config* c) {
       for (int k = 0; k < 3; ++k)
         if (!isfinite(c->ns_schedule[i][k])) return fail(MA_ERR_ARG, "non-finite ns_schedule entry");
   }
+  if (c->reserved[0] & ~6) return fail(MA_ERR_ARG, "unknown cross-check bits in reserved[0]");
   for (int i = 1; i < 4; ++i)
     if (c->reserved[i] != 0) return fail(MA_ERR_ARG, "reserved[%d] must be 0", i);
   if (!(c->adam_beta1 >= 0.0 && c->adam_beta1 < 1.0) || !(c->adam_beta2 >= 0.0 && c->adam_beta2 < 1.0))

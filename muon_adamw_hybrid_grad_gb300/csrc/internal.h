@@ -168,7 +168,7 @@ struct TcLaunch {
   int32_t total_tiles;  // work units in the launch
   NsEpiArgs epi;
   int* err;             // device error flag
-  int32_t mn_swap;      // cross-check knob: exchange LBO/SBO of the MN-major descriptor
+  int32_t pad0;
   int32_t cl;           // CTAs per cluster: 1, or 2 (operand multicast between a CTA pair)
   int32_t stall_test;   // test hook: CTA 0's producer issues no loads (its waits then run out)
   int32_t pad;
@@ -186,7 +186,6 @@ bool tc_encode_problem(TcProblem& tp, int cl, char* errbuf, size_t errlen);
 cudaError_t ns_tc_prepare(int* max_pairs);
 // grid_units: clusters to launch (CTAs = grid_units * cl), capped at the work units.
 cudaError_t launch_ns_tc(const TcLaunch& L, int grid_units, cudaStream_t st);
-size_t ns_tc_smem_bytes();
 int ns_tc_num_tiles_sym(int units_m, int bmu, int bn);  // lower-triangle work units per matrix
 
 }  // namespace ma

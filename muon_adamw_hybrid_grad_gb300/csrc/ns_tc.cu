@@ -839,8 +839,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
         const int kblocks = P.p.K / BK;
         const bool sym = P.p.kind != NS_UPDATE;
         const uint32_t idesc = idesc_bf16(G * BM, P.bn, !sym);
-        const uint32_t lbo_mn = L.mn_swap ? 1024u : 64u * BK * 2u;
-        const uint32_t sbo_mn = L.mn_swap ? 64u * BK * 2u : 1024u;
+        // MN-major right-hand operand: 64-element panels 8 KB apart (LBO), 8-row groups 1 KB apart (SBO)
+        constexpr uint32_t lbo_mn = 64u * BK * 2u;
+        constexpr uint32_t sbo_mn = 1024u;
         // the epilogues (PAIR: of both CTAs) have released this accumulator
         if (!mbar_wait<PAIR>(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, L.err, kErrWaitMma)) break;
         tc_fence_after();
@@ -1044,14 +1045,6 @@ bool tc_encode_param_maps(CUtensorMap* maps, const MuonMat& M) {
                                 (uint64_t)M.m, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
     return false;
   return true;
-}
-
-size_t ns_tc_smem_bytes() {
-  size_t m = Smem<false, false>::BYTES;
-  if (Smem<false, true>::BYTES > m) m = Smem<false, true>::BYTES;
-  if (Smem<true, false>::BYTES > m) m = Smem<true, false>::BYTES;
-  if (Smem<true, true>::BYTES > m) m = Smem<true, true>::BYTES;
-  return m;
 }
 
 namespace {

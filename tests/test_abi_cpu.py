@@ -185,6 +185,7 @@ def test_config_struct_matches_c_layout(mx):
     ("ns_schedule_len", 4),          # != ns_steps
     ("ns_schedule_len", 17),
     ("reserved1", 1),
+    ("reserved0_bit0", 1),
     ("schedule_nan", 0),
 ])
 def test_invalid_variant_config_is_rejected(mx, field, value):
@@ -193,6 +194,8 @@ def test_invalid_variant_config_is_rejected(mx, field, value):
     c = mx.muon_adamw_config_init()
     if field == "reserved1":
         c.reserved[1] = value
+    elif field == "reserved0_bit0":
+        c.reserved[0] = value
     elif field == "schedule_nan":
         c.ns_schedule_len = 5
         c.ns_schedule[2][1] = float("nan")

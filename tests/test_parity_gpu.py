@@ -72,6 +72,15 @@ def test_ragged_shapes_and_chunk_tails(mx, ns_kernel):
     assert r["worst_o"] <= O_TOL
 
 
+def test_without_cta_clusters(mx):
+    """Cross-check switch: every Newton-Schulz product on single CTAs
+    (cta_group::1, no multicast) instead of CTA pairs, against the oracle."""
+    w = workloads.get_workload("tiny")
+    w = workloads.custom_workload("tiny", w.tensors, policy="bf16_mixed", steps=2)
+    r = run_parity(w, config={"reserved": [2]})
+    assert r["worst_o"] <= O_TOL
+
+
 def test_fp32_gradients(mx):
     w = workloads.get_workload("tiny")
     w = workloads.custom_workload("tiny_fp32g", w.tensors, grad_dtype="fp32", policy="fp32_mixed", steps=2)
