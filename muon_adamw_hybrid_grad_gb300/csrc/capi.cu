@@ -314,7 +314,9 @@ ma_status build_plan(muon_adamw* h) {
   for (int pi : h->adam_params) n_adam += chunks_of(h->params[pi].numel);
   for (int pi : h->muon_params) {
     const Param& p = h->params[pi];
-    n_tiles += (size_t)((p.shape[0] + kMomTile - 1) / kMomTile) * (size_t)((p.shape[1] + kMomTile - 1) / kMomTile);
+    const bool tall = p.shape[0] > p.shape[1];
+    const int64_t tr = tall ? kMomTile : kMomWideRows, tc = tall ? kMomTile : kMomWideCols;
+    n_tiles += (size_t)((p.shape[0] + tr - 1) / tr) * (size_t)((p.shape[1] + tc - 1) / tc);
     ++n_mats;
   }
   h->norm_grid = (int)std::max<size_t>(1, std::min<size_t>(n_norm, (size_t)4 * h->num_sms));
@@ -474,8 +476,9 @@ ma_status build_plan(muon_adamw* h) {
                   ? 1
                   : 0;
       M.tile_begin = (int)tiles.size();
-      for (int r0 = 0; r0 < M.m; r0 += kMomTile)
-        for (int c0 = 0; c0 < M.n; c0 += kMomTile) tiles.push_back(MomTile{mat_index, r0, c0, 0});
+      const int tr = M.transposed ? kMomTile : kMomWideRows, tcol = M.transposed ? kMomTile : kMomWideCols;
+      for (int r0 = 0; r0 < M.m; r0 += tr)
+        for (int c0 = 0; c0 < M.n; c0 += tcol) tiles.push_back(MomTile{mat_index, r0, c0, 0});
       M.tile_end = (int)tiles.size();
       mats.push_back(M);
       ++mat_index;

@@ -10,9 +10,13 @@ namespace ma {
 
 // Elements per multi-tensor chunk of the gradient-norm and AdamW streams.
 constexpr int64_t kChunk = 1 << 16;
-// Edge of the square tiles the Muon momentum kernel walks, and the partial
-// sums of squares it writes per tile (one per warp).
+// Tiles of 4096 elements the Muon momentum kernel walks: 64 x 64 for tall
+// matrices (their X is written transposed through a shared tile), 16 rows x
+// 256 columns for the others (longer contiguous row segments); and the
+// partial sums of squares it writes per tile (one per warp).
 constexpr int kMomTile = 64;
+constexpr int kMomWideRows = 16;
+constexpr int kMomWideCols = 256;
 constexpr int kMomPartialsPerTile = 8;
 // Padding granule of the canonical Newton-Schulz workspaces (rows and cols).
 constexpr int kPad = 128;

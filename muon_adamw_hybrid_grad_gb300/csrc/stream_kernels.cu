@@ -182,8 +182,10 @@ __global__ void __launch_bounds__(kClipThreads) clip_finalize_kernel(const float
 
 // ---------------------------------------------------------------------------
 // Muon momentum + canonical bf16 pack.
-// One 64x64 tile of one parameter per iteration; 256 threads, each owns an
-// 8-wide column group of two rows. buf <- mu*buf + w*coef*g; the update
+// One tile of one parameter per iteration (64 x 64 for tall matrices, 16
+// rows x 256 columns otherwise, so that a warp streams 1 KB row segments);
+// 256 threads, each owns an 8-wide column group of two rows. buf <- mu*buf +
+// w*coef*g; the update
 // (Nesterov: w*coef*g + mu*buf) goes to X in bf16; w = 1, or 1 - mu for the
 // exponential-average form of the momentum. Wide matrices (X = update)
 // are written straight from registers, 16 bytes per thread, with no block
@@ -198,22 +200,29 @@ __global__ void __launch_bounds__(kMomThreads) muon_momentum_kernel(const MomTil
                                                                     const MuonMat* __restrict__ mats,
                                                                     const StepScalars* __restrict__ sc, MomArgs args,
                                                                     float* __restrict__ tile_partials) {
-  __shared__ __align__(16) uint16_t su[2][kMomTile][kMomTile + 8];
+  // transpose tiles of tall matrices: 16-byte chunk c of row r sits at chunk
+  // c ^ ((r >> 3) & 7), so that a thread writes its 8 values as one chunk and
+  // the column reads of the write-out hit 8 different chunks (banks)
+  __shared__ __align__(16) uint16_t su[2][kMomTile][kMomTile];
   const float coef = sc->coef * args.gscale;
   const float mu = args.mu;
-  const int cg = threadIdx.x & 7;   // column group (8 columns)
-  const int rr = threadIdx.x >> 3;  // row 0..31
+  // tall matrices: 64 x 64 tiles, 8 column groups x 32 rows of threads (rows r, r + 32)
+  const int cg = threadIdx.x & 7;
+  const int rr = threadIdx.x >> 3;
+  // other matrices: 16 x 256 tiles, a warp per row pair (rows w, w + 8) over 32 column groups
+  const int cgw = threadIdx.x & 31;
+  const int rrw = threadIdx.x >> 5;
   int ntrans = 0;                   // transposed tiles seen: selects the shared buffer
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const MomTile tl = tiles[t];
     const MuonMat M = mats[tl.mat];
-    uint16_t(*sbuf)[kMomTile + 8] = su[ntrans & 1];
+    uint16_t(*sbuf)[kMomTile] = su[ntrans & 1];
     float acc = 0.f;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      const int r = rr + 32 * half;
+      const int r = M.transposed ? rr + 32 * half : rrw + 8 * half;
       const int64_t gr = tl.r0 + r;
-      const int gc = tl.c0 + cg * 8;
+      const int gc = tl.c0 + (M.transposed ? cg : cgw) * 8;
       float u[8];
       const bool vec = gr < M.m && gc + 8 <= M.n && M.vec;
       if (vec) {
@@ -272,8 +281,8 @@ __global__ void __launch_bounds__(kMomThreads) muon_momentum_kernel(const MomTil
           }
         }
       } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sbuf[r][cg * 8 + e] = f2bf(u[e]);
+        *reinterpret_cast<uint4*>(&sbuf[r][(cg ^ ((r >> 3) & 7)) * 8]) =
+            make_uint4(pack2(u[0], u[1]), pack2(u[2], u[3]), pack2(u[4], u[5]), pack2(u[6], u[7]));
       }
     }
     if (M.transposed) {
@@ -286,8 +295,10 @@ __global__ void __launch_bounds__(kMomThreads) muon_momentum_kernel(const MomTil
         const int pr = tl.r0 + cg * 8;
         if (pc < M.n) {
           uint16_t v[8];
+          // rows cg*8 .. cg*8+7 all have (row >> 3) & 7 == cg
+          const int col = (((cc >> 3) ^ cg) << 3) | (cc & 7);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = sbuf[cg * 8 + e][cc];
+          for (int e = 0; e < 8; ++e) v[e] = sbuf[cg * 8 + e][col];
           uint16_t* dst = M.x0 + pc * (int64_t)M.L + pr;
           if (pr + 8 <= M.m) {
             uint4 w;
