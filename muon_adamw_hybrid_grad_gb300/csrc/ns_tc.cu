@@ -128,8 +128,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // false if the CTA is aborting or the wait ran past the limit (then the
 // abort flag and the device error code are set).
 template <bool CLUSTER = false>
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, int code) {
-  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                            int code) {
   const uint64_t t0 = global_timer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
@@ -142,6 +142,14 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       }
     }
   }
+}
+
+// The common case (the phase has already completed, or completes within the
+// instruction's own suspend window) stays inline on the issuing warps' paths.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err, int code) {
+  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
+  return mbar_wait_slow<CLUSTER>(bar, parity, abort_flag, err, code);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
@@ -362,8 +370,12 @@ __device__ __forceinline__ uint32_t u4_get(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// Two floats rounded to nearest-even bf16 in one conversion: lo in the low
+// half, hi in the high half (the same rounding as two scalar conversions).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return (uint32_t)ns_f2bf(lo) | ((uint32_t)ns_f2bf(hi) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Epilogue of one 32x32 block of the accumulator for A = X X^T,
@@ -390,6 +402,8 @@ __device__ __forceinline__ void epilogue_block(const NsProblem& pb, const CUtens
   if (row0 >= s || col0 >= lim) return;      // padding only: never written
   if (!update && col0 >= row0 + 32) return;  // above the diagonal: the mirror of a lower block
   const int gi = row0 + lane;
+  // warp-uniform: the block lies inside the matrix (no element to zero)
+  const bool inside = row0 + 32 <= s && col0 + 32 <= lim;
   uint4 preA[4];
   if (pb.kind == NS_POLY) {
 #pragma unroll
@@ -404,38 +418,57 @@ __device__ __forceinline__ void epilogue_block(const NsProblem& pb, const CUtens
   tmem_ld_32x32b_x32(taddr, r);
   tmem_ld_wait();
   float o[32];
-  if (update) {
-    const float rs = pb.first ? pb.rscale[mat] : 1.f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]) * rs;
-  } else if (pb.kind == NS_GRAM) {
-    const float sc = pb.first ? pb.rscale[mat] * pb.rscale[mat] : 1.f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]) * sc;
-  } else {
+  if (pb.kind == NS_POLY) {
+    // c (A A) + (b A + a I); the a I term only in blocks on the diagonal
+    const bool on_diag = col0 == row0;
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       const uint32_t u = u4_get(preA[e >> 3], (e >> 1) & 3);
       const float a = __uint_as_float((e & 1) ? (u & 0xFFFF0000u) : (u << 16));
-      o[e] = fmaf(ep.c, __uint_as_float(r[e]), fmaf(ep.b, a, col0 + e == gi ? ep.a : 0.f));
+      const float lin = on_diag ? fmaf(ep.b, a, e == lane ? ep.a : 0.f) : ep.b * a;
+      o[e] = fmaf(ep.c, __uint_as_float(r[e]), lin);
     }
-  }
+  } else if (pb.first) {
+    // first iteration: the Frobenius scale r (r^2 for A = X X^T)
+    const float rs = pb.rscale[mat];
+    const float sc = update ? rs : rs * rs;
 #pragma unroll
-  for (int e = 0; e < 32; ++e)
-    if (gi >= s || col0 + e >= lim) o[e] = 0.f;
+    for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]) * sc;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]);
+  }
+  if (!inside) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (gi >= s || col0 + e >= lim) o[e] = 0.f;
+  }
 
   uint8_t* const ct = rt + 2048;
   if (lane == 0) bulk_wait_read_all();  // the previous block's stores have read both tiles
   __syncwarp();
+  uint32_t pk[16];  // this lane's row as bf16 pairs (columns 2j, 2j + 1)
+#pragma unroll
+  for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(o[2 * j], o[2 * j + 1]);
   uint4* const rrow = reinterpret_cast<uint4*>(rt + lane * 64);
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    rrow[q ^ ((lane >> 1) & 3)] = make_uint4(pack_bf16x2(o[8 * q + 0], o[8 * q + 1]), pack_bf16x2(o[8 * q + 2], o[8 * q + 3]),
-                                             pack_bf16x2(o[8 * q + 4], o[8 * q + 5]), pack_bf16x2(o[8 * q + 6], o[8 * q + 7]));
+    rrow[q ^ ((lane >> 1) & 3)] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
   // blocks are 32-aligned: one meets the diagonal iff col0 == row0
   const bool diag = !update && col0 == row0;
   const bool below = !update && col0 + 32 <= row0;
-  if (diag) {
+  if (below) {
+    // transposed tile T[c][r] = block[r][c], written as bf16 pairs: lanes 2k
+    // and 2k + 1 swap their packed rows; the even lane writes T[2j][2k..2k+1]
+    // (both low halves), the odd lane T[2j+1][2k..2k+1] (both high halves)
+    const uint32_t sel = (lane & 1) ? 0x3276u : 0x5410u;
+    uint8_t* const tb = ct + (lane & 1) * 64 + ((lane >> 1) & 3) * 4;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t oth = __shfl_xor_sync(0xffffffffu, pk[j], 1);
+      *reinterpret_cast<uint32_t*>(tb + 2 * j * 64 + (((lane >> 3) ^ (j & 3)) << 4)) = __byte_perm(pk[j], oth, sel);
+    }
+  } else if (diag) {
     __syncwarp();
     // (row e, column lane) for e < lane <- (row lane, column e)
 #pragma unroll
@@ -443,11 +476,6 @@ __device__ __forceinline__ void epilogue_block(const NsProblem& pb, const CUtens
       if (e < lane)
         *reinterpret_cast<uint16_t*>(rt + e * 64 + (((lane >> 3) ^ ((e >> 1) & 3)) << 4) + (lane & 7) * 2) =
             ns_f2bf(o[e]);
-  } else if (below) {
-#pragma unroll
-    for (int e = 0; e < 32; ++e)
-      *reinterpret_cast<uint16_t*>(ct + e * 64 + (((lane >> 3) ^ ((e >> 1) & 3)) << 4) + (lane & 7) * 2) =
-          ns_f2bf(o[e]);
   }
   fence_proxy_async_smem();
   __syncwarp();
@@ -693,6 +721,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
   static_assert(!PAIR || CL == 2, "a paired MMA needs a CTA pair");
   constexpr int G = PAIR ? 2 : 1;  // tcgen05 cta_group
   using SM = Smem<PAIR, APPLY>;
+  static_assert((SM::BYTES >> 4) < 0x4000, "operand descriptors: 14-bit address field");
   constexpr int STAGES = SM::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -833,15 +862,23 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      // Descriptors of stage 0's operands; a stage is STAGE bytes further
+      // (the address field counts 16-byte units, so stage and K16 steps are
+      // plain additions). K-major: the K16 step is 32 bytes. MN-major
+      // right-hand operand: 64-element panels 8 KB apart (LBO), 8-row groups
+      // 1 KB apart (SBO), the K16 step is 16 rows of 128 bytes.
+      const uint32_t s0 = smem_u32(smem);
+      const uint64_t a_desc0 = sdesc(s0, 16, 1024);
+      const uint64_t bk_desc0 = sdesc(s0 + A_STAGE, 16, 1024);
+      const uint64_t bmn_desc0 = sdesc(s0 + A_STAGE, 64u * BK * 2u, 1024u);
       for (int g = unit0; g < L.total_tiles && ok; g += nunits) {
         const TileCoord c = decode_tile(L, g);
         const TcProblem& P = L.prob[c.prob];
         const int kblocks = P.p.K / BK;
         const bool sym = P.p.kind != NS_UPDATE;
         const uint32_t idesc = idesc_bf16(G * BM, P.bn, !sym);
-        // MN-major right-hand operand: 64-element panels 8 KB apart (LBO), 8-row groups 1 KB apart (SBO)
-        constexpr uint32_t lbo_mn = 64u * BK * 2u;
-        constexpr uint32_t sbo_mn = 1024u;
+        const uint64_t b_desc0 = sym ? bk_desc0 : bmn_desc0;
+        const uint32_t b_kstep = sym ? 2u : 128u;
         // the epilogues (PAIR: of both CTAs) have released this accumulator
         if (!mbar_wait<PAIR>(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, L.err, kErrWaitMma)) break;
         tc_fence_after();
@@ -852,14 +889,12 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + (size_t)stage * SM::STAGE);
-          const uint32_t sb = sa + A_STAGE;
+          const uint32_t soff = (uint32_t)stage * (uint32_t)(SM::STAGE >> 4);
+          const uint64_t ad = a_desc0 + soff;
+          const uint64_t bd = b_desc0 + soff;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = sdesc(sa + kk * 32, 16, 1024);
-            const uint64_t bd = sym ? sdesc(sb + kk * 32, 16, 1024) : sdesc(sb + kk * 16 * 128, lbo_mn, sbo_mn);
-            umma_bf16<G>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16<G>(d_tmem, ad + 2u * kk, bd + b_kstep * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
           if (PAIR)
             umma_commit_pair(empty0 + 8 * stage);  // both CTAs' parts of this stage are free
           else if (CL == 2)
