@@ -24,6 +24,7 @@ the source pages ship no code) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import math
 import os
@@ -48,8 +49,8 @@ STREAM_KINDS = ("grad_norm", "momentum", "adamw")
 # 5 A A, 4 B X, 1 last) and scaled to the 16-layer h1024 workload by the matrices processed (16/6:
 # each launch reads its operands once and writes its output once). It describes only the kernel
 # sources it was measured on: any change to them makes it null until it is measured again.
-NS_TRAFFIC = {"sources_sha256": "bc98deaf8011f0b27df2259748e932cccf1da03fc567470d624acb2ceb7de02f",
-              "bytes_per_launch": 888809518, "workload": "h1024"}
+NS_TRAFFIC = {"sources_sha256": "ee1d9b8f03fbda1ac8c9604303979c92c387edc52edbbe22620045de3fa104f5",
+              "bytes_per_launch": 890337678, "workload": "h1024"}
 NS_SOURCES = ("ns_tc.cu", "ns_epilogue.cuh", "internal.h")
 
 
@@ -298,11 +299,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    gc.disable()
     ev0.record(stream)
     for _ in range(args.steps):
         opt.step(lr)
     ev1.record(stream)
     torch.cuda.synchronize()
+    gc.enable()
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
@@ -313,15 +316,29 @@ def run_ours(args):
     value = aggregate(args.steps, world, max_s)
 
     # ---- end to end: grads from pinned host memory each step, norm read back ----
-    h2d = total * gflat.element_size()
+    # per step: the flat gradient buffer, plus the library's own copy of the
+    # step's lr- and step-dependent scalars (112 bytes); back: the norm and
+    # clip factor (16 bytes) and the device error flag (4 bytes)
+    h2d = total * gflat.element_size() + 112
+    d2h = 16 + 4
     # Each step's gradients are copied on a copy stream as soon as the previous
     # step has read its gradients (muon_adamw_record_grads_consumed), so the
     # copy overlaps that step's Newton-Schulz chain; every step's copy and the
     # read-back of every step's norm are inside the timed region.
     copy_stream = torch.cuda.Stream(device=dev)
+    # Two untimed steps through the same path first (the copy stream, its
+    # events and the pinned-copy bookkeeping are set up on first use); the
+    # timed region still holds every timed step's copy, the first one included.
+    for _ in range(2):
+        with torch.cuda.stream(copy_stream):
+            gflat.copy_(hflat, non_blocking=True)
+        stream.wait_event(copy_stream.record_event())
+        opt.step(lr)
+        mx.muon_adamw_last_norm(opt.handle)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
+    gc.disable()  # no collector pause inside the host-timed loop
     t0 = time.perf_counter()
     with torch.cuda.stream(copy_stream):
         gflat.copy_(hflat, non_blocking=True)  # step 1's gradients
@@ -334,6 +351,7 @@ def run_ours(args):
                 gflat.copy_(hflat, non_blocking=True)  # step k+2's gradients
         mx.muon_adamw_last_norm(opt.handle)  # synchronises and reads this step's norm
     e2e_s = time.perf_counter() - t0
+    gc.enable()
     e2e_s = max_over_ranks(e2e_s, dist, dev)
 
     peaks = load_peaks()
@@ -401,11 +419,11 @@ def run_ours(args):
         },
         "clocks": clk,
         "e2e": {"value": round(args.steps * world / e2e_s, 3), "unit": "steps/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": d2h,
                 "how": "every step: every gradient copied host->device from pinned memory (one copy of the "
                        "flat gradient buffer, issued once the previous step has read its gradients and "
                        "overlapping that step's Newton-Schulz chain), muon_adamw_step, and the step's norm "
-                       "read back (synchronising)"},
+                       "read back (synchronising); two untimed steps through the same path first"},
         "gpu_launches": int(launches),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
