@@ -158,6 +158,7 @@ struct muon_adamw {
   int adam_grid = 0;
   MuonMat* d_mats = nullptr;
   CUtensorMap* d_pmaps = nullptr;  // per Muon matrix: TMA maps of p and shadow
+  int32_t* d_orders = nullptr;     // work orders of the tensor-core launches
   int n_mats = 0;
   MomTile* d_tiles = nullptr;
   int n_tiles = 0;
@@ -593,6 +594,41 @@ ma_status build_plan(muon_adamw* h) {
   if (c.ns_kernel == MA_NS_TCGEN05 && !h->buckets.empty()) {
     CUDA_TRY(ns_tc_prepare(&h->max_pairs));
     if (h->max_pairs < 1) h->max_pairs = 1;
+    // each launch's work order, for the clusters that can be resident at once
+    std::vector<int32_t> all, one;
+    std::vector<size_t> at;
+    for (int kind = 0; kind < 3; ++kind)
+      for (int it = 0; it < steps; ++it)
+        for (TcLaunch& L : h->tc[kind][it]) {
+          const int ncl = std::min(L.cl == 2 ? h->max_pairs : h->num_sms, L.total_tiles);
+          tc_unit_order(L, ncl, one);
+          L.nclusters = ncl;
+          // the plain round-robin order needs no table (position = unit)
+          bool plain = true;
+          for (size_t i = 0; i < one.size() && plain; ++i)
+            plain = one[i] == ((int64_t)i < L.total_tiles ? (int32_t)i : -1);
+          if (plain) {
+            L.npos = L.total_tiles;
+            at.push_back(SIZE_MAX);
+          } else {
+            L.npos = (int32_t)one.size();
+            at.push_back(all.size());
+            all.insert(all.end(), one.begin(), one.end());
+          }
+        }
+    if (h->d_orders) cudaFree(h->d_orders);
+    h->d_orders = nullptr;
+    if (!all.empty()) {
+      CUDA_TRY(cudaMalloc(&h->d_orders, all.size() * sizeof(int32_t)));
+      CUDA_TRY(cudaMemcpy(h->d_orders, all.data(), all.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+    }
+    size_t li = 0;
+    for (int kind = 0; kind < 3; ++kind)
+      for (int it = 0; it < steps; ++it)
+        for (TcLaunch& L : h->tc[kind][it]) {
+          const size_t a = at[li++];
+          L.order = a == SIZE_MAX ? nullptr : h->d_orders + a;
+        }
   }
   h->planned = true;
   return MA_OK;
@@ -720,9 +756,8 @@ static ma_status enqueue_newton_schulz(muon_adamw* h) {
           L.epi = epi;
           L.stall_test = h->stall_test ? 1 : 0;
           h->stall_test = false;  // one launch only
-          const int grid_units = L.cl == 2 ? h->max_pairs : h->num_sms;
           const int pk = (kind == NS_UPDATE && it == c.ns_steps - 1) ? MA_K_NS_APPLY : MA_K_NS_GRAM + kind;
-          timed(h, pk, h->s0, units[kind] / h->tc[kind][it].size(), [&] { launch_ns_tc(L, grid_units, h->s0); });
+          timed(h, pk, h->s0, units[kind] / h->tc[kind][it].size(), [&] { launch_ns_tc(L, h->s0); });
         }
       } else {
         const int pk = (kind == NS_UPDATE && it == c.ns_steps - 1) ? MA_K_NS_APPLY : MA_K_NS_GRAM + kind;
@@ -1132,6 +1167,7 @@ ma_status muon_adamw_destroy(muon_adamw_t* h) {
   if (h->ev_g0) cudaEventDestroy(h->ev_g0);
   if (h->ev_g1) cudaEventDestroy(h->ev_g1);
   if (h->gexec) cudaGraphExecDestroy(h->gexec);
+  if (h->d_orders) cudaFree(h->d_orders);
   for (int k = 0; k < 2; ++k)
     if (h->ev_slot[k]) cudaEventDestroy(h->ev_slot[k]);
   if (h->h_step) cudaFreeHost(h->h_step);

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 namespace ma {
 
 // Elements per multi-tensor chunk of the gradient-norm and AdamW streams.
@@ -172,10 +174,14 @@ struct TcLaunch {
   int32_t total_tiles;  // work units in the launch
   NsEpiArgs epi;
   int* err;             // device error flag
-  int32_t pad0;
+  // Work assignment: cluster c takes the units order[c], order[c + nclusters],
+  // ... (npos entries, -1 = nothing), from tc_unit_order; no table (nullptr)
+  // when that is the plain round-robin order (position = unit).
+  const int32_t* order;
+  int32_t npos;
+  int32_t nclusters;    // clusters in the grid
   int32_t cl;           // CTAs per cluster: 1, or 2 (operand multicast between a CTA pair)
   int32_t stall_test;   // test hook: CTA 0's producer issues no loads (its waits then run out)
-  int32_t pad;
 };
 // TMA maps of one parameter for the last iteration's write-back: maps[0] the
 // fp32 master, maps[1] the bf16 shadow (unused without one); 32 x 32 boxes.
@@ -185,11 +191,17 @@ bool tc_encode_param_maps(CUtensorMap* maps, const MuonMat& M);
 bool ns_tc_pairable(const NsProblem& p);
 // Encode the tensor maps of `tp` and count its work units for cluster size cl (host).
 bool tc_encode_problem(TcProblem& tp, int cl, char* errbuf, size_t errlen);
+// Static assignment of a launch's work units to `ncl` clusters (host): each
+// unit, in the launch's order (longest first), goes to the cluster with the
+// least work so far (a unit costs its K / 64 k-steps plus a fixed 6), ties to
+// the lowest index; laid out round by round, -1 where a cluster has no unit.
+// Units of equal cost give the plain round-robin order.
+void tc_unit_order(const TcLaunch& L, int ncl, std::vector<int32_t>& order);
 // Sets the kernels' dynamic shared-memory limit (current device) and returns
 // how many CTA pairs can be resident at once.
 cudaError_t ns_tc_prepare(int* max_pairs);
 // grid_units: clusters to launch (CTAs = grid_units * cl), capped at the work units.
-cudaError_t launch_ns_tc(const TcLaunch& L, int grid_units, cudaStream_t st);
+cudaError_t launch_ns_tc(const TcLaunch& L, cudaStream_t st);  // grid: L.nclusters clusters
 int ns_tc_num_tiles_sym(int units_m, int bmu, int bn);  // lower-triangle work units per matrix
 
 }  // namespace ma

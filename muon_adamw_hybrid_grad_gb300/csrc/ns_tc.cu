@@ -31,6 +31,9 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <queue>
+#include <utility>
+
 #include "internal.h"
 #include "ns_epilogue.cuh"
 
@@ -337,6 +340,12 @@ struct TileCoord {
 
 // Work unit g -> (problem, matrix, row unit, column block). A row unit is
 // L.cl consecutive 128-row blocks (one per CTA of the cluster).
+// The work unit at position `pos` of the launch's order (no table: the
+// plain round-robin order, position = unit).
+__device__ __forceinline__ int unit_at(const TcLaunch& L, int pos) {
+  return L.order != nullptr ? __ldg(L.order + pos) : pos;
+}
+
 __device__ __forceinline__ TileCoord decode_tile(const TcLaunch& L, int g) {
   TileCoord c{0, 0, 0, 0};
   int pi = 0;
@@ -560,7 +569,11 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
   uint32_t pend = 0;  // bit b: a load into buffer b is in flight
   int acc = 0;
   uint32_t acc_phase = 0;
-  for (int g = unit0; g < L.total_tiles; g += nunits) {
+  int g_next = unit0 < L.npos ? unit_at(L, unit0) : -1;
+  for (int pos = unit0; pos < L.npos; pos += nunits) {
+    const int g = g_next;  // read one unit ahead, off this unit's critical path
+    g_next = pos + nunits < L.npos ? unit_at(L, pos + nunits) : -1;
+    if (g < 0) continue;
     const TileCoord c = decode_tile(L, g);
     const TcProblem& P = L.prob[c.prob];
     const MuonMat& M = P.p.mats[c.mat];
@@ -741,7 +754,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
   const uint32_t crank = CL == 2 ? cluster_ctarank() : 0u;
   const bool leader = crank == 0;
   const bool issues_mma = !PAIR || leader;
-  const int unit0 = blockIdx.x / CL;  // this cluster's first work unit
+  const int unit0 = blockIdx.x / CL;  // this cluster's first position in the work order
   const int nunits = gridDim.x / CL;  // clusters in the grid
   const uint16_t mc_mask = (uint16_t)((1u << CL) - 1u);
 
@@ -782,7 +795,11 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       // test hook: with stall_test, CTA 0 issues nothing, so its MMA warp's
       // bounded wait for the first stage runs out and reports the error
       bool ok = !(L.stall_test && blockIdx.x == 0);
-      for (int g = unit0; g < L.total_tiles && ok; g += nunits) {
+      int g_next = unit0 < L.npos ? unit_at(L, unit0) : -1;
+      for (int pos = unit0; pos < L.npos && ok; pos += nunits) {
+        const int g = g_next;  // read one unit ahead, off this unit's critical path
+        g_next = pos + nunits < L.npos ? unit_at(L, pos + nunits) : -1;
+        if (g < 0) continue;
         const TileCoord c = decode_tile(L, g);
         const TcProblem& P = L.prob[c.prob];
         const int kblocks = P.p.K / BK;
@@ -871,7 +888,11 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       const uint64_t a_desc0 = sdesc(s0, 16, 1024);
       const uint64_t bk_desc0 = sdesc(s0 + A_STAGE, 16, 1024);
       const uint64_t bmn_desc0 = sdesc(s0 + A_STAGE, 64u * BK * 2u, 1024u);
-      for (int g = unit0; g < L.total_tiles && ok; g += nunits) {
+      int g_next = unit0 < L.npos ? unit_at(L, unit0) : -1;
+      for (int pos = unit0; pos < L.npos && ok; pos += nunits) {
+        const int g = g_next;  // read one unit ahead, off this unit's critical path
+        g_next = pos + nunits < L.npos ? unit_at(L, pos + nunits) : -1;
+        if (g < 0) continue;
         const TileCoord c = decode_tile(L, g);
         const TcProblem& P = L.prob[c.prob];
         const int kblocks = P.p.K / BK;
@@ -937,7 +958,11 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
     uint8_t* const rt = smem + SM::SB + (size_t)(warp - 2) * SM::SB_PER_WARP;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int g = unit0; g < L.total_tiles; g += nunits) {
+    int g_next = unit0 < L.npos ? unit_at(L, unit0) : -1;
+    for (int pos = unit0; pos < L.npos; pos += nunits) {
+      const int g = g_next;  // read one unit ahead, off this unit's critical path
+      g_next = pos + nunits < L.npos ? unit_at(L, pos + nunits) : -1;
+      if (g < 0) continue;
       const TileCoord c = decode_tile(L, g);
       const TcProblem& P = L.prob[c.prob];
       // every lane waits; the vote keeps the warp converged for tcgen05.ld
@@ -1066,6 +1091,29 @@ bool tc_encode_problem(TcProblem& tp, int cl, char* errbuf, size_t errlen) {
   return true;
 }
 
+void tc_unit_order(const TcLaunch& L, int ncl, std::vector<int32_t>& order) {
+  std::vector<std::vector<int32_t>> lists((size_t)ncl);
+  using Entry = std::pair<double, int>;  // (work so far, cluster)
+  std::priority_queue<Entry, std::vector<Entry>, std::greater<Entry>> least;
+  for (int c = 0; c < ncl; ++c) least.push({0.0, c});
+  for (int q = 0; q < L.nprob; ++q) {
+    const TcProblem& P = L.prob[q];
+    const double cost = (double)(P.p.K / BK) + 6.0;
+    const int n = P.tiles_per_mat * P.p.nmat;
+    for (int u = 0; u < n; ++u) {
+      const Entry e = least.top();
+      least.pop();
+      lists[(size_t)e.second].push_back(P.tile_begin + u);
+      least.push({e.first + cost, e.second});
+    }
+  }
+  size_t rounds = 0;
+  for (const auto& l : lists) rounds = l.size() > rounds ? l.size() : rounds;
+  order.assign(rounds * (size_t)ncl, -1);
+  for (int c = 0; c < ncl; ++c)
+    for (size_t r = 0; r < lists[(size_t)c].size(); ++r) order[r * (size_t)ncl + (size_t)c] = lists[(size_t)c][r];
+}
+
 bool tc_encode_param_maps(CUtensorMap* maps, const MuonMat& M) {
   memset(maps, 0, 2 * sizeof(CUtensorMap));
   const bool shadow = M.shadow != nullptr;
@@ -1139,8 +1187,9 @@ cudaError_t ns_tc_prepare(int* max_pairs) {
   return cudaSuccess;
 }
 
-cudaError_t launch_ns_tc(const TcLaunch& L, int grid_units, cudaStream_t st) {
-  if (grid_units > L.total_tiles) grid_units = L.total_tiles;
+cudaError_t launch_ns_tc(const TcLaunch& L, cudaStream_t st) {
+  // the work order was laid out for exactly this many clusters
+  const int grid_units = L.nclusters;
   if (grid_units <= 0) return cudaSuccess;
   // every problem of a launch is the same product of the same iteration
   const bool update = L.prob[0].p.kind == NS_UPDATE;
