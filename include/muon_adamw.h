@@ -269,6 +269,21 @@ MA_API ma_status muon_adamw_set_graph_mode(muon_adamw_t* h, int enable);
  * (no step taken yet), MA_ERR_CUDA. */
 MA_API ma_status muon_adamw_record_grads_consumed(muon_adamw_t* h, void* cuda_event);
 
+/* The work order of one tensor-core Newton-Schulz launch (host only; needs no
+ * device): `nprob` (1..4) problems in launch order, problem q holding
+ * `units[q]` work units of reduction depth `k[q]` (a positive multiple of 64);
+ * units are numbered consecutively across the problems. Each unit goes, in
+ * that order, to the cluster with the least work so far (a unit costs k / 64
+ * plus 6), ties to the lowest cluster; the result is laid out round by round:
+ * cluster c runs order[c], order[c + nclusters], ..., and -1 marks a position
+ * with no unit. `*npos` receives the table length (a multiple of nclusters).
+ * The library builds the same table for every launch at planning time.
+ * Errors: MA_ERR_ARG (NULL pointer, nprob outside 1..4, nclusters < 1, a
+ * negative unit count or a bad k), MA_ERR_SHAPE (`cap` entries are too few;
+ * `*npos` is still set). */
+MA_API ma_status muon_adamw_plan_work_order(int nprob, const int64_t* k, const int64_t* units, int nclusters,
+                                            int32_t* order, int64_t cap, int64_t* npos);
+
 /* Test hook for the failure path, not for production use. Arms a one-shot
  * stall: in the next step's first Newton-Schulz launch, one CTA issues no
  * operand loads, so its MMA warp's bounded wait (2 s) runs out. The kernel

@@ -134,6 +134,10 @@ _SIGNATURES = {
     "muon_adamw_step": (ctypes.c_int, [_P, ctypes.c_double, ctypes.POINTER(ctypes.c_float)]),
     "muon_adamw_sync": (ctypes.c_int, [_P]),
     "muon_adamw_test_arm_stall": (ctypes.c_int, [_P]),
+    "muon_adamw_plan_work_order": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
+                                                  ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                                                  ctypes.POINTER(ctypes.c_int32), ctypes.c_int64,
+                                                  ctypes.POINTER(ctypes.c_int64)]),
     "muon_adamw_record_grads_consumed": (ctypes.c_int, [_P, _P]),
     "muon_adamw_set_graph_mode": (ctypes.c_int, [_P, ctypes.c_int]),
     "muon_adamw_set_param_options": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_double, ctypes.c_double]),
@@ -246,6 +250,21 @@ def muon_adamw_record_grads_consumed(h: int, cuda_event: int) -> None:
 
 def muon_adamw_test_arm_stall(h: int) -> None:
     _check(load_library().muon_adamw_test_arm_stall(_P(h)))
+
+
+def muon_adamw_plan_work_order(k, units, nclusters: int) -> list:
+    """Position -> unit table of one tensor-core launch (host only); -1 = no unit."""
+    n = len(k)
+    ka = (ctypes.c_int64 * n)(*k)
+    ua = (ctypes.c_int64 * n)(*units)
+    npos = ctypes.c_int64()
+    lib = load_library()
+    st = lib.muon_adamw_plan_work_order(n, ka, ua, nclusters, None, 0, ctypes.byref(npos))
+    if st not in (0, MA_ERR_SHAPE):
+        _check(st)
+    buf = (ctypes.c_int32 * max(1, npos.value))()
+    _check(lib.muon_adamw_plan_work_order(n, ka, ua, nclusters, buf, npos.value, ctypes.byref(npos)))
+    return list(buf)[:npos.value]
 
 
 def muon_adamw_get_state(h: int, index: int, which: int, dst_ptr: int) -> None:

@@ -1010,6 +1010,33 @@ ma_status muon_adamw_set_param_options(muon_adamw_t* h, int index, double lr_sca
   return ok();
 }
 
+ma_status muon_adamw_plan_work_order(int nprob, const int64_t* k, const int64_t* units, int nclusters,
+                                     int32_t* order, int64_t cap, int64_t* npos) {
+  if (!k || !units || !npos || (cap > 0 && !order)) return fail(MA_ERR_ARG, "NULL pointer");
+  if (nprob < 1 || nprob > kTcMaxProblems) return fail(MA_ERR_ARG, "nprob must be 1..%d", kTcMaxProblems);
+  if (nclusters < 1) return fail(MA_ERR_ARG, "nclusters must be >= 1");
+  TcLaunch L;
+  memset(&L, 0, sizeof L);
+  int64_t total = 0;
+  for (int q = 0; q < nprob; ++q) {
+    if (k[q] < 64 || k[q] % 64 != 0 || k[q] > INT32_MAX) return fail(MA_ERR_ARG, "k[%d] must be a positive multiple of 64", q);
+    if (units[q] < 0 || total + units[q] > INT32_MAX) return fail(MA_ERR_ARG, "bad unit count for problem %d", q);
+    L.prob[q].p.K = (int32_t)k[q];
+    L.prob[q].p.nmat = 1;
+    L.prob[q].tiles_per_mat = (int32_t)units[q];
+    L.prob[q].tile_begin = (int32_t)total;
+    total += units[q];
+  }
+  L.nprob = nprob;
+  L.total_tiles = (int32_t)total;
+  std::vector<int32_t> tab;
+  tc_unit_order(L, nclusters, tab);
+  *npos = (int64_t)tab.size();
+  if ((int64_t)tab.size() > cap) return fail(MA_ERR_SHAPE, "order needs %zu entries, capacity %lld", tab.size(), (long long)cap);
+  if (!tab.empty()) memcpy(order, tab.data(), tab.size() * sizeof(int32_t));
+  return ok();
+}
+
 ma_status muon_adamw_test_arm_stall(muon_adamw_t* h) {
   if (!h) return fail(MA_ERR_ARG, "NULL handle");
   if (h->cfg.ns_kernel != MA_NS_TCGEN05) return fail(MA_ERR_UNSUPPORTED, "only the tensor-core kernel has waits");
