@@ -375,6 +375,14 @@ __device__ __forceinline__ TileCoord decode_tile(const TcLaunch& L, int g) {
 }
 
 
+// A symmetric product's unit whose right-hand rows (this CTA's part of the
+// column block) are this CTA's own left-hand rows: the stage's left tile then
+// serves as the right-hand operand too and the second copy is not loaded.
+__device__ __forceinline__ bool rhs_is_lhs(const TcProblem& P, const TileCoord& c, int cl, uint32_t crank) {
+  const int nown = P.bn / cl;
+  return P.p.kind != NS_UPDATE && nown == BM && c.tj * P.bn + (int)crank * nown == (c.ti * cl + (int)crank) * BM;
+}
+
 __device__ __forceinline__ uint32_t u4_get(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
@@ -813,8 +821,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
         const int n0 = c.tj * P.bn + (int)crank * nown;
         const int nbox = sym ? nown / BM : nown / 64;
         const uint32_t own_off = PAIR ? 0u : (uint32_t)crank * (uint32_t)nown * BK * 2u;
+        const bool same = rhs_is_lhs(P, c, CL, crank);
         // bytes landing in this CTA per stage: its left rows + its (PAIR) or the whole right tile
-        const uint32_t tx = (uint32_t)(A_STAGE + (PAIR ? nown : P.bn) * BK * 2);
+        const uint32_t tx = (uint32_t)(A_STAGE + (same ? 0 : (PAIR ? nown : P.bn) * BK * 2));
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, L.err, kErrWaitProducer)) {
             ok = false;
@@ -829,7 +838,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
           } else {
             tma_load_2d_pair(sa, &P.tmP, kb * BK, rowP, mapa_shared(fb, 0));
           }
-          for (int q = 0; q < nbox; ++q) {
+          for (int q = 0; q < (same ? 0 : nbox); ++q) {
             // sym: rows (column block) of the same matrix, K-major; update: X, MN-major
             const uint32_t dst = sb + own_off + q * (sym ? BM * BK * 2 : 64 * BK * 2);
             const int x = sym ? kb * BK : n0 + q * 64;
@@ -898,7 +907,8 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
         const int kblocks = P.p.K / BK;
         const bool sym = P.p.kind != NS_UPDATE;
         const uint32_t idesc = idesc_bf16(G * BM, P.bn, !sym);
-        const uint64_t b_desc0 = sym ? bk_desc0 : bmn_desc0;
+        // the right-hand operand: the stage's right tile, or its left tile when the rows coincide
+        const uint64_t b_desc0 = rhs_is_lhs(P, c, CL, crank) ? a_desc0 : sym ? bk_desc0 : bmn_desc0;
         const uint32_t b_kstep = sym ? 2u : 128u;
         // the epilogues (PAIR: of both CTAs) have released this accumulator
         if (!mbar_wait<PAIR>(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, L.err, kErrWaitMma)) break;
