@@ -38,8 +38,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "optimizer steps/s; NS5 TFLOP/s vs bf16 peak; AdamW HBM GB/s vs peak"
-KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "ns_apply", "adamw")
-NS_KINDS = ("ns_gram", "ns_poly", "ns_update", "ns_apply")
+KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "ns_apply", "ns_fused", "adamw")
+NS_KINDS = ("ns_gram", "ns_poly", "ns_update", "ns_apply", "ns_fused")
 STREAM_KINDS = ("grad_norm", "momentum", "adamw")
 
 
@@ -438,7 +438,9 @@ def run_ours(args):
         if ns_ms > 0 else None,
         "kernels": kernels,
         "roofline": {
-            "kernel": "ns_tc_kernel (tcgen05 Newton-Schulz GEMMs: X X^T, A A, B X; all launches)",
+            "kernel": ("ns_tc_kernel (tcgen05 Newton-Schulz GEMMs: X X^T, A A, B X; all launches)"
+                       + (" and ns_small_kernel (small matrices: every iteration and the update in one launch)"
+                          if prof["ns_fused"]["launches"] else "")),
             "bound": "tensor",
             "achieved": round(ns_tflops, 1) if ns_tflops else None,
             "peak": peaks["bf16_tflops"],

@@ -105,8 +105,10 @@ typedef struct {
    * selects another correct path, which the tests check against the oracle
    * (bit 1) or bit for bit against the default (bit 2). Bit 1 runs every
    * Newton-Schulz product without CTA clusters; bit 2 writes the last
-   * iteration's parameters from registers instead of through TMA. Other bits
-   * and reserved[1..3] must be 0 (MA_ERR_ARG). */
+   * iteration's parameters from registers instead of through TMA; bit 8 runs
+   * small matrices (canonical 128 rows or fewer, at most 512 columns) through
+   * the per-product launches instead of the fused one. Other bits and
+   * reserved[1..3] must be 0 (MA_ERR_ARG). */
   int32_t reserved[4];
   int32_t muon_momentum_form;          /* ma_momentum_form; default MA_MOMENTUM_SGD */
   /* 1: AdamW parameters whose lower-cased name ends with "bias" or contains
@@ -148,7 +150,8 @@ typedef enum {
   MA_K_NS_UPDATE = 6,   /* X <- B X, iterations 1 .. ns_steps-1 */
   MA_K_ADAMW = 7,       /* fused multi-tensor AdamW */
   MA_K_NS_APPLY = 8,    /* last iteration: B X applied to the parameters (Muon step) */
-  MA_K_COUNT = 9
+  MA_K_NS_FUSED = 9,    /* small matrices (s <= 128, l <= 512): every iteration and the step in one launch */
+  MA_K_COUNT = 10
 } ma_kernel_kind;
 
 typedef struct {

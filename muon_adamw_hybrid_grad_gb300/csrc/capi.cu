@@ -105,6 +105,7 @@ struct Bucket {
   std::vector<int> params;  // param indices in slot order
   int mat0 = 0;             // first index in the MuonMat table
   uint16_t *X0 = nullptr, *X1 = nullptr, *A = nullptr, *B = nullptr;
+  bool fused = false;  // small matrices: the whole Newton-Schulz in one launch (ns_small_kernel)
 };
 
 struct ProfRec {
@@ -172,6 +173,9 @@ struct muon_adamw {
   std::vector<int> muon_params, adam_params;
   // per iteration, per kind: launches (tcgen05) or problems (SIMT)
   std::vector<std::vector<TcLaunch>> tc[3];
+  std::vector<SmallLaunch> small;      // one per fused bucket
+  std::vector<double> small_units;     // their symmetric flops per step
+  double unit_fused = 0;               // symmetric flops per step of all fused buckets
   std::vector<std::vector<NsProblem>> simt[3];
   double unit_gram = 0, unit_poly = 0, unit_update = 0;  // symmetric flops per iteration (all buckets)
   double dense_flops = 0;
@@ -246,6 +250,8 @@ ma_status check_device_flag(muon_adamw* h) {
   return MA_OK;
 }
 
+void set_epi_coefficients(NsEpiArgs& e, const muon_adamw_config& c, int it);
+
 ma_status build_plan(muon_adamw* h) {
   const muon_adamw_config& c = h->cfg;
   if (h->arena) {  // a previous attempt failed part-way
@@ -279,6 +285,8 @@ ma_status build_plan(muon_adamw* h) {
     }
     h->buckets[it->second].params.push_back(pi);
   }
+  for (Bucket& B : h->buckets)
+    B.fused = c.ns_kernel == MA_NS_TCGEN05 && !(c.reserved[0] & 8) && B.S == 128 && B.L <= kSmallMaxL;
   // --- sizes ---
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
@@ -445,10 +453,12 @@ ma_status build_plan(muon_adamw* h) {
     }
   }
   int mat_index = 0;
-  h->unit_gram = h->unit_poly = h->unit_update = h->dense_flops = 0;
+  h->unit_gram = h->unit_poly = h->unit_update = h->dense_flops = h->unit_fused = 0;
+  h->small_units.clear();
   for (size_t b = 0; b < h->buckets.size(); ++b) {
     Bucket& B = h->buckets[b];
     B.mat0 = mat_index;
+    double bucket_units = 0;
     for (size_t slot = 0; slot < B.params.size(); ++slot) {
       const Param& p = h->params[B.params[slot]];
       const size_t es = p.gdtype == MA_DT_BF16 ? 2 : 4;
@@ -486,10 +496,18 @@ ma_status build_plan(muon_adamw* h) {
       const double s = M.s, l = M.l;
       h->muon_elems += p.numel;
       h->bytes_mom += (double)p.numel * (es + 8 + 2);
-      h->unit_gram += s * (s + 1) * l;
-      h->unit_poly += s * (s + 1) * s;
-      h->unit_update += 2 * s * s * l;
+      if (B.fused) {
+        bucket_units += (double)c.ns_steps * (s * (s + 1) * l + s * (s + 1) * s + 2 * s * s * l);
+      } else {
+        h->unit_gram += s * (s + 1) * l;
+        h->unit_poly += s * (s + 1) * s;
+        h->unit_update += 2 * s * s * l;
+      }
       h->dense_flops += (double)c.ns_steps * (4 * s * s * l + 2 * s * s * s);
+    }
+    if (B.fused) {
+      h->small_units.push_back(bucket_units);
+      h->unit_fused += bucket_units;
     }
   }
   h->n_mats = mat_index;
@@ -519,6 +537,7 @@ ma_status build_plan(muon_adamw* h) {
     for (int kind = 0; kind < 3; ++kind) {
       std::vector<NsProblem> probs;
       for (Bucket& B : h->buckets) {
+        if (B.fused) continue;  // ns_small_kernel takes the whole chain
         uint16_t* Xcur = (it % 2 == 0) ? B.X0 : B.X1;
         uint16_t* Xnext = (it % 2 == 0) ? B.X1 : B.X0;
         NsProblem p{};
@@ -591,6 +610,29 @@ ma_status build_plan(muon_adamw* h) {
       }
     }
   }
+  h->small.clear();
+  for (Bucket& B : h->buckets) {
+    if (!B.fused) continue;
+    SmallLaunch sl;
+    memset(&sl, 0, sizeof sl);
+    char eb[256];
+    if (!tc_encode_small(sl, B.X0, (int)B.params.size(), B.L, eb, sizeof eb)) return fail(MA_ERR_CUDA, "%s", eb);
+    sl.mats = h->d_mats + B.mat0;
+    sl.rscale = h->d_rscale + B.mat0;
+    sl.sp = h->d_step;
+    sl.err = h->d_err;
+    sl.nmat = (int)B.params.size();
+    sl.L = B.L;
+    sl.steps = c.ns_steps;
+    for (int it = 0; it < c.ns_steps; ++it) {
+      NsEpiArgs e{};
+      set_epi_coefficients(e, c, it);
+      sl.coef[it][0] = e.a;
+      sl.coef[it][1] = e.b;
+      sl.coef[it][2] = e.c;
+    }
+    h->small.push_back(sl);
+  }
   if (c.ns_kernel == MA_NS_TCGEN05 && !h->buckets.empty()) {
     CUDA_TRY(ns_tc_prepare(&h->max_pairs));
     if (h->max_pairs < 1) h->max_pairs = 1;
@@ -661,7 +703,7 @@ ma_status valid_config(const muon_adamw_config* c) {
       for (int k = 0; k < 3; ++k)
         if (!isfinite(c->ns_schedule[i][k])) return fail(MA_ERR_ARG, "non-finite ns_schedule entry");
   }
-  if (c->reserved[0] & ~6) return fail(MA_ERR_ARG, "unknown cross-check bits in reserved[0]");
+  if (c->reserved[0] & ~14) return fail(MA_ERR_ARG, "unknown cross-check bits in reserved[0]");
   for (int i = 1; i < 4; ++i)
     if (c->reserved[i] != 0) return fail(MA_ERR_ARG, "reserved[%d] must be 0", i);
   if (!(c->adam_beta1 >= 0.0 && c->adam_beta1 < 1.0) || !(c->adam_beta2 >= 0.0 && c->adam_beta2 < 1.0))
@@ -745,6 +787,13 @@ static ma_status enqueue_newton_schulz(muon_adamw* h) {
   if (h->n_mats == 0) return MA_OK;
   timed(h, MA_K_NS_PREP, h->s0, (double)h->n_tiles * 4,
         [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, (float)c.ns_eps, h->d_rscale, h->s0); });
+  // buckets of small matrices: every iteration and the update in one launch each
+  for (size_t i = 0; i < h->small.size(); ++i) {
+    SmallLaunch& sl = h->small[i];
+    sl.stall_test = h->stall_test ? 1 : 0;
+    h->stall_test = false;  // one launch only
+    timed(h, MA_K_NS_FUSED, h->s0, h->small_units[i], [&] { launch_ns_small(sl, h->num_sms, h->s0); });
+  }
   NsEpiArgs epi;
   epi.sp = h->d_step;
   const double units[3] = {h->unit_gram, h->unit_poly, h->unit_update};
@@ -1142,7 +1191,7 @@ ma_status muon_adamw_plan_info(muon_adamw_t* h, ma_plan_info* out) {
   out->grad_elems = h->grad_elems;
   out->state_bytes = (int64_t)h->state_bytes;
   out->workspace_bytes = (int64_t)h->workspace_bytes;
-  out->ns_flops_per_step = h->cfg.ns_steps * (h->unit_gram + h->unit_poly + h->unit_update);
+  out->ns_flops_per_step = h->cfg.ns_steps * (h->unit_gram + h->unit_poly + h->unit_update) + h->unit_fused;
   out->ns_dense_flops_per_step = h->dense_flops;
   out->stream_bytes_per_step = h->bytes_norm + h->bytes_mom + h->bytes_adam;
   return ok();

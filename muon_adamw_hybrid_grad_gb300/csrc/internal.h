@@ -191,6 +191,22 @@ bool tc_encode_param_maps(CUtensorMap* maps, const MuonMat& M);
 bool ns_tc_pairable(const NsProblem& p);
 // Encode the tensor maps of `tp` and count its work units for cluster size cl (host).
 bool tc_encode_problem(TcProblem& tp, int cl, char* errbuf, size_t errlen);
+// Newton-Schulz of a bucket of small matrices (S = 128, L <= kSmallMaxL) in
+// one launch, a CTA per matrix (ns_tc.cu): every iteration and the update.
+constexpr int kSmallMaxL = 512;
+struct SmallLaunch {
+  CUtensorMap tmX;           // X of the bucket: [nmat * 128] rows x L cols, boxes of 64 x 128
+  const MuonMat* mats;       // the bucket's matrices
+  const float* rscale;       // per matrix 1 / (||update||_F + eps)
+  const StepParams* sp;      // lr and decays of the update
+  int* err;                  // device error flag
+  int32_t nmat, L, steps;
+  int32_t stall_test;        // test hook: CTA 0 loads no X (its bounded wait runs out)
+  float coef[64][3];         // (a, b, c) of each iteration
+};
+bool tc_encode_small(SmallLaunch& sl, const uint16_t* X, int nmat, int L, char* errbuf, size_t errlen);
+cudaError_t launch_ns_small(const SmallLaunch& L, int num_sms, cudaStream_t st);  // grid: min(nmat, num_sms)
+
 // Static assignment of a launch's work units to `ncl` clusters (host): each
 // unit, in the launch's order (longest first), goes to the cluster with the
 // least work so far (a unit costs its K / 64 k-steps plus a fixed 6), ties to

@@ -1002,6 +1002,321 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
   if (warp == 1) tmem_dealloc<G>(tmem_base, TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// Newton-Schulz of small matrices (canonical s <= 128 rows, padded to S = 128,
+// l <= 512 columns) in one launch: one CTA takes a whole matrix through every
+// iteration and the parameter update. X (128 x L bf16), A and B (128 x 128
+// bf16) stay in shared memory as 128-row panels of 64 columns in the 128-byte
+// swizzle layout, which serves as the K-major operand of X X^T and A A (both
+// operands: the rows coincide) and of B in B X, and as the MN-major right-hand
+// operand of B X (panels 16 KiB apart). Products accumulate in TMEM: A at
+// columns 0..127, A A at 128..255, X' = B X over columns 0..L-1 once those are
+// read. The epilogues (two warps per TMEM lane quarter) round to bf16 into the
+// panels; the last one updates the parameters from registers. The next
+// matrix's X is loaded by TMA as soon as the last B X has read X.
+// ---------------------------------------------------------------------------
+constexpr int SMALL_EPI_WARPS = 8;
+constexpr int SMALL_THREADS = 32 * (1 + SMALL_EPI_WARPS);
+constexpr int SMALL_PANEL = 128 * 64 * 2;  // 16 KiB
+
+struct SmallSmem {
+  static constexpr size_t X = 0;
+  static constexpr size_t A = X + (size_t)(kSmallMaxL / 64) * SMALL_PANEL;
+  static constexpr size_t B = A + 2 * (size_t)SMALL_PANEL;
+  static constexpr size_t BARS = B + 2 * (size_t)SMALL_PANEL;
+  static constexpr size_t BYTES = 1024 + BARS + 64;
+  static_assert(BYTES <= 232448, "shared memory per CTA");
+  static_assert((BYTES >> 4) < 0x4000, "operand descriptors: 14-bit address field");
+};
+
+// bf16 pairs of 32 consecutive columns c0.. (c0 % 32 == 0) into row r of the
+// panel layout: chunk q of the row sits at q ^ (r & 7).
+__device__ __forceinline__ void small_put_row(uint8_t* panels, int r, int c0, const uint32_t (&pk)[16]) {
+  uint8_t* const row = panels + (size_t)(c0 >> 6) * SMALL_PANEL + (size_t)r * 128;
+  const int q0 = (c0 & 63) >> 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(row + (((q0 + j) ^ (r & 7)) << 4)) =
+        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+}
+
+__device__ __forceinline__ void small_get_row(const uint8_t* panels, int r, int c0, uint4 (&v)[4]) {
+  const uint8_t* const row = panels + (size_t)(c0 >> 6) * SMALL_PANEL + (size_t)r * 128;
+  const int q0 = (c0 & 63) >> 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(row + (((q0 + j) ^ (r & 7)) << 4));
+}
+
+// Last-iteration update of one 32 x 32 block of a small matrix's parameter,
+// with the lanes along parameter rows (coalesced) and all 32 loads of p issued
+// before any store. Wide parameters (canonical row = parameter row) pass the
+// block through the warp's padded fp32 tile `t` to get there; for tall ones
+// (canonical row = parameter column) lane l already holds parameter column
+// row0 + l.
+__device__ __forceinline__ void small_apply_block(const MuonMat& M, float lrm, float dec, float rs, int row0,
+                                                  int col0, uint32_t taddr, float (*t)[33], int lane) {
+  uint32_t v[32];
+  tmem_ld_32x32b_x32(taddr, v);
+  tmem_ld_wait();
+  float o[32];
+  int gc, nr;      // this lane's parameter column; rows of the block inside the parameter
+  size_t base;     // parameter offset of the block's first row at this lane's column
+  if (!M.transposed) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) t[lane][e] = __uint_as_float(v[e]) * rs;
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 32; ++r) o[r] = t[r][lane];
+    __syncwarp();
+    gc = col0 + lane;
+    nr = M.s - row0;
+    base = (size_t)row0 * M.n + gc;
+    if (gc >= M.l) nr = 0;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * rs;
+    gc = row0 + lane;
+    nr = M.l - col0;
+    base = (size_t)col0 * M.n + gc;
+    if (gc >= M.s) nr = 0;
+  }
+  if (nr > 32) nr = 32;
+  float pv[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) pv[r] = r < nr ? M.p[base + (size_t)r * M.n] : 0.f;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    if (r < nr) {
+      const float q = fmaf(pv[r], dec, -lrm * o[r]);
+      M.p[base + (size_t)r * M.n] = q;
+      if (M.shadow) M.shadow[base + (size_t)r * M.n] = ns_f2bf(q);
+    }
+  }
+}
+
+// Every thread waits for phase `parity` of `bar`; false on the CTA when any
+// thread's bounded wait ran out (the error is recorded), so all leave together.
+__device__ __forceinline__ bool small_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, err, kErrWaitEpilogue);
+  return __syncthreads_and(ok) != 0;
+}
+
+__global__ void __launch_bounds__(SMALL_THREADS, 1) ns_small_kernel(const __grid_constant__ SmallLaunch L) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* const Xp = smem + SmallSmem::X;
+  uint8_t* const Ap = smem + SmallSmem::A;
+  uint8_t* const Bp = smem + SmallSmem::B;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmallSmem::BARS);
+  const uint32_t load_bar = smem_u32(bars), mma_bar = smem_u32(bars + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int npan = L.L / 64;
+
+  if (threadIdx.x == 0) {
+    mbar_init(load_bar, 1);
+    mbar_init(mma_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L.tmX)) : "memory");
+  }
+  if (warp == 0) tmem_alloc<1>(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t xs = smem_u32(Xp), as = smem_u32(Ap), bs = smem_u32(Bp);
+  auto load_x = [&](int mat) {  // thread 0
+    mbar_expect_tx(load_bar, (uint32_t)(npan * SMALL_PANEL));
+    for (int q = 0; q < npan; ++q) tma_load_2d(xs + q * SMALL_PANEL, &L.tmX, 64 * q, mat * 128, load_bar);
+  };
+  // epilogue geometry: TMEM lane quarter (rows) and alternate 32-column blocks
+  const int quarter = warp & 3;
+  const int half = (warp - 1) >> 2;
+  const int row = 32 * quarter + lane;  // this lane's canonical row
+  const uint32_t tq = tmem + ((uint32_t)(32 * quarter) << 16);
+
+  uint32_t load_ph = 0, mma_ph = 0;
+  bool ok = true;
+  bool pending = false;  // thread 0: an X load is in flight
+  bool mma_out = false;  // thread 0: MMAs committed and not yet waited for
+  // test hook: CTA 0 loads nothing, so its first bounded wait runs out
+  if (threadIdx.x == 0 && (int)blockIdx.x < L.nmat && !(L.stall_test && blockIdx.x == 0)) {
+    load_x(blockIdx.x);
+    pending = true;
+  }
+  for (int mat = blockIdx.x; mat < L.nmat && ok; mat += gridDim.x) {
+    const MuonMat& M = L.mats[mat];
+    const int s = M.s, l = M.l;
+    const float r = L.rscale[mat];
+    if (!(ok = small_wait(load_bar, load_ph, abort_flag, L.err))) break;
+    load_ph ^= 1u;
+    pending = false;
+    for (int it = 0; it < L.steps && ok; ++it) {
+      const bool first = it == 0, last = it == L.steps - 1;
+      const float ca = L.coef[it][0], cb = L.coef[it][1], cc = L.coef[it][2];
+      // ---- A = X X^T (columns 0..127) ----
+      if (threadIdx.x == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 128, false);
+        for (int q = 0; q < npan; ++q) {
+          const uint64_t d0 = sdesc(xs + q * SMALL_PANEL, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) umma_bf16<1>(tmem, d0 + 2u * kk, d0 + 2u * kk, id, (q | kk) != 0 ? 1u : 0u);
+        }
+        umma_commit<1>(mma_bar);
+        mma_out = true;
+      }
+      if (!(ok = small_wait(mma_bar, mma_ph, abort_flag, L.err))) break;
+      mma_ph ^= 1u;
+      mma_out = false;
+      tc_fence_after();
+      if (warp >= 1) {
+        const float sc = first ? r * r : 1.f;
+        for (int c0 = 32 * half; c0 < 128; c0 += 64) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tq + (uint32_t)c0, v);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float x0 = __uint_as_float(v[2 * j]) * sc, x1 = __uint_as_float(v[2 * j + 1]) * sc;
+            if (row >= s || c0 + 2 * j >= s) x0 = 0.f;
+            if (row >= s || c0 + 2 * j + 1 >= s) x1 = 0.f;
+            pk[j] = pack_bf16x2(x0, x1);
+          }
+          small_put_row(Ap, row, c0, pk);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      // ---- A A (columns 128..255); B = c A A + b A + a I ----
+      if (threadIdx.x == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 128, false);
+        for (int q = 0; q < 2; ++q) {
+          const uint64_t d0 = sdesc(as + q * SMALL_PANEL, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16<1>(tmem + 128u, d0 + 2u * kk, d0 + 2u * kk, id, (q | kk) != 0 ? 1u : 0u);
+        }
+        umma_commit<1>(mma_bar);
+        mma_out = true;
+      }
+      if (!(ok = small_wait(mma_bar, mma_ph, abort_flag, L.err))) break;
+      mma_ph ^= 1u;
+      mma_out = false;
+      tc_fence_after();
+      if (warp >= 1) {
+        for (int c0 = 32 * half; c0 < 128; c0 += 64) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tq + 128u + (uint32_t)c0, v);
+          uint4 a4[4];
+          small_get_row(Ap, row, c0, a4);
+          tmem_ld_wait();
+          const bool on_diag = c0 == 32 * quarter;
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t u = u4_get(a4[j >> 2], j & 3);
+            float o[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int col = 2 * j + e;
+              const float av = __uint_as_float(e ? (u & 0xFFFF0000u) : (u << 16));
+              const float lin = on_diag ? fmaf(cb, av, col == lane ? ca : 0.f) : cb * av;
+              o[e] = fmaf(cc, __uint_as_float(v[col]), lin);
+              if (row >= s || c0 + col >= s) o[e] = 0.f;
+            }
+            pk[j] = pack_bf16x2(o[0], o[1]);
+          }
+          small_put_row(Bp, row, c0, pk);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      // ---- X' = B X (columns 0..L-1) ----
+      if (threadIdx.x == 0) {
+        tc_fence_after();
+        for (int n0 = 0; n0 < L.L; n0 += 256) {
+          const int nn = L.L - n0 < 256 ? L.L - n0 : 256;
+          const uint32_t id = idesc_bf16(128, nn, true);
+          const uint64_t b0 = sdesc(xs + (n0 / 64) * SMALL_PANEL, SMALL_PANEL, 1024);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t a = sdesc(bs + (ks >> 2) * SMALL_PANEL, 16, 1024) + 2u * (ks & 3);
+            umma_bf16<1>(tmem + (uint32_t)n0, a, b0 + 128u * ks, id, ks != 0 ? 1u : 0u);
+          }
+        }
+        umma_commit<1>(mma_bar);
+        mma_out = true;
+      }
+      if (!(ok = small_wait(mma_bar, mma_ph, abort_flag, L.err))) break;
+      mma_ph ^= 1u;
+      mma_out = false;
+      tc_fence_after();
+      if (!last) {
+        if (warp >= 1) {
+          const float sc = first ? r : 1.f;
+          for (int c0 = 32 * half; c0 < L.L; c0 += 64) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tq + (uint32_t)c0, v);
+            tmem_ld_wait();
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float x0 = __uint_as_float(v[2 * j]) * sc, x1 = __uint_as_float(v[2 * j + 1]) * sc;
+              if (row >= s || c0 + 2 * j >= l) x0 = 0.f;
+              if (row >= s || c0 + 2 * j + 1 >= l) x1 = 0.f;
+              pk[j] = pack_bf16x2(x0, x1);
+            }
+            small_put_row(Xp, row, c0, pk);
+          }
+        }
+        fence_proxy_async_smem();
+      } else {
+        // X has been read for the last time: the next matrix's comes in meanwhile
+        if (threadIdx.x == 0 && mat + (int)gridDim.x < L.nmat) {
+          load_x(mat + gridDim.x);
+          pending = true;
+        }
+        if (warp >= 1) {
+          // A and B are free now: a padded 32 x 33 fp32 tile per epilogue warp
+          float(*t)[33] = reinterpret_cast<float(*)[33]>(Ap + (size_t)(warp - 1) * 32 * 33 * 4);
+          const float rs = first ? r : 1.f;
+          const float lrm = L.sp->ns_lr * M.lr_mult;
+          const float dec = L.sp->ns_decay[M.group];
+          for (int c0 = 32 * half; c0 < l; c0 += 64)
+            small_apply_block(M, lrm, dec, rs, 32 * quarter, c0, tq + (uint32_t)c0, t, lane);
+        }
+      }
+      tc_fence_before();
+      __syncthreads();
+    }
+  }
+  // A load issued for a matrix this CTA no longer reaches (after an abort)
+  // lands before the CTA leaves; the MMAs have all been waited for.
+  if (!ok && pending) {
+    const uint64_t t0 = global_timer();
+    while (!mbar_try_wait(load_bar, load_ph) && global_timer() - t0 < kWaitLimitNs) {
+    }
+  }
+  // ... and MMAs still running finish before TMEM is released
+  if (!ok && mma_out) {
+    const uint64_t t0 = global_timer();
+    while (!mbar_try_wait(mma_bar, mma_ph) && global_timer() - t0 < kWaitLimitNs) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc<1>(tmem, 512);
+}
+
 // ---- host side ----
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1188,6 +1503,9 @@ cudaError_t ns_tc_prepare(int* max_pairs) {
   if ((e = set_smem_attr<2, false, true>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<2, false, false>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<2, true, true>()) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)SmallSmem::BYTES)) != cudaSuccess)
+    return e;
   int a = 0, b = 0, c = 0;
   if ((e = max_pairs_of<false, true>(&a)) != cudaSuccess) return e;
   if ((e = max_pairs_of<false, false>(&b)) != cudaSuccess) return e;
@@ -1195,6 +1513,18 @@ cudaError_t ns_tc_prepare(int* max_pairs) {
   int m = a < b ? a : b;
   *max_pairs = m < c ? m : c;
   return cudaSuccess;
+}
+
+bool tc_encode_small(SmallLaunch& sl, const uint16_t* X, int nmat, int L, char* errbuf, size_t errlen) {
+  // X of every matrix of the bucket: [nmat * 128] rows x L cols, panels of 128 x 64
+  return encode_2d(&sl.tmX, X, (uint64_t)L, (uint64_t)nmat * 128u, 64, 128, errbuf, errlen);
+}
+
+cudaError_t launch_ns_small(const SmallLaunch& L, int num_sms, cudaStream_t st) {
+  const int grid = L.nmat < num_sms ? L.nmat : num_sms;
+  if (grid <= 0) return cudaSuccess;
+  ns_small_kernel<<<grid, SMALL_THREADS, SmallSmem::BYTES, st>>>(L);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_ns_tc(const TcLaunch& L, cudaStream_t st) {

@@ -81,6 +81,40 @@ def test_without_cta_clusters(mx):
     assert r["worst_o"] <= O_TOL
 
 
+def test_small_matrices_through_per_product_launches(mx):
+    """Cross-check switch: matrices of 128 canonical rows or fewer (here with
+    padding, both orientations and several widths) through the per-product
+    tensor-core launches instead of the fused small-matrix kernel, against
+    the oracle."""
+    r = run_parity(_ragged(), config={"reserved": [8]})
+    assert r["worst_o"] <= O_TOL
+
+
+def test_fused_small_matrix_kernel(mx):
+    """Buckets of small matrices run their whole Newton-Schulz chain and the
+    update in one launch each (two buckets here: 128 x 512 in both
+    orientations, and 64 x 200), checked against the oracle; no per-product
+    launch is made for them."""
+    shapes = [(128, 512), (512, 128), (64, 200), (200, 64), (128, 512)]
+    t = [TensorSpec(f"model.action_expert.layers.{k}.mlp.w.weight", sh) for k, sh in enumerate(shapes)]
+    t.append(TensorSpec("model.vlm.norm.weight", (300,)))
+    w = workloads.custom_workload("small_fused", t, policy="bf16_mixed", steps=3)
+    r = run_parity(w)
+    assert r["worst_o"] <= O_TOL
+    gpu = GpuSide(w, workloads.master_weights(w))
+    try:
+        gpu.load_grads(workloads.gradients(w, 1))
+        gpu.mx.muon_adamw_set_profiling(gpu.opt.handle, True)
+        gpu.step(w.lr)
+        prof = gpu.opt.profile()
+        assert prof["ns_fused"]["launches"] == 2
+        for k in ("ns_gram", "ns_poly", "ns_update", "ns_apply"):
+            assert prof[k]["launches"] == 0
+        assert prof["ns_fused"]["units"] > 0
+    finally:
+        gpu.close()
+
+
 def test_fp32_gradients(mx):
     w = workloads.get_workload("tiny")
     w = workloads.custom_workload("tiny_fp32g", w.tensors, grad_dtype="fp32", policy="fp32_mixed", steps=2)
