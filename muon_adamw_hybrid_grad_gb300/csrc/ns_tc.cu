@@ -1029,6 +1029,12 @@ struct SmallSmem {
   static_assert((BYTES >> 4) < 0x4000, "operand descriptors: 14-bit address field");
 };
 
+// Bring `bytes` (a multiple of 16, 16-byte aligned start) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 // bf16 pairs of 32 consecutive columns c0.. (c0 % 32 == 0) into row r of the
 // panel layout: chunk q of the row sits at q ^ (r & 7).
 __device__ __forceinline__ void small_put_row(uint8_t* panels, int r, int c0, const uint32_t (&pk)[16]) {
@@ -1154,6 +1160,15 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) ns_small_kernel(const __grid
     if (!(ok = small_wait(load_bar, load_ph, abort_flag, L.err))) break;
     load_ph ^= 1u;
     pending = false;
+    if (threadIdx.x == 0) {
+      // the parameters the update reads at the end, into L2 while the iterations run
+      const size_t pbytes = (size_t)M.m * M.n * 4;
+      if ((reinterpret_cast<uintptr_t>(M.p) & 15) == 0)
+        for (size_t o = 0; o + 16 <= pbytes; o += (size_t)1 << 20) {
+          const size_t n = pbytes - o < ((size_t)1 << 20) ? pbytes - o : ((size_t)1 << 20);
+          bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(M.p) + o, (uint32_t)(n & ~(size_t)15));
+        }
+    }
     for (int it = 0; it < L.steps && ok; ++it) {
       const bool first = it == 0, last = it == L.steps - 1;
       const float ca = L.coef[it][0], cb = L.coef[it][1], cc = L.coef[it][2];
@@ -1262,19 +1277,25 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) ns_small_kernel(const __grid
       if (!last) {
         if (warp >= 1) {
           const float sc = first ? r : 1.f;
-          for (int c0 = 32 * half; c0 < L.L; c0 += 64) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tq + (uint32_t)c0, v);
+          // two blocks per TMEM wait (L is a multiple of 128: blocks c0 and c0 + 64 both exist)
+          for (int c0 = 32 * half; c0 < L.L; c0 += 128) {
+            uint32_t v[2][32];
+            tmem_ld_32x32b_x32(tq + (uint32_t)c0, v[0]);
+            tmem_ld_32x32b_x32(tq + (uint32_t)(c0 + 64), v[1]);
             tmem_ld_wait();
-            uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float x0 = __uint_as_float(v[2 * j]) * sc, x1 = __uint_as_float(v[2 * j + 1]) * sc;
-              if (row >= s || c0 + 2 * j >= l) x0 = 0.f;
-              if (row >= s || c0 + 2 * j + 1 >= l) x1 = 0.f;
-              pk[j] = pack_bf16x2(x0, x1);
+            for (int h = 0; h < 2; ++h) {
+              const int cb0 = c0 + 64 * h;
+              uint32_t pk[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                float x0 = __uint_as_float(v[h][2 * j]) * sc, x1 = __uint_as_float(v[h][2 * j + 1]) * sc;
+                if (row >= s || cb0 + 2 * j >= l) x0 = 0.f;
+                if (row >= s || cb0 + 2 * j + 1 >= l) x1 = 0.f;
+                pk[j] = pack_bf16x2(x0, x1);
+              }
+              small_put_row(Xp, row, cb0, pk);
             }
-            small_put_row(Xp, row, c0, pk);
           }
         }
         fence_proxy_async_smem();
