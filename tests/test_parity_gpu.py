@@ -115,6 +115,30 @@ def test_fused_small_matrix_kernel(mx):
         gpu.close()
 
 
+def _small_workload(steps=3):
+    shapes = [(128, 512), (512, 128), (100, 384), (96, 96)]
+    t = [TensorSpec(f"model.action_expert.layers.{k}.mlp.w.weight", sh) for k, sh in enumerate(shapes)]
+    t.append(TensorSpec("model.action_expert.layers.0.mlp.w.bias", (96,)))
+    return workloads.custom_workload("small", t, policy="bf16_mixed", steps=steps)
+
+
+@pytest.mark.parametrize("steps_ns", [1, 3])
+def test_fused_small_matrix_step_counts(mx, steps_ns):
+    """The fused small-matrix kernel with one iteration (first and last at
+    once: both Frobenius scales and the update in the same launch) and
+    three, against the oracle."""
+    r = run_parity(_small_workload(2), config={"ns_steps": steps_ns}, oracle_overrides={"muon_ns_steps": steps_ns})
+    assert r["worst_o"] <= O_TOL
+
+
+def test_fused_small_matrix_ema_and_schedule(mx):
+    """Per-iteration coefficients and the exponential-average momentum through
+    the fused small-matrix kernel, against the oracle."""
+    r = run_parity(_small_workload(3), config={"muon_momentum_form": "ema", "ns_schedule": SCHEDULE},
+                   oracle_overrides={"muon_momentum_form": "ema", "ns_schedule": SCHEDULE})
+    assert r["worst_o"] <= O_TOL
+
+
 def test_fp32_gradients(mx):
     w = workloads.get_workload("tiny")
     w = workloads.custom_workload("tiny_fp32g", w.tensors, grad_dtype="fp32", policy="fp32_mixed", steps=2)
@@ -536,12 +560,14 @@ def test_grads_consumed_event_allows_overwriting_gradients(mx):
         gpu.close()
 
 
-def test_graph_mode_matches_direct_launches(mx):
+@pytest.mark.parametrize("which", ["options", "small"])
+def test_graph_mode_matches_direct_launches(mx, which):
     """Steps replayed from the captured CUDA graph (the default) and steps
     launched one kernel at a time give bitwise-identical parameters and
     shadows, with a different lr every step (the step's scalars are read from
-    HBM) and with profiling (which forces direct launches) on for one step."""
-    w = _options_workload()
+    HBM) and with profiling (which forces direct launches) on for one step;
+    for per-product launches and for the fused small-matrix kernel."""
+    w = _options_workload() if which == "options" else _small_workload()
     masters = workloads.master_weights(w)
     lrs = (w.lr, 0.5 * w.lr, 2.0 * w.lr)
     outs = []
