@@ -12,7 +12,10 @@ touched per step) exceed the 129 MB L2, so no flush is needed between steps.
 Prints one JSON line (rank 0). value = optimizer steps/s for the whole job;
 under torchrun each rank runs an independent replica (the optimizer step of
 one model does not shard here: "replicas only"), so value = N * K / (max over
-ranks of the timed region). Extra keys: per-kernel CUDA-event breakdown, the
+ranks of the timed region). The timed region runs the steps as a user does
+(the Newton-Schulz chain replayed from its CUDA graph); the per-kernel times
+come from as many steps again with the library's per-launch CUDA events on.
+Extra keys: per-kernel CUDA-event breakdown, the
 roofline of the dominant kernel (the Newton-Schulz GEMM), the SM clocks seen
 during the timed region, an end-to-end figure (gradients copied from pinned
 host memory every step, the norm read back), and the fp64 oracle timed on a
@@ -320,10 +323,9 @@ def run_ours(args):
         opt.step(lr)
     torch.cuda.synchronize()
     info = opt.plan_info()
-    # ---- timed region (device time, CUDA events on the launching stream; the
-    # library's per-launch events give each kernel's time inside it) ----
-    mx.muon_adamw_reset_profile(opt.handle)
-    mx.muon_adamw_set_profiling(opt.handle, True)
+    # ---- timed region (device time, CUDA events on the launching stream),
+    # the steps as a user runs them (the Newton-Schulz chain replayed from
+    # its CUDA graph, no per-launch events) ----
     clocks = ClockSampler(local)
     time.sleep(0.3)
     if dist is not None:
@@ -342,10 +344,17 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
-    mx.muon_adamw_set_profiling(opt.handle, False)
-    prof = opt.profile()
     max_s = max_over_ranks(ms / 1e3, dist, dev)
     value = aggregate(args.steps, world, max_s)
+    # ---- per-kernel times: as many steps again with the library's per-launch
+    # CUDA events on (direct launches; the events sit between them) ----
+    mx.muon_adamw_reset_profile(opt.handle)
+    mx.muon_adamw_set_profiling(opt.handle, True)
+    for _ in range(args.steps):
+        opt.step(lr)
+    torch.cuda.synchronize()
+    mx.muon_adamw_set_profiling(opt.handle, False)
+    prof = opt.profile()
 
     # ---- end to end: grads from pinned host memory each step, norm read back ----
     # per step: the flat gradient buffer, plus the library's own copy of the

@@ -789,6 +789,12 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
   if (CL == 2) cluster_sync();  // the peer's barriers exist before any copy or commit reaches them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched with programmatic stream serialization: the set-up above may
+  // overlap the previous launch's last CTAs; every global access below comes
+  // after that launch has completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next launch may start its own set-up as this launch's CTAs leave
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1502,17 +1508,19 @@ cudaError_t max_pairs_of(int* n) {
 template <bool APPLY, bool PAIR>
 cudaError_t launch_pair(const TcLaunch& L, int grid_units, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(2 * grid_units, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = Smem<PAIR, APPLY>::BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, ns_tc_kernel<2, APPLY, PAIR>, L);
 }
 }  // namespace
@@ -1556,11 +1564,18 @@ cudaError_t launch_ns_tc(const TcLaunch& L, cudaStream_t st) {
   const bool update = L.prob[0].p.kind == NS_UPDATE;
   const bool apply = update && L.prob[0].p.last;
   if (L.cl == 1) {
-    if (apply)
-      ns_tc_kernel<1, true, false><<<grid_units, THREADS, Smem<false, true>::BYTES, st>>>(L);
-    else
-      ns_tc_kernel<1, false, false><<<grid_units, THREADS, Smem<false, false>::BYTES, st>>>(L);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid_units, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = apply ? Smem<false, true>::BYTES : Smem<false, false>::BYTES;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return apply ? cudaLaunchKernelEx(&cfg, ns_tc_kernel<1, true, false>, L)
+                 : cudaLaunchKernelEx(&cfg, ns_tc_kernel<1, false, false>, L);
   }
   if (apply) return launch_pair<true, true>(L, grid_units, st);
   if (update) return launch_pair<false, false>(L, grid_units, st);
