@@ -4,24 +4,38 @@
 // (核心揭秘一 / Muon 的工作原理): A = X X^T, B = b A + c A A, X <- a X + B X,
 // five times, on the short side, evaluated as A = X X^T, B = a I + b A + c A A,
 // X' = B X so that the largest product's epilogue reads nothing back. Each
-// launch covers one of the three products for every Muon matrix of up to
-// four shape buckets.
+// ns_tc_kernel launch covers one of the three products for every Muon matrix
+// of up to four shape buckets; the last iteration's B X updates the
+// parameters in its epilogue instead of storing X'.
 //
-// Structure (one persistent CTA per SM, 320 threads):
-//   warp 0     TMA producer: 128x64 tiles of the left operand and bn x 64
-//              tiles of the right operand into a 4-stage shared-memory ring
-//              (128-byte swizzle), completion tracked by mbarrier tx counts;
-//   warp 1     allocates 512 TMEM columns; one lane issues
-//              tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32,
-//              M = 128, N = bn, K = 16) and commits stage releases and
+// ns_tc_kernel (one persistent CTA per SM, 320 threads):
+//   warp 0     TMA producer: 128x64 tiles of the left operand and the CTA's
+//              part of the right-hand tile into a shared-memory ring
+//              (128-byte swizzle; 6 stages of 32 KiB for CTA pairs, 4 of
+//              48 KiB otherwise, fewer for the last iteration), completion
+//              tracked by mbarrier transaction counts;
+//   warp 1     allocates 512 TMEM columns; one lane issues tcgen05.mma
+//              kind::f16 (bf16 x bf16 -> fp32), either cta_group::2 with
+//              M = 256 over a CTA pair (X X^T, A A, last iteration) or
+//              cta_group::1 with M = 128 and the right-hand tile multicast
+//              within the pair (B X), and commits stage releases and
 //              accumulator-ready signals to mbarriers;
 //   warps 2-9  epilogue: tcgen05.ld of the fp32 accumulator (a warp may only
 //              read its TMEM lane quarter, warp % 4; two warps share each
 //              quarter and take alternate 32-column blocks), the fused
-//              polynomial epilogue, vectorised bf16/fp32 stores.
+//              polynomial, bf16 staging tiles leaving through TMA stores
+//              (the last iteration: fp32 parameter blocks in and out by TMA).
 // Two accumulators (2 x 256 columns) let the epilogue of one tile overlap
 // the main loop of the next. X X^T and A A are symmetric: only output tiles
-// that touch the lower triangle are computed and the epilogue mirrors them.
+// that touch the lower triangle are computed and the epilogue mirrors them;
+// on a diagonal unit the left tile also serves as the right-hand operand.
+// Units reach clusters in a longest-first order fixed at planning time, and
+// consecutive launches overlap their set-up with the previous launch's tail
+// (programmatic dependent launch).
+//
+// ns_small_kernel takes buckets of small matrices (canonical S = 128,
+// L <= 512) through every iteration and the update in one launch, one CTA
+// per matrix with X, A and B resident in shared memory.
 //
 // Every mbarrier wait is bounded (kWaitLimitNs of wall time). On expiry the
 // CTA records an error code in the device flag, the other roles stop at
@@ -558,7 +572,7 @@ __device__ __forceinline__ void apply_block_direct(const MuonMat& M, const NsEpi
 // q ^ ((r >> 1) & 3), which keeps both the row-per-lane accesses (parameter
 // row = TMEM lane) and the column-per-lane ones (tall parameters, parameter
 // column = TMEM lane) free of bank conflicts. Matrices without maps take
-// epilogue_block.
+// apply_block_direct.
 template <int CL, bool PAIR>
 __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem, size_t pbuf_off, size_t sb_off,
                                                uint32_t pbar_base, uint32_t tmem_base, uint32_t tfull0,
