@@ -93,8 +93,10 @@ typedef enum { MA_MOMENTUM_SGD = 0, MA_MOMENTUM_EMA = 1 } ma_momentum_form;
  *   base lr); adam_beta1 0.9, adam_beta2 0.999, adam_eps 1e-8,
  *   adam_weight_decay 0.1; max_grad_norm 1.0 [训练栈默认参数速查表]
  *   (<= 0 disables clipping); clip_eps 1e-6;
- *   ns_kernel MA_NS_TCGEN05 (MA_NS_SIMT selects a slow CUDA-core GEMM used
- *   to cross-check the tensor-core kernel). */
+ *   ns_kernel MA_NS_TCGEN05: tensor-core kernels, one launch per product for
+ *   most shape buckets and one launch per bucket of small matrices (canonical
+ *   128 rows or fewer, at most 512 columns) for the whole chain and update
+ *   (MA_NS_SIMT selects a slow CUDA-core GEMM used to cross-check them). */
 typedef struct {
   int32_t mode;
   int32_t precision;
@@ -289,7 +291,7 @@ MA_API ma_status muon_adamw_plan_work_order(int nprob, const int64_t* k, const i
 
 /* Test hook for the failure path, not for production use. Arms a one-shot
  * stall: in the next step's first Newton-Schulz launch, one CTA issues no
- * operand loads, so its MMA warp's bounded wait (2 s) runs out. The kernel
+ * operand loads, so its bounded wait (2 s) runs out. The kernel
  * then records the error, drains and releases its resources and returns;
  * that step's result is invalid and the step reports MA_ERR_DEVICE_CHECK
  * when its norm is read (or on muon_adamw_sync). Nothing faults, and the
