@@ -331,19 +331,21 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
+    # one event between consecutive steps: the region is first to last event,
+    # and each step's own time gives the median and minimum
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     gc.disable()
-    ev0.record(stream)
-    for _ in range(args.steps):
+    evs[0].record(stream)
+    for k in range(args.steps):
         opt.step(lr)
-    ev1.record(stream)
+        evs[k + 1].record(stream)
     torch.cuda.synchronize()
     gc.enable()
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
+    ms = evs[0].elapsed_time(evs[-1])
+    step_ms = [evs[k].elapsed_time(evs[k + 1]) for k in range(args.steps)]
     max_s = max_over_ranks(ms / 1e3, dist, dev)
     value = aggregate(args.steps, world, max_s)
     # ---- per-kernel times: as many steps again with the library's per-launch
@@ -427,6 +429,8 @@ def run_ours(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(max_s * 1e3 / args.steps, 4),
+        "step_ms_median": round(statistics.median(step_ms), 4) if step_ms else None,
+        "step_ms_min": round(min(step_ms), 4) if step_ms else None,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
