@@ -579,12 +579,16 @@ ma_status build_plan(muon_adamw* h) {
       }
       h->simt[kind][it] = probs;
       if (c.ns_kernel == MA_NS_TCGEN05) {
-        // problems whose row blocks pair up run in CTA pairs (operand multicast); the rest singly
+        // X X^T, A A and the last iteration run in CTA pairs (one M = 256 MMA
+        // over both CTAs) where their row blocks pair up; X' = B X of the other
+        // iterations and unpaired problems run in single CTAs
         const bool allow_pairs = !(c.reserved[0] & 2);
         for (int cl = 2; cl >= 1; --cl) {
           std::vector<NsProblem> group;
-          for (const NsProblem& pp : probs)
-            if ((cl == 2) == (allow_pairs && ns_tc_pairable(pp))) group.push_back(pp);
+          for (const NsProblem& pp : probs) {
+            const bool paired = allow_pairs && ns_tc_pairable(pp);
+            if ((cl == 2) == paired) group.push_back(pp);
+          }
           // longest work units first: the static round-robin then ends on short units
           std::stable_sort(group.begin(), group.end(),
                            [](const NsProblem& a, const NsProblem& b) { return a.K > b.K; });

@@ -180,7 +180,7 @@ struct TcLaunch {
   const int32_t* order;
   int32_t npos;
   int32_t nclusters;    // clusters in the grid
-  int32_t cl;           // CTAs per cluster: 1, or 2 (operand multicast between a CTA pair)
+  int32_t cl;           // CTAs per cluster: 1, or 2 (a CTA pair running cta_group::2 MMAs)
   int32_t stall_test;   // test hook: CTA 0's producer issues no loads (its waits then run out)
 };
 // TMA maps of one parameter for the last iteration's write-back: maps[0] the

@@ -17,9 +17,10 @@
 //   warp 1     allocates 512 TMEM columns; one lane issues tcgen05.mma
 //              kind::f16 (bf16 x bf16 -> fp32), either cta_group::2 with
 //              M = 256 over a CTA pair (X X^T, A A, last iteration) or
-//              cta_group::1 with M = 128 and the right-hand tile multicast
-//              within the pair (B X), and commits stage releases and
-//              accumulator-ready signals to mbarriers;
+//              cta_group::1 with M = 128 in a CTA of its own (B X), and
+//              commits stage releases and accumulator-ready signals to
+//              mbarriers; every operand copy is a plain TMA load into the
+//              shared memory of the CTA that reads it;
 //   warps 2-9  epilogue: tcgen05.ld of the fp32 accumulator (a warp may only
 //              read its TMEM lane quarter, warp % 4; two warps share each
 //              quarter and take alternate 32-column blocks), the fused
@@ -235,23 +236,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// The same, on the mbarrier at the same shared-memory offset in every CTA of
-// `cta_mask` (MMAs of this CTA alone).
-__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(cta_mask)
-               : "memory");
-}
-
-// The same for the MMAs of a CTA pair, on both CTAs' mbarriers.
-__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"((uint16_t)3)
-      : "memory");
-}
-
 template <int CL>
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
   if constexpr (CL == 1) {
@@ -281,20 +265,18 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
+// The MMAs of a CTA pair (issued by the even CTA) have completed: one
+// arrival on the mbarrier at offset `bar` in each CTA of the pair, as two
+// commits (the executing CTA's own barrier, then the odd CTA's, addressed
+// through the cluster window).
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  umma_commit<2>(bar);
+  umma_commit<2>(mapa_shared(bar, 1));
+}
+
 // Arrive on an mbarrier of any CTA of the cluster (release at cluster scope).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// TMA load of one box into the same shared-memory offset of every CTA in
-// `cta_mask`, completing on the mbarrier at the same offset in each.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-      : "memory");
 }
 
 // TMA load into this CTA's shared memory whose completion is counted on an
@@ -734,26 +716,23 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
   __syncwarp();
 }
 
-// CL = 1: one CTA per work unit. CL = 2: a cluster of two CTAs (a CTA pair)
-// per unit of two adjacent 128-row blocks that share the right-hand operand
-// tile, in one of two ways:
-//   PAIR: the pair runs tcgen05.mma.cta_group::2 with M = 256. The even CTA
-//     (leader) issues every MMA, which reads each CTA's own 128 rows of the
-//     left operand and each CTA's half of the right-hand tile from that CTA's
-//     shared memory and accumulates into each CTA's own TMEM. Both CTAs load
-//     their parts by TMA; the odd CTA's copies complete on the leader's full
-//     barrier, whose expected byte count covers both. The leader's commits
-//     release each stage and each accumulator in both CTAs; both CTAs'
-//     epilogue warps release the accumulator on the leader's barrier. Used
-//     where the right-hand operand is K-major (X X^T, A A) and for the last
-//     iteration.
-//   otherwise: each CTA runs its own M = 128 MMAs; each loads half of the
-//     shared right-hand tile and multicasts it into both CTAs, and a stage is
-//     free once both CTAs' MMAs have read it. Used for X' = B X, whose
-//     MN-major right-hand operand ran slower through the paired MMA.
+// CL = 1: one CTA per work unit, running its own M = 128 MMAs (X' = B X of
+// iterations 1 .. n-1, and every product when pairs are switched off).
+// CL = 2 (PAIR): a cluster of two CTAs per unit of two adjacent 128-row
+// blocks that share the right-hand operand tile, running
+// tcgen05.mma.cta_group::2 with M = 256. The even CTA (leader) issues every
+// MMA, which reads each CTA's own 128 rows of the left operand and each CTA's
+// half of the right-hand tile from that CTA's shared memory and accumulates
+// into each CTA's own TMEM. Both CTAs load their parts by TMA; the odd CTA's
+// copies complete on the leader's full barrier, whose expected byte count
+// covers both. The leader's commits release each stage and each accumulator
+// in both CTAs; both CTAs' epilogue warps release the accumulator on the
+// leader's barrier. Used where the right-hand operand is K-major (X X^T, A A)
+// and for the last iteration. No operand tile is ever multicast: each CTA
+// loads exactly the bytes its own shared memory holds.
 template <int CL, bool APPLY, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant__ TcLaunch L) {
-  static_assert(!PAIR || CL == 2, "a paired MMA needs a CTA pair");
+  static_assert(PAIR == (CL == 2), "a cluster of two CTAs runs the paired MMA");
   constexpr int G = PAIR ? 2 : 1;  // tcgen05 cta_group
   using SM = Smem<PAIR, APPLY>;
   static_assert((SM::BYTES >> 4) < 0x4000, "operand descriptors: 14-bit address field");
@@ -778,13 +757,12 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
   const bool issues_mma = !PAIR || leader;
   const int unit0 = blockIdx.x / CL;  // this cluster's first position in the work order
   const int nunits = gridDim.x / CL;  // clusters in the grid
-  const uint16_t mc_mask = (uint16_t)((1u << CL) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);  // one producer arrival + the bytes of every copy
-      // one commit from each CTA whose MMAs read the stage
-      mbar_init(empty0 + 8 * s, PAIR ? 1 : CL);
+      // one commit from the CTA that issues the MMAs (both CTAs' parts, PAIR)
+      mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -834,16 +812,14 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
         const int rowP = c.mat * P.p.M + (c.ti * CL + (int)crank) * BM;
         const bool sym = P.p.kind != NS_UPDATE;
         // this CTA's part of the right-hand tile: columns [n0, n0 + bn / CL) of the
-        // column block, in boxes of 128 rows (K-major) or 64 columns (MN-major);
-        // PAIR keeps it here, otherwise it is multicast into both CTAs at its
-        // offset in the tile
+        // column block (the whole block for CL = 1, half of it for a pair), in
+        // boxes of 128 rows (K-major) or 64 columns (MN-major)
         const int nown = P.bn / CL;
         const int n0 = c.tj * P.bn + (int)crank * nown;
         const int nbox = sym ? nown / BM : nown / 64;
-        const uint32_t own_off = PAIR ? 0u : (uint32_t)crank * (uint32_t)nown * BK * 2u;
         const bool same = rhs_is_lhs(P, c, CL, crank);
-        // bytes landing in this CTA per stage: its left rows + its (PAIR) or the whole right tile
-        const uint32_t tx = (uint32_t)(A_STAGE + (same ? 0 : (PAIR ? nown : P.bn) * BK * 2));
+        // bytes landing in this CTA per stage: its left rows + its part of the right tile
+        const uint32_t tx = (uint32_t)(A_STAGE + (same ? 0 : nown * BK * 2));
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, L.err, kErrWaitProducer)) {
             ok = false;
@@ -860,13 +836,11 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
           }
           for (int q = 0; q < (same ? 0 : nbox); ++q) {
             // sym: rows (column block) of the same matrix, K-major; update: X, MN-major
-            const uint32_t dst = sb + own_off + q * (sym ? BM * BK * 2 : 64 * BK * 2);
+            const uint32_t dst = sb + q * (sym ? BM * BK * 2 : 64 * BK * 2);
             const int x = sym ? kb * BK : n0 + q * 64;
             const int y = sym ? c.mat * P.p.N + n0 + q * BM : c.mat * P.p.K + kb * BK;
             if (PAIR && !leader)
               tma_load_2d_pair(dst, &P.tmQ, x, y, mapa_shared(fb, 0));
-            else if (CL == 2 && !PAIR)
-              tma_load_2d_multicast(dst, &P.tmQ, x, y, fb, mc_mask);
             else
               tma_load_2d(dst, &P.tmQ, x, y, fb);
           }
@@ -948,8 +922,6 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
             umma_bf16<G>(d_tmem, ad + 2u * kk, bd + b_kstep * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
           if (PAIR)
             umma_commit_pair(empty0 + 8 * stage);  // both CTAs' parts of this stage are free
-          else if (CL == 2)
-            umma_commit_multicast(empty0 + 8 * stage, mc_mask);  // this CTA no longer reads either copy
           else
             umma_commit<1>(empty0 + 8 * stage);
           if (++stage == STAGES) {
@@ -1544,17 +1516,14 @@ cudaError_t ns_tc_prepare(int* max_pairs) {
   if ((e = set_smem_attr<1, false, false>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<1, true, false>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<2, false, true>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<2, false, false>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<2, true, true>()) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)SmallSmem::BYTES)) != cudaSuccess)
     return e;
-  int a = 0, b = 0, c = 0;
+  int a = 0, c = 0;
   if ((e = max_pairs_of<false, true>(&a)) != cudaSuccess) return e;
-  if ((e = max_pairs_of<false, false>(&b)) != cudaSuccess) return e;
   if ((e = max_pairs_of<true, true>(&c)) != cudaSuccess) return e;
-  int m = a < b ? a : b;
-  *max_pairs = m < c ? m : c;
+  *max_pairs = a < c ? a : c;
   return cudaSuccess;
 }
 
@@ -1592,7 +1561,6 @@ cudaError_t launch_ns_tc(const TcLaunch& L, cudaStream_t st) {
                  : cudaLaunchKernelEx(&cfg, ns_tc_kernel<1, false, false>, L);
   }
   if (apply) return launch_pair<true, true>(L, grid_units, st);
-  if (update) return launch_pair<false, false>(L, grid_units, st);
   return launch_pair<false, true>(L, grid_units, st);
 }
 
