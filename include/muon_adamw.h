@@ -96,7 +96,12 @@ typedef enum { MA_MOMENTUM_SGD = 0, MA_MOMENTUM_EMA = 1 } ma_momentum_form;
  *   ns_kernel MA_NS_TCGEN05: tensor-core kernels, one launch per product for
  *   most shape buckets and one launch per bucket of small matrices (canonical
  *   128 rows or fewer, at most 512 columns) for the whole chain and update
- *   (MA_NS_SIMT selects a slow CUDA-core GEMM used to cross-check them). */
+ *   (MA_NS_SIMT selects a slow CUDA-core GEMM used to cross-check them).
+ *   With either setting, matrices whose short side is below 64 run
+ *   Newton-Schulz in fp32 on the CUDA cores: with bf16 storage, updates of
+ *   such matrices whose singular values are all alike (noise-like gradients)
+ *   would come out up to 2.7e-2 (relative Frobenius) from the exact
+ *   iteration, above the 2e-2 that bf16 Newton-Schulz keeps elsewhere. */
 typedef struct {
   int32_t mode;
   int32_t precision;
@@ -153,7 +158,8 @@ typedef enum {
   MA_K_ADAMW = 7,       /* fused multi-tensor AdamW */
   MA_K_NS_APPLY = 8,    /* last iteration: B X applied to the parameters (Muon step) */
   MA_K_NS_FUSED = 9,    /* small matrices (s <= 128, l <= 512): every iteration and the step in one launch */
-  MA_K_COUNT = 10
+  MA_K_NS_NARROW = 10,  /* narrow matrices (s < 64): fp32 Newton-Schulz and the step on the CUDA cores */
+  MA_K_COUNT = 11
 } ma_kernel_kind;
 
 typedef struct {

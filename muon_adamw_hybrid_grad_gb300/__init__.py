@@ -50,7 +50,7 @@ MA_NS_SCHEDULE_MAX = 16
 MA_MAX_OPTION_GROUPS = 8
 
 KERNEL_KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "adamw", "ns_apply",
-                "ns_fused")
+                "ns_fused", "ns_narrow")
 MA_K_COUNT = len(KERNEL_KINDS)
 GROUP_NAMES = {MA_GROUP_MUON: "muon", MA_GROUP_ADAMW: "adamw", MA_GROUP_FROZEN: "frozen"}
 

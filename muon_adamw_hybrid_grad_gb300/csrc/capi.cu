@@ -105,7 +105,9 @@ struct Bucket {
   std::vector<int> params;  // param indices in slot order
   int mat0 = 0;             // first index in the MuonMat table
   uint16_t *X0 = nullptr, *X1 = nullptr, *A = nullptr, *B = nullptr;
-  bool fused = false;  // small matrices: the whole Newton-Schulz in one launch (ns_small_kernel)
+  bool fused = false;   // small matrices: the whole Newton-Schulz in one launch (ns_small_kernel)
+  bool narrow = false;  // short side < kNarrowMinS: fp32 Newton-Schulz (ns_narrow_kernel)
+  float* XF = nullptr;  // narrow: fp32 X of each slot (S x L floats per slot)
 };
 
 struct ProfRec {
@@ -176,6 +178,9 @@ struct muon_adamw {
   std::vector<SmallLaunch> small;      // one per fused bucket
   std::vector<double> small_units;     // their symmetric flops per step
   double unit_fused = 0;               // symmetric flops per step of all fused buckets
+  std::vector<NarrowLaunch> narrow;    // one per narrow bucket
+  std::vector<double> narrow_units;    // their symmetric flops per step
+  double unit_narrow = 0;              // symmetric flops per step of all narrow buckets
   std::vector<std::vector<NsProblem>> simt[3];
   double unit_gram = 0, unit_poly = 0, unit_update = 0;  // symmetric flops per iteration (all buckets)
   double dense_flops = 0;
@@ -266,27 +271,30 @@ ma_status build_plan(muon_adamw* h) {
     if (p.group == MA_GROUP_MUON && p.numel > 0) h->muon_params.push_back(i);
     if (p.group == MA_GROUP_ADAMW && p.numel > 0) h->adam_params.push_back(i);
   }
-  // --- buckets (by padded canonical shape, first-seen order) ---
-  std::map<std::pair<int, int>, int> bidx;
+  // --- buckets (by padded canonical shape and narrowness, first-seen order) ---
+  std::map<std::pair<std::pair<int, int>, bool>, int> bidx;
   h->buckets.clear();
   for (int pi : h->muon_params) {
     const Param& p = h->params[pi];
     const int64_t m = p.shape[0], n = p.shape[1];
     const int S = (int)pad_up(std::min(m, n), kPad), L = (int)pad_up(std::max(m, n), kPad);
-    auto key = std::make_pair(S, L);
+    const bool narrow = std::min(m, n) < kNarrowMinS;
+    auto key = std::make_pair(std::make_pair(S, L), narrow);
     auto it = bidx.find(key);
     if (it == bidx.end()) {
       bidx[key] = (int)h->buckets.size();
       Bucket b;
       b.S = S;
       b.L = L;
+      b.narrow = narrow;
       h->buckets.push_back(b);
       it = bidx.find(key);
     }
     h->buckets[it->second].params.push_back(pi);
   }
   for (Bucket& B : h->buckets)
-    B.fused = c.ns_kernel == MA_NS_TCGEN05 && !(c.reserved[0] & 8) && B.S == 128 && B.L <= kSmallMaxL;
+    B.fused = c.ns_kernel == MA_NS_TCGEN05 && !(c.reserved[0] & 8) && !B.narrow && B.S == 128 &&
+              B.L <= kSmallMaxL;
   // --- sizes ---
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
@@ -302,15 +310,19 @@ ma_status build_plan(muon_adamw* h) {
     off += al(h->params[pi].numel * sizeof(float));
   }
   h->state_bytes = off;
-  // per bucket: X ping, X pong (s x l), A, B (s x s), all bf16
+  // per bucket: X ping, X pong (s x l), A, B (s x s), all bf16; a narrow
+  // bucket: X (bf16, written by the momentum pass and not read) and its fp32
+  // X in place of the other three
   std::vector<size_t> ws_off(h->buckets.size() * 4);
   for (size_t b = 0; b < h->buckets.size(); ++b) {
     const Bucket& B = h->buckets[b];
     const size_t nb = B.params.size();
     const size_t xs = al(nb * (size_t)B.S * B.L * 2), as = al(nb * (size_t)B.S * B.S * 2);
+    const size_t sizes[4] = {xs, B.narrow ? al(nb * (size_t)B.S * B.L * 4) : xs, B.narrow ? 0 : as,
+                             B.narrow ? 0 : as};
     for (int q = 0; q < 4; ++q) {
       ws_off[4 * b + q] = off;
-      off += q < 2 ? xs : as;
+      off += sizes[q];
     }
   }
   h->workspace_bytes = off - h->state_bytes;
@@ -367,9 +379,15 @@ ma_status build_plan(muon_adamw* h) {
   for (size_t b = 0; b < h->buckets.size(); ++b) {
     Bucket& B = h->buckets[b];
     B.X0 = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 0]);
-    B.X1 = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 1]);
-    B.A = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 2]);
-    B.B = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 3]);
+    if (B.narrow) {
+      B.XF = reinterpret_cast<float*>(base + ws_off[4 * b + 1]);
+      B.X1 = B.A = B.B = nullptr;
+    } else {
+      B.XF = nullptr;
+      B.X1 = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 1]);
+      B.A = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 2]);
+      B.B = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 3]);
+    }
   }
   h->d_norm_chunks = reinterpret_cast<GradChunk*>(base + off_norm_chunks);
   h->n_norm_chunks = (int)n_norm;
@@ -453,8 +471,9 @@ ma_status build_plan(muon_adamw* h) {
     }
   }
   int mat_index = 0;
-  h->unit_gram = h->unit_poly = h->unit_update = h->dense_flops = h->unit_fused = 0;
+  h->unit_gram = h->unit_poly = h->unit_update = h->dense_flops = h->unit_fused = h->unit_narrow = 0;
   h->small_units.clear();
+  h->narrow_units.clear();
   for (size_t b = 0; b < h->buckets.size(); ++b) {
     Bucket& B = h->buckets[b];
     B.mat0 = mat_index;
@@ -481,6 +500,7 @@ ma_status build_plan(muon_adamw* h) {
                (reinterpret_cast<uintptr_t>(p.shadow) % 16 == 0);
       M.lr_mult = (float)(p.lr_scale * c.muon_lr_scale * c.moonlight_coef * sqrt((double)M.l));
       M.group = p.og;
+      M.xf = B.narrow ? B.XF + slot * (size_t)B.S * B.L : nullptr;
       pmaps.resize(2 * (size_t)(mat_index + 1));
       M.tma = (c.ns_kernel == MA_NS_TCGEN05 && !(c.reserved[0] & 4) &&
                tc_encode_param_maps(&pmaps[2 * (size_t)mat_index], M))
@@ -496,7 +516,7 @@ ma_status build_plan(muon_adamw* h) {
       const double s = M.s, l = M.l;
       h->muon_elems += p.numel;
       h->bytes_mom += (double)p.numel * (es + 8 + 2);
-      if (B.fused) {
+      if (B.fused || B.narrow) {
         bucket_units += (double)c.ns_steps * (s * (s + 1) * l + s * (s + 1) * s + 2 * s * s * l);
       } else {
         h->unit_gram += s * (s + 1) * l;
@@ -508,6 +528,9 @@ ma_status build_plan(muon_adamw* h) {
     if (B.fused) {
       h->small_units.push_back(bucket_units);
       h->unit_fused += bucket_units;
+    } else if (B.narrow) {
+      h->narrow_units.push_back(bucket_units);
+      h->unit_narrow += bucket_units;
     }
   }
   h->n_mats = mat_index;
@@ -537,7 +560,7 @@ ma_status build_plan(muon_adamw* h) {
     for (int kind = 0; kind < 3; ++kind) {
       std::vector<NsProblem> probs;
       for (Bucket& B : h->buckets) {
-        if (B.fused) continue;  // ns_small_kernel takes the whole chain
+        if (B.fused || B.narrow) continue;  // ns_small_kernel or ns_narrow_kernel takes the whole chain
         uint16_t* Xcur = (it % 2 == 0) ? B.X0 : B.X1;
         uint16_t* Xnext = (it % 2 == 0) ? B.X1 : B.X0;
         NsProblem p{};
@@ -613,6 +636,29 @@ ma_status build_plan(muon_adamw* h) {
         }
       }
     }
+  }
+  h->narrow.clear();
+  for (Bucket& B : h->buckets) {
+    if (!B.narrow) continue;
+    NarrowLaunch nl;
+    memset(&nl, 0, sizeof nl);
+    nl.mats = h->d_mats + B.mat0;
+    nl.sc = h->d_scalars;
+    nl.sp = h->d_step;
+    nl.nmat = (int)B.params.size();
+    nl.steps = c.ns_steps;
+    nl.nesterov = c.muon_nesterov;
+    nl.mu = (float)c.muon_momentum;
+    nl.gscale = c.muon_momentum_form == MA_MOMENTUM_EMA ? (float)(1.0 - c.muon_momentum) : 1.0f;
+    nl.eps = (float)c.ns_eps;
+    for (int it = 0; it < c.ns_steps; ++it) {
+      NsEpiArgs e{};
+      set_epi_coefficients(e, c, it);
+      nl.coef[it][0] = e.a;
+      nl.coef[it][1] = e.b;
+      nl.coef[it][2] = e.c;
+    }
+    h->narrow.push_back(nl);
   }
   h->small.clear();
   for (Bucket& B : h->buckets) {
@@ -791,6 +837,9 @@ static ma_status enqueue_newton_schulz(muon_adamw* h) {
   if (h->n_mats == 0) return MA_OK;
   timed(h, MA_K_NS_PREP, h->s0, (double)h->n_tiles * 4,
         [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, (float)c.ns_eps, h->d_rscale, h->s0); });
+  // narrow matrices: fp32 Newton-Schulz on the CUDA cores, one launch per bucket
+  for (size_t i = 0; i < h->narrow.size(); ++i)
+    timed(h, MA_K_NS_NARROW, h->s0, h->narrow_units[i], [&] { launch_ns_narrow(h->narrow[i], h->num_sms, h->s0); });
   // buckets of small matrices: every iteration and the update in one launch each
   for (size_t i = 0; i < h->small.size(); ++i) {
     SmallLaunch& sl = h->small[i];
@@ -1195,7 +1244,8 @@ ma_status muon_adamw_plan_info(muon_adamw_t* h, ma_plan_info* out) {
   out->grad_elems = h->grad_elems;
   out->state_bytes = (int64_t)h->state_bytes;
   out->workspace_bytes = (int64_t)h->workspace_bytes;
-  out->ns_flops_per_step = h->cfg.ns_steps * (h->unit_gram + h->unit_poly + h->unit_update) + h->unit_fused;
+  out->ns_flops_per_step =
+      h->cfg.ns_steps * (h->unit_gram + h->unit_poly + h->unit_update) + h->unit_fused + h->unit_narrow;
   out->ns_dense_flops_per_step = h->dense_flops;
   out->stream_bytes_per_step = h->bytes_norm + h->bytes_mom + h->bytes_adam;
   return ok();

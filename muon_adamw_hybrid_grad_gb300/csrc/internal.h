@@ -22,6 +22,9 @@ constexpr int kMomWideCols = 256;
 constexpr int kMomPartialsPerTile = 8;
 // Padding granule of the canonical Newton-Schulz workspaces (rows and cols).
 constexpr int kPad = 128;
+// Muon matrices whose short side is below this run Newton-Schulz in fp32 on
+// the CUDA cores (ns_narrow.cu) instead of through the bf16 tensor-core path.
+constexpr int kNarrowMinS = 64;
 
 enum GradDtype : int32_t { DT_F32 = 0, DT_BF16 = 1 };
 
@@ -63,6 +66,7 @@ struct MuonMat {        // one Muon matrix (device-visible metadata)
   float lr_mult;        // muon_lr_scale * moonlight * sqrt(max(m, n))
   int32_t tma;          // 1 if p (and shadow) have TMA maps: the last iteration moves them by TMA
   int32_t group;        // option group: index into NsEpiArgs::decay
+  float* xf;            // narrow matrices (s < kNarrowMinS): fp32 X in the parameter's layout; else nullptr
 };
 
 struct MomTile {
@@ -206,6 +210,22 @@ struct SmallLaunch {
 };
 bool tc_encode_small(SmallLaunch& sl, const uint16_t* X, int nmat, int L, char* errbuf, size_t errlen);
 cudaError_t launch_ns_small(const SmallLaunch& L, int num_sms, cudaStream_t st);  // grid: min(nmat, num_sms)
+
+// Newton-Schulz of narrow matrices (short side < kNarrowMinS) in fp32 on the
+// CUDA cores (ns_narrow.cu): one CTA per matrix recomputes the update from the
+// momentum buffer and the gradient, runs every iteration and the parameter
+// update. `mats` are the matrices of one narrow bucket, each with its xf.
+struct NarrowLaunch {
+  const MuonMat* mats;
+  const StepScalars* sc;     // clip coefficient
+  const StepParams* sp;      // lr and decays of the update
+  int32_t nmat, steps;
+  int32_t nesterov;
+  float mu, gscale;          // momentum coefficient, weight of the clipped gradient
+  float eps;                 // of the Frobenius normalisation
+  float coef[64][3];         // (a, b, c) of each iteration
+};
+cudaError_t launch_ns_narrow(const NarrowLaunch& L, int num_sms, cudaStream_t st);  // grid: min(nmat, 4 SMs)
 
 // Static assignment of a launch's work units to `ncl` clusters (host): each
 // unit, in the launch's order (longest first), goes to the cluster with the
