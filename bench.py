@@ -4,25 +4,30 @@
 
 One "step" is one full optimizer step of the workload (global grad norm and
 clip, Muon momentum, five Newton-Schulz iterations and update, AdamW) with
-all inputs resident in HBM. Default workload: h1024 (action expert, hidden
-1024, MLP 4096, 16 layers: 112 Muon matrices, 268 M elements; 82,944 AdamW
-elements; bf16 gradients, fp32 masters, bf16 shadow). Its inputs (~2.6 GB
-touched per step) exceed the 129 MB L2, so no flush is needed between steps.
+all inputs resident in HBM. Default workload: full_vla, the largest
+single-GPU configuration: the 2048-hidden, 24-layer action expert (168 Muon
+matrices, 1.61 G elements) plus a 1.69 G-element AdamW backbone and a frozen
+151936 x 2048 embedding, fp32 masters and moments, bf16 gradients, lr from
+cosine_with_min_lr at step 1000 of 2000. Each step touches ~83 GB, far above
+the 129 MB L2, so no flush is needed between steps. Other workloads:
+--workload tiny | h1024 | h2048 | h2048_fp32grad | many_small.
 
 Prints one JSON line (rank 0). value = optimizer steps/s for the whole job;
-under torchrun each rank runs an independent replica (the optimizer step of
-one model does not shard here: "replicas only"), so value = N * K / (max over
-ranks of the timed region). The timed region runs the steps as a user does
-(the Newton-Schulz chain replayed from its CUDA graph); the per-kernel times
-come from as many steps again with the library's per-launch CUDA events on.
-Extra keys: per-kernel CUDA-event breakdown, the
-roofline of the dominant kernel (the Newton-Schulz GEMM), the SM clocks seen
+under torchrun each rank runs an independent replica ("replicas only"), so
+value = N * K / (max over ranks of the timed region); --gpus must equal the
+number of ranks. The timed region runs the steps as a user does (the
+Newton-Schulz chain replayed from its CUDA graph); the per-kernel times come
+from as many steps again with the library's per-launch CUDA events on.
+Extra keys: per-kernel CUDA-event breakdown, the roofline of the dominant
+kernel (the Newton-Schulz GEMM), the step roofline (the step's ideal time
+from its flops and bytes against the measured step), the SM clocks seen
 during the timed region, an end-to-end figure (gradients copied from pinned
 host memory every step, the norm read back), and the fp64 oracle timed on a
 bounded sample on the host cores (cpu_baseline).
 
 --impl reference times the fp64 CPU oracle (the only reference that exists:
-the source pages ship no code) on a bounded sample of the same workload.
+the source pages ship no code) on the same bounded sample: each timed step
+runs the sample once; the line's value is the estimated rate of whole steps.
 """
 from __future__ import annotations
 
@@ -41,7 +46,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "optimizer steps/s; NS5 TFLOP/s vs bf16 peak; AdamW HBM GB/s vs peak"
-KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "ns_apply", "ns_fused", "adamw")
+KINDS = ("grad_norm", "clip", "momentum", "ns_prep", "ns_gram", "ns_poly", "ns_update", "ns_apply", "ns_fused",
+         "ns_narrow", "adamw")
 NS_KINDS = ("ns_gram", "ns_poly", "ns_update", "ns_apply", "ns_fused")
 STREAM_KINDS = ("grad_norm", "momentum", "adamw")
 
@@ -136,7 +142,7 @@ class ClockSampler:
         self.lines = []
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
                  "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -169,65 +175,90 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle on a bounded sample
+# CPU oracle on a bounded sample (both the cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_seconds(w, layers_sampled: int = 1):
-    """Time the fp64 oracle on a bounded sample of workload `w` and scale it
-    to one full step. Returns (seconds per full step, description)."""
-    import numpy as np
+# Workloads at most this large are timed as whole oracle steps; larger ones on a sample.
+WHOLE_STEP_MAX_DENSE_FLOPS = 8e12
+WHOLE_STEP_MAX_ADAMW_ELEMS = 16_000_000
+SAMPLE_ADAMW_ELEMS = 1_000_000
 
-    import oracle
-    import workloads
 
-    names = [t.name for t in w.tensors]
-    groups = [oracle.route(n, len(t.shape), frozen=t.frozen) for n, t in zip(names, w.tensors)]
-    muon = [i for i, g in enumerate(groups) if g == "muon"]
-    adam = [i for i, g in enumerate(groups) if g == "adamw"]
-    # sample: the Muon matrices of the first `layers_sampled` layers (all shapes),
-    # and AdamW tensors up to 1 M elements
-    layer_of = lambda n: n.split(".layers.")[1].split(".")[0] if ".layers." in n else None  # noqa: E731
-    first_layers = []
-    for i in muon:
-        lid = layer_of(names[i])
-        if lid not in first_layers:
-            first_layers.append(lid)
-    keep_layers = set(first_layers[:layers_sampled])
-    ms = [i for i in muon if layer_of(names[i]) in keep_layers]
-    ad, tot = [], 0
-    for i in adam:
-        if tot >= 1_000_000:
-            break
-        ad.append(i)
-        tot += w.tensors[i].numel
-    idx = ms + ad
-    sub = type(w)(w.name + "_sample", tuple(w.tensors[i] for i in idx), w.policy, w.grad_dtype, 1, w.lr)
-    masters = [workloads.master_weight(w, i).astype(np.float64) for i in idx]
-    grads = [workloads.gradient(w, i, 1) for i in idx]
-    orc = oracle.HybridOracle([names[i] for i in idx], [w.tensors[i].shape for i in idx])
-    t0 = time.perf_counter()
-    orc.step(masters, grads, w.lr)
-    dt = time.perf_counter() - t0
+def _dense_ns_flops(shape, steps: int = 5) -> float:
+    s, l = min(shape), max(shape)
+    return steps * (4.0 * s * s * l + 2.0 * s * s * s)
 
-    def ns_flops(shape):
-        s, l = min(shape), max(shape)
-        return 5 * (4 * s * s * l + 2 * s * s * s)
 
-    f_all = sum(ns_flops(w.tensors[i].shape) for i in muon)
-    f_smp = sum(ns_flops(w.tensors[i].shape) for i in ms) or 1
-    e_all = sum(w.tensors[i].numel for i in adam)
-    e_smp = sum(w.tensors[i].numel for i in ad) or 1
-    # split the sample time by a separate timing of its AdamW part
-    t1 = time.perf_counter()
-    orc2 = oracle.HybridOracle([names[i] for i in ad], [w.tensors[i].shape for i in ad])
-    orc2.step([masters[len(ms) + k].copy() for k in range(len(ad))], grads[len(ms):], w.lr)
-    dt_ad = time.perf_counter() - t1
-    dt_ms = max(dt - dt_ad, 0.0)
-    full = dt_ms * (f_all / f_smp) + (dt_ad * (e_all / e_smp) if ad else 0.0)
-    desc = (f"fp64 numpy oracle, one step over the Muon matrices of {len(keep_layers)} of "
-            f"{len(first_layers)} layers ({len(ms)} matrices) and {len(ad)} AdamW tensors "
-            f"({e_smp} elements), {dt:.2f} s; scaled to the full step by NS flops and AdamW elements")
-    return full, desc, dt
+class OracleSample:
+    """A bounded sample of workload ``w`` for the fp64 oracle, and its scaling
+    to one full optimizer step.
+
+    Workloads with at most 8 TFLOP of dense Newton-Schulz and 16 M AdamW
+    elements per step (tiny, many_small, h1024) are run whole. Otherwise the
+    sample is one Muon matrix of each distinct shape and the first AdamW
+    tensors up to 1 M elements. Each part is run as its own oracle step
+    (norm of its gradients, momentum, Newton-Schulz and update; AdamW) and a
+    full step is estimated as
+        sum over shapes (matrices of that shape) x (time of its sample matrix)
+        + AdamW time x (AdamW elements / sampled AdamW elements).
+    Inputs are generated once, outside the timed calls."""
+
+    def __init__(self, w):
+        import numpy as np
+
+        import oracle
+        import workloads
+
+        self.np, self.oracle = np, oracle
+        names = [t.name for t in w.tensors]
+        groups = [oracle.route(n, len(t.shape), frozen=t.frozen) for n, t in zip(names, w.tensors)]
+        muon = [i for i, g in enumerate(groups) if g == "muon"]
+        adam = [i for i, g in enumerate(groups) if g == "adamw"]
+        dense = sum(_dense_ns_flops(w.tensors[i].shape) for i in muon)
+        adam_elems = sum(w.tensors[i].numel for i in adam)
+        self.whole = dense <= WHOLE_STEP_MAX_DENSE_FLOPS and adam_elems <= WHOLE_STEP_MAX_ADAMW_ELEMS
+        self.lr = w.lr
+        if self.whole:
+            idx = muon + adam
+            self.parts = [(idx, 1.0)]
+            self.desc = (f"fp64 numpy oracle, one whole step of {w.name} ({len(muon)} Muon matrices, "
+                         f"{adam_elems} AdamW elements)")
+        else:
+            by_shape = {}
+            for i in muon:
+                by_shape.setdefault(tuple(w.tensors[i].shape), []).append(i)
+            self.parts = [([ix[0]], float(len(ix))) for ix in by_shape.values()]
+            ad, tot = [], 0
+            for i in adam:
+                if tot >= SAMPLE_ADAMW_ELEMS:
+                    break
+                ad.append(i)
+                tot += w.tensors[i].numel
+            if ad:
+                self.parts.append((ad, adam_elems / tot))
+            shapes = ", ".join(f"{k[0]}x{k[1]} (x{len(v)})" for k, v in by_shape.items())
+            self.desc = (f"fp64 numpy oracle on a sample of {w.name}: one Muon matrix of each shape ({shapes}) "
+                         f"and {len(ad)} AdamW tensors ({tot} of {adam_elems} elements), each part one oracle "
+                         f"step; full step = sum of part times x (matrices of the shape, or AdamW elements / "
+                         f"sampled)")
+        self.inputs = []
+        for idx, scale in self.parts:
+            self.inputs.append(([names[i] for i in idx], [w.tensors[i].shape for i in idx],
+                                [workloads.master_weight(w, i).astype(np.float64) for i in idx],
+                                [workloads.gradient(w, i, 1) for i in idx], scale))
+
+    def run(self):
+        """One timed pass over the sample: (seconds that ran, estimated seconds of a full step)."""
+        ran = full = 0.0
+        for names, shapes, masters, grads, scale in self.inputs:
+            params = [m.copy() for m in masters]
+            orc = self.oracle.HybridOracle(names, shapes)
+            t0 = time.perf_counter()
+            orc.step(params, grads, self.lr)
+            dt = time.perf_counter() - t0
+            ran += dt
+            full += dt * scale
+        return ran, full
 
 
 # ---------------------------------------------------------------------------
@@ -266,6 +297,37 @@ def adamw_standalone(mx, torch, entries, w, lr, stream, peaks, steps: int = 10, 
                    "and written, the gradient read, the bf16 shadow written under bf16_mixed"}
 
 
+def _batches(idx, size: int = 16):
+    idx = list(idx)
+    for k in range(0, len(idx), size):
+        yield idx[k:k + size]
+
+
+def step_roofline(info, step_s: float, peaks: dict, shadow: bool) -> dict:
+    """The step's ideal time t* against the measured step: the Newton-Schulz
+    flops at the bf16 peak plus the step's algorithmic HBM bytes at the HBM
+    bandwidth, taken one after the other (serial) or fully overlapped (max).
+    The bytes are the streaming kernels' (gradient norm, momentum, AdamW) plus
+    the Muon update's read and write of p (and its bf16 shadow), which the
+    last Newton-Schulz launch does in its epilogue."""
+    f = info["ns_flops_per_step"]
+    b = info["stream_bytes_per_step"] + info["muon_elems"] * (8 + (2 if shadow else 0))
+    out = {"ns_flops_per_step": f, "hbm_bytes_per_step": b, "measured_ms": round(step_s * 1e3, 4),
+           "hbm_gbs": peaks["hbm_gbs"], "how": "t* = F_NS / P_bf16 + B_stream / BW_HBM (serial), "
+           "max(F_NS / P_bf16, B_stream / BW_HBM) (overlapped); frac = t* / measured step time"}
+    for kind, key in (("burst", "bf16_tflops"), ("sustained", "bf16_tflops_sustained")):
+        peak = peaks.get(key)
+        if not peak:
+            continue
+        t_ns = f / (peak * 1e12)
+        t_st = b / (peaks["hbm_gbs"] * 1e9)
+        out[kind] = {"bf16_tflops": peak, "t_serial_ms": round((t_ns + t_st) * 1e3, 4),
+                     "t_overlapped_ms": round(max(t_ns, t_st) * 1e3, 4),
+                     "frac_serial": round((t_ns + t_st) / step_s, 3),
+                     "frac_overlapped": round(max(t_ns, t_st) / step_s, 3)}
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -286,12 +348,12 @@ def run_ours(args):
         step_, total_, warm_, min_rate = w.schedule
         lr = w.lr * mx.muon_adamw_cosine_with_min_lr(step_, total_, warm_, min_rate)
     gdt = torch.bfloat16 if w.grad_dtype == "bf16" else torch.float32
-    masters = workloads.master_weights(w)
-    grads = workloads.gradients(w, 1)
     # Gradients live in one flat device buffer (per-parameter views at 128-byte
     # aligned offsets, as a data-parallel gradient bucket would hold them), and
     # their host copy in one flat pinned buffer, so that the end-to-end leg
-    # moves each step's inputs with one host->device copy.
+    # moves each step's inputs with one host->device copy. Inputs are made in
+    # batches of tensors and uploaded as they are made (full-size workloads
+    # never sit whole in host memory).
     align = 128 // torch.tensor([], dtype=gdt).element_size()
     offs, total = [], 0
     for t in w.tensors:
@@ -300,22 +362,24 @@ def run_ours(args):
             total += (t.numel + align - 1) // align * align
     gflat = torch.zeros(max(total, 1), dtype=gdt, device=dev)
     hflat = torch.zeros(max(total, 1), dtype=gdt).pin_memory()
-    P, G, S, entries = [], [], [], []
-    for i, t in enumerate(w.tensors):
-        p = torch.from_numpy(masters[i]).to(dev)
-        g = None
-        if not t.frozen:
-            n = t.numel
-            g = gflat[offs[i]:offs[i] + n].view(t.shape)
-            g.copy_(torch.from_numpy(grads[i]).to(dev).to(gdt))
-            hflat[offs[i]:offs[i] + n].copy_(torch.from_numpy(grads[i]).reshape(-1).to(gdt))
-        s = torch.empty(t.shape, dtype=torch.bfloat16, device=dev) if (w.policy == "bf16_mixed" and not t.frozen) \
-            else None
-        P.append(p)
-        G.append(g)
-        S.append(s)
-        entries.append((t.name, p, g, s, mx.MA_GROUP_FROZEN if t.frozen else None))
-    del masters, grads
+    n = len(w.tensors)
+    P, G, S, entries = [None] * n, [None] * n, [None] * n, [None] * n
+    for batch in _batches(range(n)):
+        ms = workloads.master_weights(w, batch)
+        gs = workloads.gradients(w, 1, batch)
+        for i, m, g_np in zip(batch, ms, gs):
+            t = w.tensors[i]
+            P[i] = torch.from_numpy(m).to(dev)
+            if not t.frozen:
+                k = t.numel
+                src = torch.from_numpy(g_np).reshape(-1).to(gdt)
+                hflat[offs[i]:offs[i] + k].copy_(src)
+                G[i] = gflat[offs[i]:offs[i] + k].view(t.shape)
+                G[i].copy_(src.view(t.shape).to(dev))
+            if w.policy == "bf16_mixed" and not t.frozen:
+                S[i] = torch.empty(t.shape, dtype=torch.bfloat16, device=dev)
+            entries[i] = (t.name, P[i], G[i], S[i], mx.MA_GROUP_FROZEN if t.frozen else None)
+        del ms, gs
     stream = torch.cuda.current_stream()
     opt = mx.MuonAdamW(entries, precision=mx.MA_BF16_MIXED if w.policy == "bf16_mixed" else mx.MA_FP32_MIXED,
                        stream=stream)
@@ -352,9 +416,11 @@ def run_ours(args):
     # CUDA events on (direct launches; the events sit between them) ----
     mx.muon_adamw_reset_profile(opt.handle)
     mx.muon_adamw_set_profiling(opt.handle, True)
+    t_prof = time.perf_counter()
     for _ in range(args.steps):
         opt.step(lr)
     torch.cuda.synchronize()
+    t_prof = time.perf_counter() - t_prof
     mx.muon_adamw_set_profiling(opt.handle, False)
     prof = opt.profile()
 
@@ -398,6 +464,12 @@ def run_ours(args):
     e2e_s = max_over_ranks(e2e_s, dist, dev)
 
     peaks = load_peaks()
+    # A kernel timed inside a long run of steps is held to the sustained bf16
+    # peak, one timed in a short burst to the burst peak.
+    sustained = t_prof >= 0.5 and peaks.get("bf16_tflops_sustained")
+    tc_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    tc_peak_kind = ("bf16 dense sustained" if sustained else "bf16 dense burst") + \
+        f", {peaks['source']} (MEASURED_PEAKS.json)"
     ns_ms = sum(prof[k]["ms"] for k in NS_KINDS)
     ns_flops = sum(prof[k]["units"] for k in NS_KINDS)
     ns_launches = sum(prof[k]["launches"] for k in NS_KINDS)
@@ -411,13 +483,21 @@ def run_ours(args):
              "ms_per_launch": round(e["ms"] / e["launches"], 5)}
         if k in NS_KINDS:
             d["tflops"] = round(e["units"] / (e["ms"] / 1e3) / 1e12, 1)
-            d["frac_bf16_peak"] = round(d["tflops"] / peaks["bf16_tflops"], 3)
+            d["frac_bf16_peak"] = round(d["tflops"] / tc_peak, 3)
+            d["frac_bf16_burst"] = round(d["tflops"] / peaks["bf16_tflops"], 3)
+        elif k == "ns_narrow":
+            d["tflops_fp32"] = round(e["units"] / (e["ms"] / 1e3) / 1e12, 2)
         elif k in STREAM_KINDS:
             d["gbs"] = round(e["units"] / (e["ms"] / 1e3) / 1e9, 1)
             d["frac_hbm"] = round(d["gbs"] / peaks["hbm_gbs"], 3)
+            d["frac_8tbs"] = round(d["gbs"] / 8000.0, 3)
             if k == "adamw":
-                d["note"] = ("second stream, concurrent with the Newton-Schulz chain: the event time includes "
-                             "waiting for SMs")
+                d["note"] = ("second stream, beside the momentum pass and the Newton-Schulz chain: the event "
+                             "time includes sharing HBM and waiting for SMs (adamw_standalone times it alone)")
+            elif k == "momentum" and prof["adamw"]["launches"]:
+                d["note"] = "runs beside AdamW (second stream): both share HBM bandwidth"
+        elif k == "ns_prep" and prof["adamw"]["launches"]:
+            d["note"] = "its event time includes waiting for AdamW's blocks to leave the SMs"
         kernels[k] = d
     launches = sum(prof[k]["launches"] for k in KINDS)
     adam_alone = adamw_standalone(mx, torch, entries, w, lr, stream, peaks)
@@ -439,14 +519,15 @@ def run_ours(args):
         "config": {
             "workload": f"{w.name}: {len(w.tensors)} tensors, {info['n_muon']} Muon matrices "
                         f"({info['muon_elems']} elements, {info['n_buckets']} shape buckets), "
-                        f"{info['adamw_elems']} AdamW elements, {w.grad_dtype} grads, {w.policy}",
+                        f"{info['adamw_elems']} AdamW elements, {info['n_frozen']} frozen, {w.grad_dtype} grads, "
+                        f"{w.policy}",
             "lr": lr,
             "l2": "no flush: each step touches "
                   f"{info['stream_bytes_per_step'] / 1e9:.2f} GB of state and gradients, far above the 129 MB L2",
             "parallelism": f"replicas x{world}",
         },
         "ns5_tflops": round(ns_tflops, 1) if ns_tflops else None,
-        "ns5_frac_bf16_peak": round(ns_tflops / peaks["bf16_tflops"], 3) if ns_tflops else None,
+        "ns5_frac_bf16_peak": round(ns_tflops / tc_peak, 3) if ns_tflops else None,
         "ns5_dense_equiv_tflops": round(info["ns_dense_flops_per_step"] * args.steps / (ns_ms / 1e3) / 1e12, 1)
         if ns_ms > 0 else None,
         "kernels": kernels,
@@ -456,15 +537,18 @@ def run_ours(args):
                           if prof["ns_fused"]["launches"] else "")),
             "bound": "tensor",
             "achieved": round(ns_tflops, 1) if ns_tflops else None,
-            "peak": peaks["bf16_tflops"],
-            "peak_kind": f"bf16 dense burst, {peaks['source']} (MEASURED_PEAKS.json)",
+            "peak": tc_peak,
+            "peak_kind": tc_peak_kind,
             "unit": "TFLOP/s",
-            "frac": round(ns_tflops / peaks["bf16_tflops"], 3) if ns_tflops else None,
+            "frac": round(ns_tflops / tc_peak, 3) if ns_tflops else None,
+            "frac_of_burst": round(ns_tflops / peaks["bf16_tflops"], 3) if ns_tflops else None,
             "traffic": ns_traffic_per_launch(w.name),
-            "traffic_unit": "bytes per launch (ncu, scaled from the 6-layer case; null when stale)",
+            "traffic_unit": "DRAM bytes per launch (ncu, scaled from a smaller case of the same shapes; null "
+                            "when stale)",
             "launches_timed": ns_launches,
             "algorithmic_flops_per_launch": round(ns_flops / max(1, ns_launches)),
         },
+        "step_roofline": step_roofline(info, max_s / args.steps, peaks, w.policy == "bf16_mixed"),
         "clocks": clk,
         "e2e": {"value": round(args.steps * world / e2e_s, 3), "unit": "steps/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": d2h,
@@ -475,11 +559,16 @@ def run_ours(args):
         "gpu_launches": int(launches),
         "adamw_standalone": adam_alone,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        full, desc, spent = oracle_sample_seconds(w, layers_sampled=args.cpu_layers)
-        out["cpu_baseline"] = {"value": round(1.0 / full, 6), "unit": "steps/s", "cores": host_cores(),
-                               "kind": "oracle", "sample": desc}
     opt.close()
+    del opt
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp = OracleSample(w)
+        runs = [smp.run() for _ in range(args.cpu_repeats)]
+        full = statistics.median(r[1] for r in runs)
+        out["cpu_baseline"] = {"value": round(1.0 / full, 6), "unit": "steps/s", "cores": host_cores(),
+                               "kind": "oracle", "extrapolated": not smp.whole,
+                               "sample": f"{smp.desc}; median of {len(runs)} passes, each "
+                                         f"{statistics.median(r[0] for r in runs):.2f} s of oracle work"}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist is not None:
@@ -493,15 +582,15 @@ def run_reference(args):
     if rank != 0:
         return
     w = workloads.get_workload(args.workload)
+    smp = OracleSample(w)
     for _ in range(args.warmup):
-        oracle_sample_seconds(w, layers_sampled=1)
-    per_step = []
-    desc = ""
-    for _ in range(args.steps):
-        full, desc, _spent = oracle_sample_seconds(w, layers_sampled=1)
-        per_step.append(full)
-    total = sum(per_step)
-    value = args.steps / total
+        smp.run()
+    t_wall = time.perf_counter()
+    runs = [smp.run() for _ in range(args.steps)]
+    t_wall = time.perf_counter() - t_wall
+    ran = sum(r[0] for r in runs)
+    full = sum(r[1] for r in runs)
+    value = args.steps / full
     out = {
         "impl": "reference",
         "metric": METRIC,
@@ -510,15 +599,21 @@ def run_reference(args):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(total * 1e3 / args.steps, 2),
+        "ms_per_step": round(ran * 1e3 / args.steps, 2),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (same seeded inputs as the GPU arm)",
         "config": {"workload": w.name, "parallelism": "host CPU, rank 0 only"},
+        "extrapolated": not smp.whole,
+        "sample": {"what_ran": smp.desc, "steps_timed": args.steps,
+                   "oracle_s_per_timed_step": round(ran / args.steps, 4),
+                   "full_step_s_estimated": round(full / args.steps, 4), "wall_s_timed_region": round(t_wall, 3),
+                   "how": "each timed step runs the sample once (ms_per_step is its time); value is the "
+                          "estimated rate of whole optimizer steps"},
         "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": host_cores(), "kind": "oracle",
-                         "sample": desc},
+                         "extrapolated": not smp.whole, "sample": smp.desc},
         "e2e": {"value": round(value, 6), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
@@ -527,15 +622,20 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="h1024")
+    ap.add_argument("--workload", default="full_vla")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--cpu-layers", type=int, default=2, help="layers in the oracle's timed sample")
+    ap.add_argument("--cpu-repeats", type=int, default=2, help="passes of the oracle sample for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE is {world}: launch one process per GPU, e.g. "
+                 f"python -m torch.distributed.run --nnodes=1 --nproc-per-node {args.gpus} --master-addr 127.0.0.1 "
+                 f"bench.py --gpus {args.gpus}")
     if args.impl == "reference":
         run_reference(args)
     else:

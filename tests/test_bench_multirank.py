@@ -61,7 +61,7 @@ def test_max_over_ranks_and_aggregate_with_gloo():
 
 def test_reference_arm_prints_only_on_rank0():
     code = ("import sys; sys.path.insert(0, %r); import bench; "
-            "bench.main(['--impl', 'reference', '--workload', 'tiny', '--steps', '1', '--warmup', '3'])" % ROOT)
+            "bench.main(['--impl', 'reference', '--workload', 'tiny', '--steps', '1', '--warmup', '3', '--gpus', '2'])" % ROOT)
     outs = _run_ranks(code)
     line = json.loads(outs[0].strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
