@@ -340,6 +340,76 @@ MA_API ma_status muon_adamw_reset_profile(muon_adamw_t* h);
  * and the handle. Caller memory is not touched. h == NULL is MA_ERR_ARG. */
 MA_API ma_status muon_adamw_destroy(muon_adamw_t* h);
 
+/* ---- Sharded step: several ranks, one GPU each ----
+ * The article runs this optimizer under FSDP on 8 GPUs (核心揭秘一 / 为 FSDP
+ * 分片量身定制的细节: MuonShardPlan all-gathers each matrix's shards so that
+ * Newton-Schulz sees the whole matrix). Here the step itself is divided over
+ * `world` ranks that all hold every parameter and gradient (data parallel,
+ * gradients already reduced):
+ *   - each Muon matrix is updated whole by one owner rank, chosen
+ *     longest-processing-time-first on its dense Newton-Schulz flops
+ *     5 (4 s^2 l + 2 s^3), s/l its short/long side;
+ *   - AdamW parameters, concatenated in registration order, are split into
+ *     `world` contiguous ranges of nearly equal length, each cut moved down
+ *     to a multiple of 64 elements of the parameter it falls in;
+ *   - every rank computes the sum of squares of the gradients it owns; the
+ *     caller all-reduces (sums) these numbers, and every rank clips with the
+ *     global norm sqrt(sum) exactly as the single-GPU step does;
+ *   - after the step each rank has updated only what it owns: the caller
+ *     shares the results (a broadcast of each Muon matrix from its owner, an
+ *     all-gather of the AdamW ranges, and the same for bf16 shadows).
+ * The library issues no collective and never reads another rank's memory.
+ * A rank allocates the state of what it owns only (AdamW m and v for its
+ * range). The partition depends only on the registrations and `world`, so
+ * every rank computes the same one. */
+#define MA_SHARD_MAX_WORLD 4096
+
+/* The partition above as a pure host function (needs no device): n_params
+ * parameters with groups[i] (MA_GROUP_MUON / ADAMW / FROZEN), numels[i] and,
+ * for Muon matrices, rows[i] x cols[i]. owner_out[i] (n_params entries):
+ * the rank that updates Muon matrix i, -1 for the others. begin_out/end_out
+ * (n_params * world entries, [i * world + r]): the elements [begin, end) of
+ * parameter i that rank r updates (the whole matrix at its owner, a range for
+ * AdamW, empty otherwise). Errors: MA_ERR_ARG (NULL pointer, bad group,
+ * world outside 1..MA_SHARD_MAX_WORLD), MA_ERR_SHAPE (negative size, a Muon
+ * matrix whose rows x cols is not numel). */
+MA_API ma_status muon_adamw_plan_shards(int n_params, const int32_t* groups, const int64_t* numels,
+                                        const int64_t* rows, const int64_t* cols, int world, int32_t* owner_out,
+                                        int64_t* begin_out, int64_t* end_out);
+
+/* Make handle h rank `rank` of `world` (0 <= rank < world), before the first
+ * step; world 1 (the default) is the single-GPU step. Errors: MA_ERR_ARG,
+ * MA_ERR_STATE (after the first step). */
+MA_API ma_status muon_adamw_set_shard(muon_adamw_t* h, int rank, int world);
+
+/* The elements [*begin, *end) of parameter `index` that rank `rank` updates
+ * under h's partition (the whole trainable parameter for world 1). Computed
+ * from the registrations so far, which are final from the first step on.
+ * get_state/set_state of a sharded handle move exactly this rank's range
+ * (end - begin values); for a parameter this rank does not update they return
+ * MA_ERR_STATE. Errors: MA_ERR_ARG. */
+MA_API ma_status muon_adamw_shard_range(muon_adamw_t* h, int index, int rank, int64_t* begin, int64_t* end);
+
+/* First half of a step (any handle; the only way a handle of world > 1
+ * steps, muon_adamw_step returns MA_ERR_STATE there): like muon_adamw_step
+ * up to the gradient norm, it freezes the plan at the first call, advances
+ * the step counter and queues on the handle's stream the sum of squares of
+ * the gradients this rank owns, written as one fp64 value to local_sumsq
+ * (device pointer, 8-byte aligned). Asynchronous. Errors: MA_ERR_ARG,
+ * MA_ERR_ALIGN, MA_ERR_STATE (step_begin twice without step_end), MA_ERR_OOM,
+ * MA_ERR_CUDA. */
+MA_API ma_status muon_adamw_step_begin(muon_adamw_t* h, double lr, double* local_sumsq);
+
+/* Second half: global_sumsq (device pointer, 8-byte aligned) holds the sum of
+ * every rank's local_sumsq, written on or before the handle's stream reaches
+ * this point (e.g. an all-reduce queued on that stream); the norm is its
+ * square root, the clip coefficient min(1, max_grad_norm / (norm + clip_eps))
+ * as in muon_adamw_step, then this rank's Muon matrices and AdamW ranges are
+ * updated. grad_norm_out as in muon_adamw_step. Errors: MA_ERR_ARG,
+ * MA_ERR_ALIGN, MA_ERR_STATE (no step_begin), MA_ERR_CUDA,
+ * MA_ERR_DEVICE_CHECK. */
+MA_API ma_status muon_adamw_step_end(muon_adamw_t* h, const double* global_sumsq, float* grad_norm_out);
+
 /* ---- Allocation-free gradient norm ----
  * The article has no counterpart to this entry point; it exists for callers
  * that cannot call cudaMalloc, such as a host that gives all device memory

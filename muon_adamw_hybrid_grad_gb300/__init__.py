@@ -152,6 +152,16 @@ _SIGNATURES = {
     "muon_adamw_get_profile": (ctypes.c_int, [_P, ctypes.POINTER(Profile)]),
     "muon_adamw_reset_profile": (ctypes.c_int, [_P]),
     "muon_adamw_destroy": (ctypes.c_int, [_P]),
+    "muon_adamw_plan_shards": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                                              ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                                              ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                                              ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
+                                              ctypes.POINTER(ctypes.c_int64)]),
+    "muon_adamw_set_shard": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int]),
+    "muon_adamw_shard_range": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
+                                              ctypes.POINTER(ctypes.c_int64)]),
+    "muon_adamw_step_begin": (ctypes.c_int, [_P, ctypes.c_double, _P]),
+    "muon_adamw_step_end": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_float)]),
     "muon_adamw_grad_norm_noalloc": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_int64),
                                                     ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_double,
                                                     ctypes.c_double, _P, _P]),
@@ -317,6 +327,66 @@ def muon_adamw_destroy(h: int) -> None:
     _check(load_library().muon_adamw_destroy(_P(h)))
 
 
+MA_SHARD_MAX_WORLD = 4096
+
+
+def muon_adamw_plan_shards(groups: Sequence[int], numels: Sequence[int], rows: Sequence[int],
+                           cols: Sequence[int], world: int):
+    """The sharded step's partition (host only). Returns (owner, ranges):
+    owner[i] is the rank that updates Muon matrix i (-1 otherwise), ranges[i]
+    a list of `world` (begin, end) element ranges of parameter i."""
+    n = len(groups)
+    g = (ctypes.c_int32 * max(1, n))(*[int(x) for x in groups])
+    nu = (ctypes.c_int64 * max(1, n))(*[int(x) for x in numels])
+    r = (ctypes.c_int64 * max(1, n))(*[int(x) for x in rows])
+    c = (ctypes.c_int64 * max(1, n))(*[int(x) for x in cols])
+    owner = (ctypes.c_int32 * max(1, n))()
+    b = (ctypes.c_int64 * max(1, n * world))()
+    e = (ctypes.c_int64 * max(1, n * world))()
+    _check(load_library().muon_adamw_plan_shards(n, g, nu, r, c, int(world), owner, b, e))
+    return ([int(owner[i]) for i in range(n)],
+            [[(int(b[i * world + k]), int(e[i * world + k])) for k in range(world)] for i in range(n)])
+
+
+def muon_adamw_set_shard(h: int, rank: int, world: int) -> None:
+    _check(load_library().muon_adamw_set_shard(_P(h), int(rank), int(world)))
+
+
+def muon_adamw_shard_range(h: int, index: int, rank: int):
+    b, e = ctypes.c_int64(), ctypes.c_int64()
+    _check(load_library().muon_adamw_shard_range(_P(h), int(index), int(rank), ctypes.byref(b), ctypes.byref(e)))
+    return int(b.value), int(e.value)
+
+
+def muon_adamw_step_begin(h: int, lr: float, local_sumsq_ptr: int) -> None:
+    _check(load_library().muon_adamw_step_begin(_P(h), float(lr), _P(local_sumsq_ptr or None)))
+
+
+def muon_adamw_step_end(h: int, global_sumsq_ptr: int, want_norm: bool = False) -> Optional[float]:
+    if want_norm:
+        out = ctypes.c_float()
+        _check(load_library().muon_adamw_step_end(_P(h), _P(global_sumsq_ptr or None), ctypes.byref(out)))
+        return float(out.value)
+    _check(load_library().muon_adamw_step_end(_P(h), _P(global_sumsq_ptr or None), None))
+    return None
+
+
+def shard_exchange(tensors, ranges, rank: int, world: int, dist, group=None) -> None:
+    """After a sharded step, give every rank the parts the others updated:
+    for each tensor i (None is skipped) and each rank r, the elements
+    ranges[i][r] = (begin, end) of its flattened view are broadcast from r.
+    Collectives only (torch.distributed): gloo for CPU tensors, NCCL for CUDA
+    ones."""
+    for t, rr in zip(tensors, ranges):
+        if t is None:
+            continue
+        flat = t.view(-1)
+        for src in range(world):
+            b, e = rr[src]
+            if e > b:
+                dist.broadcast(flat[b:e], src=src, group=group)
+
+
 MA_NOALLOC_MAX_TENSORS = 64
 
 
@@ -349,7 +419,7 @@ class MuonAdamW:
     Tensors must stay alive and keep their storage until ``close()``.
     """
 
-    def __init__(self, params, *, stream=None, **config):
+    def __init__(self, params, *, stream=None, shard=None, **config):
         import torch
 
         cfg = muon_adamw_config_init()
@@ -376,6 +446,13 @@ class MuonAdamW:
         self.cfg = cfg
         self.stream = stream if stream is not None else torch.cuda.current_stream()
         self.handle = muon_adamw_create(cfg, self.stream.cuda_stream)
+        self.rank, self.world = (0, 1) if shard is None else (int(shard[0]), int(shard[1]))
+        if self.world > 1:
+            try:
+                muon_adamw_set_shard(self.handle, self.rank, self.world)
+            except Exception:
+                self.close()
+                raise
         self._keep = []
         self.indices = []
         self.groups = []
@@ -423,11 +500,59 @@ class MuonAdamW:
     def step(self, lr: float, want_norm: bool = False):
         return muon_adamw_step(self.handle, lr, want_norm)
 
+    def shard_range(self, index: int, rank: Optional[int] = None):
+        """(begin, end): the elements of parameter `index` that `rank` (this
+        handle's rank by default) updates."""
+        return muon_adamw_shard_range(self.handle, index, self.rank if rank is None else rank)
+
+    def shard_ranges(self):
+        """Per parameter, the (begin, end) range of every rank."""
+        return [[self.shard_range(i, r) for r in range(self.world)] for i in range(len(self._keep))]
+
+    def step_begin(self, lr: float, local_sumsq) -> None:
+        """First half of a step: this rank's gradient sum of squares into the
+        one-element fp64 CUDA tensor `local_sumsq`."""
+        muon_adamw_step_begin(self.handle, lr, local_sumsq.data_ptr())
+
+    def step_end(self, global_sumsq, want_norm: bool = False):
+        """Second half: clip with the summed `global_sumsq` and update this
+        rank's parameters."""
+        return muon_adamw_step_end(self.handle, global_sumsq.data_ptr(), want_norm)
+
+    def sharded_step(self, lr: float, dist, group=None, want_norm: bool = False):
+        """One step of rank `self.rank` of `self.world`: step_begin, an
+        all-reduce (sum) of the local sums of squares, step_end, then the
+        exchange of every rank's updated parameters and shadows."""
+        import torch
+
+        if not hasattr(self, "_sumsq"):
+            self._sumsq = torch.zeros(1, dtype=torch.float64, device=self._device())
+        self.step_begin(lr, self._sumsq)
+        dist.all_reduce(self._sumsq, group=group)
+        norm = self.step_end(self._sumsq, want_norm)
+        ranges = self.shard_ranges()
+        shard_exchange([k[0] for k in self._keep], ranges, self.rank, self.world, dist, group)
+        shard_exchange([k[2] for k in self._keep], ranges, self.rank, self.world, dist, group)
+        return norm
+
+    def _device(self):
+        for p, g, _ in self._keep:
+            if p is not None:
+                return p.device
+        import torch
+
+        return torch.device("cuda")
+
     def state(self, index: int, which: int = 0):
+        """The optimizer state of parameter `index` on the host (for a sharded
+        handle: this rank's range of it, flattened, where that is not the
+        whole parameter)."""
         import torch
 
         p = self._keep[index][0]
-        out = torch.empty(p.shape, dtype=torch.float32)
+        b, e = self.shard_range(index) if self.world > 1 else (0, p.numel())
+        shape = p.shape if e - b == p.numel() else (e - b,)
+        out = torch.empty(shape, dtype=torch.float32)
         muon_adamw_get_state(self.handle, index, which, out.data_ptr())
         return out
 

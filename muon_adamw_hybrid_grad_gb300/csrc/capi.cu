@@ -98,6 +98,7 @@ struct Param {
   double lr_scale = 1.0, wd_scale = 1.0;  // per-parameter multipliers
   bool options_set = false;               // set explicitly (wins over the exemption rule)
   int og = 0;                             // option group (index into the per-step tables)
+  int64_t own_b = 0, own_e = 0;           // the elements this rank updates (all of them unless sharded)
 };
 
 struct Bucket {
@@ -143,6 +144,8 @@ struct muon_adamw {
   cudaGraphExec_t gexec = nullptr;                // the captured Newton-Schulz chain
   std::vector<Param> params;
   bool planned = false;
+  int shard_rank = 0, shard_world = 1;  // sharded step: this rank's part of the parameters
+  bool begun = false;                   // sharded step: step_begin queued, step_end not yet
   std::vector<std::pair<double, double>> option_groups;  // (lr_scale, wd_scale); [0] = (1, 1)
   int64_t t = 0;
 
@@ -257,19 +260,49 @@ ma_status check_device_flag(muon_adamw* h) {
 
 void set_epi_coefficients(NsEpiArgs& e, const muon_adamw_config& c, int it);
 
+// The elements of each parameter that this rank updates: all of every
+// trainable parameter, or this rank's part of the partition of shard.cu.
+void assign_ownership(muon_adamw* h) {
+  const size_t n = h->params.size();
+  if (h->shard_world <= 1) {
+    for (Param& p : h->params) {
+      p.own_b = 0;
+      p.own_e = p.group == MA_GROUP_FROZEN ? 0 : p.numel;
+    }
+    return;
+  }
+  std::vector<int> group(n), owner;
+  std::vector<int64_t> numel(n), rows(n), cols(n), b, e;
+  for (size_t i = 0; i < n; ++i) {
+    const Param& p = h->params[i];
+    group[i] = p.group;
+    numel[i] = p.numel;
+    rows[i] = p.shape.size() == 2 ? p.shape[0] : p.numel;
+    cols[i] = p.shape.size() == 2 ? p.shape[1] : 1;
+  }
+  shard_partition(group, numel, rows, cols, h->shard_world, owner, b, e);
+  for (size_t i = 0; i < n; ++i) {
+    h->params[i].own_b = b[i * (size_t)h->shard_world + (size_t)h->shard_rank];
+    h->params[i].own_e = e[i * (size_t)h->shard_world + (size_t)h->shard_rank];
+  }
+}
+
 ma_status build_plan(muon_adamw* h) {
   const muon_adamw_config& c = h->cfg;
   if (h->arena) {  // a previous attempt failed part-way
     cudaFree(h->arena);
     h->arena = nullptr;
   }
-  // --- classify ---
+  // --- ownership (the whole of every trainable parameter unless sharded) ---
+  assign_ownership(h);
+  // --- classify: the parameters this rank updates ---
   h->muon_params.clear();
   h->adam_params.clear();
   for (int i = 0; i < (int)h->params.size(); ++i) {
     const Param& p = h->params[i];
-    if (p.group == MA_GROUP_MUON && p.numel > 0) h->muon_params.push_back(i);
-    if (p.group == MA_GROUP_ADAMW && p.numel > 0) h->adam_params.push_back(i);
+    if (p.own_e <= p.own_b) continue;
+    if (p.group == MA_GROUP_MUON) h->muon_params.push_back(i);
+    if (p.group == MA_GROUP_ADAMW) h->adam_params.push_back(i);
   }
   // --- buckets (by padded canonical shape and narrowness, first-seen order) ---
   std::map<std::pair<std::pair<int, int>, bool>, int> bidx;
@@ -304,10 +337,11 @@ ma_status build_plan(muon_adamw* h) {
     off += al(h->params[pi].numel * sizeof(float));
   }
   for (int pi : h->adam_params) {
+    const int64_t n_own = h->params[pi].own_e - h->params[pi].own_b;
     st0_off[pi] = off;
-    off += al(h->params[pi].numel * sizeof(float));
+    off += al(n_own * sizeof(float));
     st1_off[pi] = off;
-    off += al(h->params[pi].numel * sizeof(float));
+    off += al(n_own * sizeof(float));
   }
   h->state_bytes = off;
   // per bucket: X ping, X pong (s x l), A, B (s x s), all bf16; a narrow
@@ -331,8 +365,8 @@ ma_status build_plan(muon_adamw* h) {
   auto chunks_of = [](int64_t n) { return (size_t)((n + kChunk - 1) / kChunk); };
   size_t n_norm = 0, n_adam = 0, n_tiles = 0, n_mats = 0;
   for (const Param& p : h->params)
-    if (p.group != MA_GROUP_FROZEN && p.numel > 0) n_norm += chunks_of(p.numel);
-  for (int pi : h->adam_params) n_adam += chunks_of(h->params[pi].numel);
+    if (p.group != MA_GROUP_FROZEN && p.own_e > p.own_b) n_norm += chunks_of(p.own_e - p.own_b);
+  for (int pi : h->adam_params) n_adam += chunks_of(h->params[pi].own_e - h->params[pi].own_b);
   for (int pi : h->muon_params) {
     const Param& p = h->params[pi];
     const bool tall = p.shape[0] > p.shape[1];
@@ -416,14 +450,15 @@ ma_status build_plan(muon_adamw* h) {
   h->bytes_norm = h->bytes_mom = h->bytes_adam = 0;
   for (size_t i = 0; i < h->params.size(); ++i) {
     const Param& p = h->params[i];
-    if (p.group == MA_GROUP_FROZEN || p.numel == 0) continue;
+    if (p.group == MA_GROUP_FROZEN || p.own_e <= p.own_b) continue;
     const size_t es = p.gdtype == MA_DT_BF16 ? 2 : 4;
-    h->grad_elems += p.numel;
-    h->bytes_norm += (double)p.numel * es;
-    for (int64_t o = 0; o < p.numel; o += kChunk) {
+    const int64_t n_own = p.own_e - p.own_b;
+    h->grad_elems += n_own;
+    h->bytes_norm += (double)n_own * es;
+    for (int64_t o = 0; o < n_own; o += kChunk) {
       GradChunk gc;
-      gc.g = static_cast<const char*>(p.g) + o * es;
-      gc.n = std::min<int64_t>(kChunk, p.numel - o);
+      gc.g = static_cast<const char*>(p.g) + (p.own_b + o) * es;
+      gc.n = std::min<int64_t>(kChunk, n_own - o);
       gc.dtype = p.gdtype == MA_DT_BF16 ? DT_BF16 : DT_F32;
       gc.vec = (reinterpret_cast<uintptr_t>(gc.g) % 16) == 0;
       norm_chunks.push_back(gc);
@@ -451,16 +486,18 @@ ma_status build_plan(muon_adamw* h) {
   for (int pi : h->adam_params) {
     const Param& p = h->params[pi];
     const size_t es = p.gdtype == MA_DT_BF16 ? 2 : 4;
-    h->adam_elems += p.numel;
-    h->bytes_adam += (double)p.numel * (es + 24 + (p.shadow ? 2 : 0));
-    for (int64_t o = 0; o < p.numel; o += kChunk) {
+    const int64_t n_own = p.own_e - p.own_b;
+    h->adam_elems += n_own;
+    h->bytes_adam += (double)n_own * (es + 24 + (p.shadow ? 2 : 0));
+    for (int64_t o = 0; o < n_own; o += kChunk) {
+      const int64_t e0 = p.own_b + o;  // element of the parameter; the state holds the owned range only
       AdamChunk a;
-      a.p = p.p + o;
-      a.g = static_cast<const char*>(p.g) + o * es;
+      a.p = p.p + e0;
+      a.g = static_cast<const char*>(p.g) + e0 * es;
       a.m = p.st0 + o;
       a.v = p.st1 + o;
-      a.shadow = p.shadow ? p.shadow + o : nullptr;
-      a.n = std::min<int64_t>(kChunk, p.numel - o);
+      a.shadow = p.shadow ? p.shadow + e0 : nullptr;
+      a.n = std::min<int64_t>(kChunk, n_own - o);
       a.gdtype = p.gdtype == MA_DT_BF16 ? DT_BF16 : DT_F32;
       const uintptr_t pa = reinterpret_cast<uintptr_t>(a.p), ga = reinterpret_cast<uintptr_t>(a.g),
                       sa = reinterpret_cast<uintptr_t>(a.shadow);
@@ -785,22 +822,25 @@ static void fill_step_params(muon_adamw* h, double lr, StepParams* sp) {
   sp->ns_lr = (float)lr;
 }
 
-// The launches of one step that read gradients, in order: the norm pass and
-// clip on s0; AdamW forked onto s1; the momentum pass on s0. Each stream then
-// records its grads-consumed event. The per-step scalars are read from
-// h->d_step.
-static ma_status enqueue_gradient_passes(muon_adamw* h) {
-  const muon_adamw_config& c = h->cfg;
+// The gradient-norm pass on s0: per-block partial sums of squares over the
+// gradients this rank owns (every trainable gradient unless sharded).
+static ma_status enqueue_norm_pass(muon_adamw* h) {
   if (h->n_norm_chunks > 0) {
     timed(h, MA_K_GRAD_NORM, h->s0, h->bytes_norm,
           [&] { launch_grad_sumsq(h->d_norm_chunks, h->n_norm_chunks, h->d_norm_partials, h->norm_grid, h->s0); });
   } else {
     CUDA_TRY(cudaMemsetAsync(h->d_norm_partials, 0, sizeof(float), h->s0));
   }
-  timed(h, MA_K_CLIP, h->s0, (double)h->norm_grid * 4, [&] {
-    launch_clip_finalize(h->d_norm_partials, h->n_norm_chunks > 0 ? h->norm_grid : 1, (float)c.max_grad_norm,
-                         (float)c.clip_eps, h->d_scalars, h->s0);
-  });
+  return MA_OK;
+}
+
+static int norm_partials(const muon_adamw* h) { return h->n_norm_chunks > 0 ? h->norm_grid : 1; }
+
+// The launches of one step that read gradients after the norm and clip: AdamW
+// forked onto s1; the momentum pass on s0. Each stream then records its
+// grads-consumed event. The per-step scalars are read from h->d_step.
+static ma_status enqueue_update_passes(muon_adamw* h) {
+  const muon_adamw_config& c = h->cfg;
   const bool have_adam = h->n_adam_chunks > 0;
   if (have_adam) {
     CUDA_TRY(cudaEventRecord(h->ev_fork, h->s0));
@@ -1021,15 +1061,14 @@ ma_status muon_adamw_register_param(muon_adamw_t* h, const char* name, int ndim,
   return ok();
 }
 
-ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
-  if (!h) return fail(MA_ERR_ARG, "NULL handle");
-  if (!isfinite(lr)) return fail(MA_ERR_ARG, "lr is not finite");
+// Start a step: freeze the plan at the first one, advance t and queue the
+// copy of the step's lr- and t-dependent scalars.
+static ma_status begin_step(muon_adamw* h, double lr) {
   CUDA_TRY(cudaSetDevice(h->device));
   if (!h->planned) {
     ma_status st = build_plan(h);
     if (st != MA_OK) return st;
   }
-  const muon_adamw_config& c = h->cfg;
   h->t += 1;
   // the step's scalars go through one of two pinned slots; the slot's
   // previous copy (two steps ago) has been read before it is rewritten
@@ -1038,9 +1077,16 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
   fill_step_params(h, lr, &h->h_step[slot]);
   CUDA_TRY(cudaMemcpyAsync(h->d_step, &h->h_step[slot], sizeof(StepParams), cudaMemcpyHostToDevice, h->s0));
   CUDA_TRY(cudaEventRecord(h->ev_slot[slot], h->s0));
-  ma_status st = enqueue_gradient_passes(h);
+  return MA_OK;
+}
+
+// Finish a step once the clip coefficient is in h->d_scalars: the update
+// passes, the Newton-Schulz chain (one graph launch, or its launches one by
+// one) and the join of the AdamW stream; with grad_norm_out, wait and read.
+static ma_status finish_step(muon_adamw* h, float* grad_norm_out) {
+  const muon_adamw_config& c = h->cfg;
+  ma_status st = enqueue_update_passes(h);
   if (st != MA_OK) return st;
-  // the Newton-Schulz chain: one graph launch, or its launches one by one
   const bool graph = h->graph_mode && !h->graph_broken && !h->profiling && !h->stall_test &&
                      c.ns_kernel == MA_NS_TCGEN05 && h->n_mats > 0;
   if (graph && !h->gexec) capture_newton_schulz_graph(h);
@@ -1061,8 +1107,118 @@ ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
     CUDA_TRY(cudaMemcpyAsync(&sc, h->d_scalars, sizeof sc, cudaMemcpyDeviceToHost, h->s0));
     CUDA_TRY(cudaStreamSynchronize(h->s0));
     *grad_norm_out = sc.total;
-    ma_status st = check_device_flag(h);
+    st = check_device_flag(h);
     if (st != MA_OK) return st;
+  }
+  return ok();
+}
+
+ma_status muon_adamw_step(muon_adamw_t* h, double lr, float* grad_norm_out) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  if (!isfinite(lr)) return fail(MA_ERR_ARG, "lr is not finite");
+  if (h->shard_world > 1)
+    return fail(MA_ERR_STATE, "a sharded handle steps with muon_adamw_step_begin / muon_adamw_step_end");
+  ma_status st = begin_step(h, lr);
+  if (st != MA_OK) return st;
+  const muon_adamw_config& c = h->cfg;
+  st = enqueue_norm_pass(h);
+  if (st != MA_OK) return st;
+  timed(h, MA_K_CLIP, h->s0, (double)h->norm_grid * 4, [&] {
+    launch_clip_finalize(h->d_norm_partials, norm_partials(h), (float)c.max_grad_norm, (float)c.clip_eps,
+                         h->d_scalars, h->s0);
+  });
+  return finish_step(h, grad_norm_out);
+}
+
+ma_status muon_adamw_step_begin(muon_adamw_t* h, double lr, double* local_sumsq) {
+  if (!h || !local_sumsq) return fail(MA_ERR_ARG, "NULL handle or local_sumsq");
+  if (!isfinite(lr)) return fail(MA_ERR_ARG, "lr is not finite");
+  if (h->begun) return fail(MA_ERR_STATE, "step_begin twice without step_end");
+  if (reinterpret_cast<uintptr_t>(local_sumsq) % 8) return fail(MA_ERR_ALIGN, "local_sumsq not 8-byte aligned");
+  ma_status st = begin_step(h, lr);
+  if (st != MA_OK) return st;
+  st = enqueue_norm_pass(h);
+  if (st != MA_OK) return st;
+  timed(h, MA_K_CLIP, h->s0, (double)h->norm_grid * 4,
+        [&] { launch_sumsq_partials(h->d_norm_partials, norm_partials(h), local_sumsq, h->s0); });
+  CUDA_TRY(cudaGetLastError());
+  h->begun = true;
+  return ok();
+}
+
+ma_status muon_adamw_step_end(muon_adamw_t* h, const double* global_sumsq, float* grad_norm_out) {
+  if (!h || !global_sumsq) return fail(MA_ERR_ARG, "NULL handle or global_sumsq");
+  if (!h->begun) return fail(MA_ERR_STATE, "step_end without step_begin");
+  if (reinterpret_cast<uintptr_t>(global_sumsq) % 8) return fail(MA_ERR_ALIGN, "global_sumsq not 8-byte aligned");
+  h->begun = false;
+  CUDA_TRY(cudaSetDevice(h->device));
+  const muon_adamw_config& c = h->cfg;
+  timed(h, MA_K_CLIP, h->s0, 8.0, [&] {
+    launch_clip_from_sumsq(global_sumsq, (float)c.max_grad_norm, (float)c.clip_eps, h->d_scalars, h->s0);
+  });
+  return finish_step(h, grad_norm_out);
+}
+
+ma_status muon_adamw_set_shard(muon_adamw_t* h, int rank, int world) {
+  if (!h) return fail(MA_ERR_ARG, "NULL handle");
+  if (world < 1 || world > MA_SHARD_MAX_WORLD || rank < 0 || rank >= world)
+    return fail(MA_ERR_ARG, "rank %d of world %d: need 0 <= rank < world <= %d", rank, world, MA_SHARD_MAX_WORLD);
+  if (h->planned) return fail(MA_ERR_STATE, "set_shard after the first step (plan is frozen)");
+  h->shard_rank = rank;
+  h->shard_world = world;
+  return ok();
+}
+
+ma_status muon_adamw_shard_range(muon_adamw_t* h, int index, int rank, int64_t* begin, int64_t* end) {
+  if (!h || !begin || !end) return fail(MA_ERR_ARG, "NULL argument");
+  if (index < 0 || index >= (int)h->params.size()) return fail(MA_ERR_ARG, "bad parameter index %d", index);
+  if (rank < 0 || rank >= h->shard_world) return fail(MA_ERR_ARG, "rank %d outside world %d", rank, h->shard_world);
+  const Param& q = h->params[index];
+  if (h->shard_world == 1) {
+    *begin = 0;
+    *end = q.group == MA_GROUP_FROZEN ? 0 : q.numel;
+    return ok();
+  }
+  const size_t n = h->params.size();
+  std::vector<int> group(n), owner;
+  std::vector<int64_t> numel(n), rows(n), cols(n), b, e;
+  for (size_t i = 0; i < n; ++i) {
+    const Param& p = h->params[i];
+    group[i] = p.group;
+    numel[i] = p.numel;
+    rows[i] = p.shape.size() == 2 ? p.shape[0] : p.numel;
+    cols[i] = p.shape.size() == 2 ? p.shape[1] : 1;
+  }
+  shard_partition(group, numel, rows, cols, h->shard_world, owner, b, e);
+  *begin = b[(size_t)index * (size_t)h->shard_world + (size_t)rank];
+  *end = e[(size_t)index * (size_t)h->shard_world + (size_t)rank];
+  return ok();
+}
+
+ma_status muon_adamw_plan_shards(int n_params, const int32_t* groups, const int64_t* numels, const int64_t* rows,
+                                 const int64_t* cols, int world, int32_t* owner_out, int64_t* begin_out,
+                                 int64_t* end_out) {
+  if (n_params < 0 || (n_params > 0 && (!groups || !numels || !rows || !cols || !owner_out || !begin_out || !end_out)))
+    return fail(MA_ERR_ARG, "NULL pointer or negative n_params");
+  if (world < 1 || world > MA_SHARD_MAX_WORLD) return fail(MA_ERR_ARG, "world must be 1..%d", MA_SHARD_MAX_WORLD);
+  std::vector<int> group((size_t)n_params), owner;
+  std::vector<int64_t> numel((size_t)n_params), r((size_t)n_params), cl((size_t)n_params), b, e;
+  for (int i = 0; i < n_params; ++i) {
+    if (groups[i] != MA_GROUP_MUON && groups[i] != MA_GROUP_ADAMW && groups[i] != MA_GROUP_FROZEN)
+      return fail(MA_ERR_ARG, "groups[%d] must be MUON, ADAMW or FROZEN", i);
+    if (numels[i] < 0 || rows[i] < 0 || cols[i] < 0) return fail(MA_ERR_SHAPE, "negative size for parameter %d", i);
+    if (groups[i] == MA_GROUP_MUON && rows[i] * cols[i] != numels[i])
+      return fail(MA_ERR_SHAPE, "Muon parameter %d: rows x cols != numel", i);
+    group[(size_t)i] = groups[i];
+    numel[(size_t)i] = numels[i];
+    r[(size_t)i] = rows[i];
+    cl[(size_t)i] = cols[i];
+  }
+  shard_partition(group, numel, r, cl, world, owner, b, e);
+  for (int i = 0; i < n_params; ++i) owner_out[i] = owner[(size_t)i];
+  if (!b.empty()) {
+    memcpy(begin_out, b.data(), b.size() * sizeof(int64_t));
+    memcpy(end_out, e.data(), e.size() * sizeof(int64_t));
   }
   return ok();
 }
@@ -1168,7 +1324,9 @@ static ma_status state_ptr(muon_adamw_t* h, int index, int which, float** ptr, i
   } else {
     return fail(MA_ERR_ARG, "bad which %d", which);
   }
-  *n = p.numel;
+  if (p.numel > 0 && p.own_e <= p.own_b)
+    return fail(MA_ERR_STATE, "parameter %d is not updated by this rank (sharded step)", index);
+  *n = p.own_e - p.own_b;  // the whole parameter, or this rank's range of an AdamW parameter
   return MA_OK;
 }
 

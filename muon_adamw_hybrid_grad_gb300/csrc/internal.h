@@ -147,6 +147,12 @@ void clear_last_error();
 void launch_grad_sumsq(const GradChunk* chunks, int nchunks, float* partials, int grid, cudaStream_t st);
 void launch_clip_finalize(const float* partials, int n, float max_norm, float clip_eps, StepScalars* out,
                           cudaStream_t st);
+// The sum of the norm pass's partials, in fp64, to *out (one block): this
+// rank's share of the global sum of squares in a sharded step.
+void launch_sumsq_partials(const float* partials, int n, double* out, cudaStream_t st);
+// Norm and clip coefficient from a global sum of squares (one thread), with
+// the same rules as clip_finalize.
+void launch_clip_from_sumsq(const double* sumsq, float max_norm, float clip_eps, StepScalars* out, cudaStream_t st);
 void launch_muon_momentum(const MomTile* tiles, int ntiles, const MuonMat* mats, const StepScalars* sc,
                           MomArgs args, float* tile_partials, int grid, cudaStream_t st);
 void launch_ns_prep(const MuonMat* mats, int nmat, const float* tile_partials, float eps, float* rscale,
@@ -226,6 +232,16 @@ struct NarrowLaunch {
   float coef[64][3];         // (a, b, c) of each iteration
 };
 cudaError_t launch_ns_narrow(const NarrowLaunch& L, int num_sms, cudaStream_t st);  // grid: min(nmat, 4 SMs)
+
+// Partition of the trainable parameters over `world` ranks (host; shard.cu).
+// group/numel/rows/cols per parameter (rows, cols used for Muon matrices).
+// owner[i]: the rank that updates Muon matrix i (-1 otherwise); begin/end
+// [i * world + r]: the elements [begin, end) of parameter i that rank r
+// updates (the whole matrix at its owner, a contiguous range for AdamW,
+// empty otherwise).
+void shard_partition(const std::vector<int>& group, const std::vector<int64_t>& numel,
+                     const std::vector<int64_t>& rows, const std::vector<int64_t>& cols, int world,
+                     std::vector<int>& owner, std::vector<int64_t>& begin, std::vector<int64_t>& end);
 
 // Static assignment of a launch's work units to `ncl` clusters (host): each
 // unit, in the launch's order (longest first), goes to the cluster with the

@@ -57,6 +57,31 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
   s = t;
 }
 
+// Sum of squares of 8 bf16 values packed in a 16-byte vector.
+__device__ __forceinline__ float sumsq_bf16x8(const uint4& w) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+  float s8 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(u[i] << 16), hi = __uint_as_float(u[i] & 0xFFFF0000u);
+    s8 = fmaf(lo, lo, s8);
+    s8 = fmaf(hi, hi, s8);
+  }
+  return s8;
+}
+
+__device__ __forceinline__ float sumsq_f32x4(const float4& w) {
+  float s4 = w.x * w.x;
+  s4 = fmaf(w.y, w.y, s4);
+  s4 = fmaf(w.z, w.z, s4);
+  return fmaf(w.w, w.w, s4);
+}
+
+// One block per 64 Ki-element chunk (grid-stride). Where a tensor's pointer is
+// 16-byte aligned (every chunk of it then is too: a chunk is 128 KiB of bf16
+// or 256 KiB of fp32), its elements are read as 16-byte vectors, four in
+// flight per thread; the rest of the chunk, and unaligned tensors, element by
+// element.
 __global__ void __launch_bounds__(kNoAllocThreads) noalloc_sumsq_kernel(const __grid_constant__ NoAllocTensors T,
                                                                         float* __restrict__ partials) {
   __shared__ double sh[kNoAllocThreads / 32];
@@ -67,16 +92,39 @@ __global__ void __launch_bounds__(kNoAllocThreads) noalloc_sumsq_kernel(const __
     const int64_t first = (t == 0) ? 0 : T.chunk_end[t - 1];
     const int64_t begin = (int64_t)(c - first) * kChunk;
     const int64_t end = begin + kChunk < T.numel[t] ? begin + kChunk : T.numel[t];
+    const bool vec = (reinterpret_cast<uintptr_t>(T.ptr[t]) & 15) == 0;
     if (T.dtype[t] == MA_DT_BF16) {
       const uint16_t* g = static_cast<const uint16_t*>(T.ptr[t]);
-      for (int64_t i = begin + threadIdx.x; i < end; i += kNoAllocThreads) {
-        const float x = __uint_as_float(((uint32_t)g[i]) << 16);
+      const int64_t nv = vec ? (end - begin) / 8 : 0;  // vectors of 8 from `begin`
+      const uint4* gv = reinterpret_cast<const uint4*>(g + begin);
+      int64_t i = threadIdx.x;
+      for (; i + 3 * kNoAllocThreads < nv; i += 4 * kNoAllocThreads) {
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) w[u] = __ldg(gv + i + u * kNoAllocThreads);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) kahan_add(s, comp, sumsq_bf16x8(w[u]));
+      }
+      for (; i < nv; i += kNoAllocThreads) kahan_add(s, comp, sumsq_bf16x8(__ldg(gv + i)));
+      for (int64_t j = begin + nv * 8 + threadIdx.x; j < end; j += kNoAllocThreads) {
+        const float x = __uint_as_float(((uint32_t)g[j]) << 16);
         kahan_add(s, comp, x * x);
       }
     } else {
       const float* g = static_cast<const float*>(T.ptr[t]);
-      for (int64_t i = begin + threadIdx.x; i < end; i += kNoAllocThreads) {
-        const float x = g[i];
+      const int64_t nv = vec ? (end - begin) / 4 : 0;  // vectors of 4 from `begin`
+      const float4* gv = reinterpret_cast<const float4*>(g + begin);
+      int64_t i = threadIdx.x;
+      for (; i + 3 * kNoAllocThreads < nv; i += 4 * kNoAllocThreads) {
+        float4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) w[u] = __ldg(gv + i + u * kNoAllocThreads);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) kahan_add(s, comp, sumsq_f32x4(w[u]));
+      }
+      for (; i < nv; i += kNoAllocThreads) kahan_add(s, comp, sumsq_f32x4(__ldg(gv + i)));
+      for (int64_t j = begin + nv * 4 + threadIdx.x; j < end; j += kNoAllocThreads) {
+        const float x = g[j];
         kahan_add(s, comp, x * x);
       }
     }

@@ -181,6 +181,35 @@ __global__ void __launch_bounds__(kClipThreads) clip_finalize_kernel(const float
 }
 
 // ---------------------------------------------------------------------------
+// Sharded step: this rank's sum of squares (fp64) from its partials, and the
+// norm and clip coefficient from the sum over all ranks.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kClipThreads) sumsq_partials_kernel(const float* __restrict__ partials, int n,
+                                                                      double* __restrict__ out) {
+  __shared__ double sh[kClipThreads / 32];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < n; i += kClipThreads) s += (double)partials[i];
+  const double tot = block_sum_double<kClipThreads>(s, sh);
+  if (threadIdx.x == 0) *out = tot;
+}
+
+__global__ void clip_from_sumsq_kernel(const double* __restrict__ sumsq, float max_norm, float clip_eps,
+                                       StepScalars* __restrict__ out) {
+  const double total = sqrt(*sumsq);
+  double coef;
+  if (isnan(total)) {
+    coef = total;
+  } else if (max_norm > 0.f) {
+    coef = (double)max_norm / (total + (double)clip_eps);
+    if (coef > 1.0) coef = 1.0;
+  } else {
+    coef = 1.0;
+  }
+  out->total = (float)total;
+  out->coef = (float)coef;
+}
+
+// ---------------------------------------------------------------------------
 // Muon momentum + canonical bf16 pack.
 // One tile of one parameter per iteration (64 x 64 for tall matrices, 16
 // rows x 256 columns otherwise, so that a warp streams 1 KB row segments);
@@ -416,6 +445,14 @@ void launch_grad_sumsq(const GradChunk* chunks, int nchunks, float* partials, in
 void launch_clip_finalize(const float* partials, int n, float max_norm, float clip_eps, StepScalars* out,
                           cudaStream_t st) {
   clip_finalize_kernel<<<1, kClipThreads, 0, st>>>(partials, n, max_norm, clip_eps, out);
+}
+
+void launch_sumsq_partials(const float* partials, int n, double* out, cudaStream_t st) {
+  sumsq_partials_kernel<<<1, kClipThreads, 0, st>>>(partials, n, out);
+}
+
+void launch_clip_from_sumsq(const double* sumsq, float max_norm, float clip_eps, StepScalars* out, cudaStream_t st) {
+  clip_from_sumsq_kernel<<<1, 1, 0, st>>>(sumsq, max_norm, clip_eps, out);
 }
 
 void launch_muon_momentum(const MomTile* tiles, int ntiles, const MuonMat* mats, const StepScalars* sc,
