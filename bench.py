@@ -53,13 +53,14 @@ STREAM_KINDS = ("grad_norm", "momentum", "adamw")
 
 
 # DRAM bytes per ns_tc_kernel launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# capture of the 6-layer case of this workload (the ns_tc_kernel summary in profiles/: the 12 launches
-# of iterations 2-5 of one step, averaged per product), weighted over a step's 15 launches (5 X X^T,
-# 5 A A, 4 B X, 1 last) and scaled to the 16-layer h1024 workload by the matrices processed (16/6:
-# each launch reads its operands once and writes its output once). It describes only the kernel
-# sources it was measured on: any change to them makes it null until it is measured again.
-NS_TRAFFIC = {"sources_sha256": "6634fe8ec9f0be1a816b6dbd71d0f7724bab4e5e0cb5ee3bf737b6c7b2aaa8f0",
-              "bytes_per_launch": 887316082, "workload": "h1024"}
+# capture of a 3-layer case of the full_vla expert (expert:2048:8192:3:fp32_mixed: the same matrix
+# shapes and policy; the ns_tc_kernel summary in profiles/): the 15 launches of one step (5 X X^T,
+# 5 A A, 4 B X, 1 last) averaged, 728.8 MB, and scaled to the 24-layer expert by the matrices
+# processed (x 8: each launch reads its operands and writes its output once per matrix). It describes
+# only the kernel sources it was measured on: any change to them makes it null until it is measured
+# again.
+NS_TRAFFIC = {"sources_sha256": "f5d2f3a841e1d9fd76795a2d820458f58c4a2dcef6b97908ce8b844d8ba0644d",
+              "bytes_per_launch": 5830297463, "workload": "full_vla"}
 NS_SOURCES = ("ns_tc.cu", "ns_epilogue.cuh", "internal.h")
 
 

@@ -190,13 +190,18 @@ WORKLOADS = tuple(_BUILDERS)
 
 
 def get_workload(name: str) -> Workload:
-    """A named workload, or ``expert:<hidden>:<mlp>:<layers>`` for an action
-    expert of that size built like h1024 (bf16 grads with the rank-8 part,
-    bf16_mixed policy)."""
+    """A named workload, or ``expert:<hidden>:<mlp>:<layers>[:<policy>]`` for
+    an action expert of that size built like h1024 (bf16 grads with the
+    rank-8 part; policy bf16_mixed unless ``fp32_mixed`` is given, as the
+    2048-hidden expert of h2048 and full_vla uses)."""
     if name.startswith("expert:"):
-        hidden, mlp, layers = (int(x) for x in name.split(":")[1:4])
+        parts = name.split(":")[1:]
+        hidden, mlp, layers = (int(x) for x in parts[:3])
+        policy = parts[3] if len(parts) > 3 else "bf16_mixed"
+        if policy not in ("bf16_mixed", "fp32_mixed"):
+            raise KeyError(f"unknown policy {policy!r} in {name!r}")
         t = _expert_layers(hidden, mlp, layers, rank8=True) + _expert_vectors(hidden, layers)
-        return Workload(name, tuple(t), policy="bf16_mixed", grad_dtype="bf16", steps=10, lr=BASE_LR)
+        return Workload(name, tuple(t), policy=policy, grad_dtype="bf16", steps=10, lr=BASE_LR)
     try:
         return _BUILDERS[name]()
     except KeyError:
