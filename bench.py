@@ -448,20 +448,27 @@ def run_ours(args):
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
+    # CUDA events on the copy stream around every copy: each copy's own duration
+    cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     gc.disable()  # no collector pause inside the host-timed loop
     t0 = time.perf_counter()
     with torch.cuda.stream(copy_stream):
+        cev[0][0].record(copy_stream)
         gflat.copy_(hflat, non_blocking=True)  # step 1's gradients
+        cev[0][1].record(copy_stream)
     for k in range(args.steps):
         stream.wait_event(copy_stream.record_event())
         opt.step(lr)
         if k + 1 < args.steps:
             copy_stream.wait_event(opt.record_grads_consumed())
             with torch.cuda.stream(copy_stream):
+                cev[k + 1][0].record(copy_stream)
                 gflat.copy_(hflat, non_blocking=True)  # step k+2's gradients
+                cev[k + 1][1].record(copy_stream)
         mx.muon_adamw_last_norm(opt.handle)  # synchronises and reads this step's norm
     e2e_s = time.perf_counter() - t0
     gc.enable()
+    copy_ms = statistics.median(a.elapsed_time(b) for a, b in cev)
     e2e_s = max_over_ranks(e2e_s, dist, dev)
 
     peaks = load_peaks()
@@ -553,6 +560,8 @@ def run_ours(args):
         "clocks": clk,
         "e2e": {"value": round(args.steps * world / e2e_s, 3), "unit": "steps/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": d2h,
+                "gradient_copy_ms_median": round(copy_ms, 3),
+                "gradient_copy_gbs": round(total * gflat.element_size() / (copy_ms / 1e3) / 1e9, 1),
                 "how": "every step: every gradient copied host->device from pinned memory (one copy of the "
                        "flat gradient buffer, issued once the previous step has read its gradients and "
                        "overlapping that step's Newton-Schulz chain), muon_adamw_step, and the step's norm "
