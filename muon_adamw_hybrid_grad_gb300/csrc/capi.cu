@@ -610,6 +610,8 @@ ma_status build_plan(muon_adamw* h) {
         p.pmaps = h->d_pmaps + 2 * (size_t)B.mat0;
         p.first = it == 0;
         p.last = it == steps - 1;
+        p.shadow = 0;
+        for (int pi : B.params) p.shadow |= h->params[pi].shadow != nullptr ? 1 : 0;
         if (kind == NS_GRAM) {
           p.P = Xcur;
           p.Q = Xcur;
@@ -668,6 +670,7 @@ ma_status build_plan(muon_adamw* h) {
             L.total_tiles = tiles_total;
             L.err = h->d_err;
             L.cl = cl;
+            for (int q = 0; q < L.nprob; ++q) L.shadow |= L.prob[q].p.shadow;
             h->tc[kind][it].push_back(L);
           }
         }

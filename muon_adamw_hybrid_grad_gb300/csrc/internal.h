@@ -137,6 +137,7 @@ struct NsProblem {
   int32_t M, N, K;
   int32_t nmat;
   int32_t first, last;  // first / last Newton-Schulz iteration
+  int32_t shadow;       // some matrix of the bucket has a bf16 shadow
 };
 
 // ---- the thread-local message behind muon_adamw_last_error() (capi.cu) ----
@@ -192,6 +193,7 @@ struct TcLaunch {
   int32_t nclusters;    // clusters in the grid
   int32_t cl;           // CTAs per cluster: 1, or 2 (a CTA pair running cta_group::2 MMAs)
   int32_t stall_test;   // test hook: CTA 0's producer issues no loads (its waits then run out)
+  int32_t shadow;       // some matrix of the launch writes a bf16 shadow (the last iteration keeps shadow tiles)
 };
 // TMA maps of one parameter for the last iteration's write-back: maps[0] the
 // fp32 master, maps[1] the bf16 shadow (unused without one); 32 x 32 boxes.

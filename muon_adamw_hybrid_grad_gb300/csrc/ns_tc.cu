@@ -76,14 +76,17 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 // last iteration's variant (APPLY) trades operand stages for two parameter
 // blocks per epilogue warp, into which p is fetched by TMA ahead of use.
 //   [stages][APPLY: 2 fp32 blocks per epilogue warp][bf16 tiles per epilogue warp][mbarriers, TMEM slot, flag]
-template <bool PAIR, bool APPLY>
+// Without bf16 shadows (SHADOW false) the last iteration's variant needs no
+// shadow tiles, and its paired ring gets a fifth stage in their place.
+template <bool PAIR, bool APPLY, bool SHADOW = true>
 struct Smem {
   static constexpr int STAGE = A_STAGE + (PAIR ? B_STAGE / 2 : B_STAGE);
-  static constexpr int STAGES = PAIR ? (APPLY ? 4 : 6) : (APPLY ? 3 : 4);
+  static constexpr int STAGES = PAIR ? (APPLY ? (SHADOW ? 4 : 5) : 6) : (APPLY ? 3 : 4);
   static constexpr size_t PBUF = (size_t)STAGES * STAGE;
   static constexpr size_t SB = PBUF + (APPLY ? (size_t)EPI_WARPS * 2 * PBLOCK_BYTES : 0);
-  // bf16 tiles per epilogue warp: APPLY the shadow tile; otherwise a row tile and a column tile
-  static constexpr size_t SB_PER_WARP = APPLY ? 2048 : 4096;
+  // bf16 tiles per epilogue warp: APPLY the shadow tile (none without shadows); otherwise a row
+  // tile and a column tile
+  static constexpr size_t SB_PER_WARP = APPLY ? (SHADOW ? 2048 : 0) : 4096;
   static constexpr size_t BARS = SB + (size_t)EPI_WARPS * SB_PER_WARP;
   // full[S], empty[S], tmem full[2], tmem empty[2], drain, APPLY: parameter blocks [2 per epilogue warp]
   static constexpr int NBARS = 2 * STAGES + 5 + (APPLY ? 2 * EPI_WARPS : 0);
@@ -555,7 +558,7 @@ __device__ __forceinline__ void apply_block_direct(const MuonMat& M, const NsEpi
 // row = TMEM lane) and the column-per-lane ones (tall parameters, parameter
 // column = TMEM lane) free of bank conflicts. Matrices without maps take
 // apply_block_direct.
-template <int CL, bool PAIR>
+template <int CL, bool PAIR, bool SHADOW>
 __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem, size_t pbuf_off, size_t sb_off,
                                                uint32_t pbar_base, uint32_t tmem_base, uint32_t tfull0,
                                                uint32_t tempty0, volatile int* abort_flag, int warp, int lane,
@@ -565,7 +568,7 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
   const int half = w8 >> 2;
   uint8_t* const pb = smem + pbuf_off + (size_t)w8 * 2 * PBLOCK_BYTES;
   const uint32_t pb_s = smem_u32(pb);
-  uint8_t* const shb = smem + sb_off + (size_t)w8 * Smem<PAIR, true>::SB_PER_WARP;
+  uint8_t* const shb = smem + sb_off + (size_t)w8 * Smem<PAIR, true, SHADOW>::SB_PER_WARP;
   const uint32_t shb_s = smem_u32(shb);
   const uint32_t bar0 = pbar_base + 16u * (uint32_t)w8;
   const NsEpiArgs& ep = L.epi;
@@ -586,7 +589,7 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
     const int colw = c.tj * P.bn + 32 * half;       // canonical column of block 0; block k at +64k
     const bool tma = M.tma != 0;
     const bool tr = M.transposed != 0;
-    const bool has_shadow = M.shadow != nullptr;
+    const bool has_shadow = SHADOW && M.shadow != nullptr;
     const int s = M.s, l = M.l;
     const CUtensorMap* maps = P.p.pmaps + 2 * c.mat;
     if (tma) {
@@ -730,11 +733,11 @@ __device__ __forceinline__ void apply_epilogue(const TcLaunch& L, uint8_t* smem,
 // leader's barrier. Used where the right-hand operand is K-major (X X^T, A A)
 // and for the last iteration. No operand tile is ever multicast: each CTA
 // loads exactly the bytes its own shared memory holds.
-template <int CL, bool APPLY, bool PAIR>
+template <int CL, bool APPLY, bool PAIR, bool SHADOW = true>
 __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant__ TcLaunch L) {
   static_assert(PAIR == (CL == 2), "a cluster of two CTAs runs the paired MMA");
   constexpr int G = PAIR ? 2 : 1;  // tcgen05 cta_group
-  using SM = Smem<PAIR, APPLY>;
+  using SM = Smem<PAIR, APPLY, SHADOW>;
   static_assert((SM::BYTES >> 4) < 0x4000, "operand descriptors: 14-bit address field");
   constexpr int STAGES = SM::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -951,7 +954,7 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
     }
   } else if (APPLY) {
     // ---------------- epilogue of the last iteration ----------------
-    apply_epilogue<CL, PAIR>(L, smem, SM::PBUF, SM::SB, smem_u32(bars + 2 * STAGES + 5), tmem_base, tfull0, tempty0,
+    apply_epilogue<CL, PAIR, SHADOW>(L, smem, SM::PBUF, SM::SB, smem_u32(bars + 2 * STAGES + 5), tmem_base, tfull0, tempty0,
                        abort_flag, warp, lane, crank, unit0, nunits);
   } else {
     // ---------------- epilogue ----------------
@@ -1469,13 +1472,13 @@ bool tc_encode_param_maps(CUtensorMap* maps, const MuonMat& M) {
 }
 
 namespace {
-template <int CL, bool APPLY, bool PAIR>
+template <int CL, bool APPLY, bool PAIR, bool SHADOW = true>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(ns_tc_kernel<CL, APPLY, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)Smem<PAIR, APPLY>::BYTES);
+  return cudaFuncSetAttribute(ns_tc_kernel<CL, APPLY, PAIR, SHADOW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)Smem<PAIR, APPLY, SHADOW>::BYTES);
 }
 
-template <bool APPLY, bool PAIR>
+template <bool APPLY, bool PAIR, bool SHADOW = true>
 cudaError_t max_pairs_of(int* n) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -1485,13 +1488,13 @@ cudaError_t max_pairs_of(int* n) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Smem<PAIR, APPLY>::BYTES;
+  cfg.dynamicSmemBytes = Smem<PAIR, APPLY, SHADOW>::BYTES;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, ns_tc_kernel<2, APPLY, PAIR>, &cfg);
+  return cudaOccupancyMaxActiveClusters(n, ns_tc_kernel<2, APPLY, PAIR, SHADOW>, &cfg);
 }
 
-template <bool APPLY, bool PAIR>
+template <bool APPLY, bool PAIR, bool SHADOW = true>
 cudaError_t launch_pair(const TcLaunch& L, int grid_units, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -1503,11 +1506,11 @@ cudaError_t launch_pair(const TcLaunch& L, int grid_units, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(2 * grid_units, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Smem<PAIR, APPLY>::BYTES;
+  cfg.dynamicSmemBytes = Smem<PAIR, APPLY, SHADOW>::BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, ns_tc_kernel<2, APPLY, PAIR>, L);
+  return cudaLaunchKernelEx(&cfg, ns_tc_kernel<2, APPLY, PAIR, SHADOW>, L);
 }
 }  // namespace
 
@@ -1517,13 +1520,16 @@ cudaError_t ns_tc_prepare(int* max_pairs) {
   if ((e = set_smem_attr<1, true, false>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<2, false, true>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<2, true, true>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<2, true, true, false>()) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)SmallSmem::BYTES)) != cudaSuccess)
     return e;
-  int a = 0, c = 0;
+  int a = 0, c = 0, d = 0;
   if ((e = max_pairs_of<false, true>(&a)) != cudaSuccess) return e;
   if ((e = max_pairs_of<true, true>(&c)) != cudaSuccess) return e;
-  *max_pairs = a < c ? a : c;
+  if ((e = max_pairs_of<true, true, false>(&d)) != cudaSuccess) return e;
+  const int m = a < c ? a : c;
+  *max_pairs = m < d ? m : d;
   return cudaSuccess;
 }
 
@@ -1560,7 +1566,7 @@ cudaError_t launch_ns_tc(const TcLaunch& L, cudaStream_t st) {
     return apply ? cudaLaunchKernelEx(&cfg, ns_tc_kernel<1, true, false>, L)
                  : cudaLaunchKernelEx(&cfg, ns_tc_kernel<1, false, false>, L);
   }
-  if (apply) return launch_pair<true, true>(L, grid_units, st);
+  if (apply) return L.shadow ? launch_pair<true, true>(L, grid_units, st) : launch_pair<true, true, false>(L, grid_units, st);
   return launch_pair<false, true>(L, grid_units, st);
 }
 
