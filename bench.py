@@ -55,12 +55,12 @@ STREAM_KINDS = ("grad_norm", "momentum", "adamw")
 # DRAM bytes per ns_tc_kernel launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of a 3-layer case of the full_vla expert (expert:2048:8192:3:fp32_mixed: the same matrix
 # shapes and policy; the ns_tc_kernel summary in profiles/): the 15 launches of one step (5 X X^T,
-# 5 A A, 4 B X, 1 last) averaged, 728.8 MB, and scaled to the 24-layer expert by the matrices
+# 5 A A, 4 B X, 1 last) averaged, 726.0 MB, and scaled to the 24-layer expert by the matrices
 # processed (x 8: each launch reads its operands and writes its output once per matrix). It describes
 # only the kernel sources it was measured on: any change to them makes it null until it is measured
 # again.
-NS_TRAFFIC = {"sources_sha256": "f5d2f3a841e1d9fd76795a2d820458f58c4a2dcef6b97908ce8b844d8ba0644d",
-              "bytes_per_launch": 5830297463, "workload": "full_vla"}
+NS_TRAFFIC = {"sources_sha256": "0f1f944f8c3f1433b90ebcb4ffd81f047facc938a6e601e5fbc6dd107d31d0ee",
+              "bytes_per_launch": 5807824896, "workload": "full_vla"}
 NS_SOURCES = ("ns_tc.cu", "ns_epilogue.cuh", "internal.h")
 
 
@@ -448,8 +448,11 @@ def run_ours(args):
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    # CUDA events on the copy stream around every copy: each copy's own duration
+    # CUDA events on the copy stream around every copy (each copy's own
+    # duration), and at each step's start on the optimizer's stream (when,
+    # within the previous step, the next copy began)
     cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     gc.disable()  # no collector pause inside the host-timed loop
     t0 = time.perf_counter()
     with torch.cuda.stream(copy_stream):
@@ -458,6 +461,7 @@ def run_ours(args):
         cev[0][1].record(copy_stream)
     for k in range(args.steps):
         stream.wait_event(copy_stream.record_event())
+        sev[k].record(stream)
         opt.step(lr)
         if k + 1 < args.steps:
             copy_stream.wait_event(opt.record_grads_consumed())
@@ -466,9 +470,15 @@ def run_ours(args):
                 gflat.copy_(hflat, non_blocking=True)  # step k+2's gradients
                 cev[k + 1][1].record(copy_stream)
         mx.muon_adamw_last_norm(opt.handle)  # synchronises and reads this step's norm
+    sev[args.steps].record(stream)
     e2e_s = time.perf_counter() - t0
     gc.enable()
+    torch.cuda.synchronize()
     copy_ms = statistics.median(a.elapsed_time(b) for a, b in cev)
+    # for steps 1..K-1: when the next step's copy started and ended, after the step's start
+    copy_start = [sev[k].elapsed_time(cev[k + 1][0]) for k in range(args.steps - 1)]
+    copy_end = [sev[k].elapsed_time(cev[k + 1][1]) for k in range(args.steps - 1)]
+    step_dev = [sev[k].elapsed_time(sev[k + 1]) for k in range(args.steps)]
     e2e_s = max_over_ranks(e2e_s, dist, dev)
 
     peaks = load_peaks()
@@ -562,6 +572,9 @@ def run_ours(args):
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": d2h,
                 "gradient_copy_ms_median": round(copy_ms, 3),
                 "gradient_copy_gbs": round(total * gflat.element_size() / (copy_ms / 1e3) / 1e9, 1),
+                "next_copy_start_ms_median": round(statistics.median(copy_start), 3) if copy_start else None,
+                "next_copy_end_ms_median": round(statistics.median(copy_end), 3) if copy_end else None,
+                "step_ms_median": round(statistics.median(step_dev), 3),
                 "how": "every step: every gradient copied host->device from pinned memory (one copy of the "
                        "flat gradient buffer, issued once the previous step has read its gradients and "
                        "overlapping that step's Newton-Schulz chain), muon_adamw_step, and the step's norm "
