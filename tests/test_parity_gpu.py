@@ -72,6 +72,38 @@ def test_ragged_shapes_and_chunk_tails(mx, ns_kernel):
     assert r["worst_o"] <= O_TOL
 
 
+def _random_shapes_workload(policy):
+    """Seeded random matrix shapes (1..699 per side) that reach every
+    Newton-Schulz path: narrow fp32 (short side < 64), the fused small-matrix
+    kernel, single-CTA and paired tensor-core launches; plus AdamW vectors of
+    random lengths across chunk boundaries."""
+    rng = np.random.default_rng(20261202)
+    t = []
+    for k in range(14):
+        m, n = int(rng.integers(1, 700)), int(rng.integers(1, 700))
+        t.append(TensorSpec(f"model.action_expert.layers.{k}.mlp.w{k}.weight", (m, n), rank8=True))
+    for k in range(6):
+        t.append(TensorSpec(f"model.vlm.layers.{k}.norm.weight", (int(rng.integers(1, 200000)),)))
+    return workloads.custom_workload(f"random_{policy}", t, policy=policy, steps=2)
+
+
+@pytest.mark.parametrize("policy", ["bf16_mixed", "fp32_mixed"])
+def test_random_shapes_every_path(mx, policy):
+    w = _random_shapes_workload(policy)
+    r = run_parity(w)
+    assert r["worst_o"] <= O_TOL
+    gpu = GpuSide(w, workloads.master_weights(w))
+    try:
+        gpu.load_grads(workloads.gradients(w, 1))
+        gpu.mx.muon_adamw_set_profiling(gpu.opt.handle, True)
+        gpu.step(w.lr)
+        prof = gpu.opt.profile()
+        for k in ("ns_narrow", "ns_fused", "ns_gram", "ns_poly", "ns_update", "ns_apply"):
+            assert prof[k]["launches"] > 0, k
+    finally:
+        gpu.close()
+
+
 def test_without_cta_clusters(mx):
     """Cross-check switch: every Newton-Schulz product on single CTAs
     (cta_group::1) instead of CTA pairs, against the oracle."""
