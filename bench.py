@@ -459,6 +459,7 @@ def run_ours(args):
         cev[0][0].record(copy_stream)
         gflat.copy_(hflat, non_blocking=True)  # step 1's gradients
         cev[0][1].record(copy_stream)
+    host_t = [t0]
     for k in range(args.steps):
         stream.wait_event(copy_stream.record_event())
         sev[k].record(stream)
@@ -470,6 +471,7 @@ def run_ours(args):
                 gflat.copy_(hflat, non_blocking=True)  # step k+2's gradients
                 cev[k + 1][1].record(copy_stream)
         mx.muon_adamw_last_norm(opt.handle)  # synchronises and reads this step's norm
+        host_t.append(time.perf_counter())
     sev[args.steps].record(stream)
     e2e_s = time.perf_counter() - t0
     gc.enable()
@@ -479,6 +481,7 @@ def run_ours(args):
     copy_start = [sev[k].elapsed_time(cev[k + 1][0]) for k in range(args.steps - 1)]
     copy_end = [sev[k].elapsed_time(cev[k + 1][1]) for k in range(args.steps - 1)]
     step_dev = [sev[k].elapsed_time(sev[k + 1]) for k in range(args.steps)]
+    step_host = [(host_t[k + 1] - host_t[k]) * 1e3 for k in range(args.steps)]
     e2e_s = max_over_ranks(e2e_s, dist, dev)
 
     peaks = load_peaks()
@@ -575,6 +578,9 @@ def run_ours(args):
                 "next_copy_start_ms_median": round(statistics.median(copy_start), 3) if copy_start else None,
                 "next_copy_end_ms_median": round(statistics.median(copy_end), 3) if copy_end else None,
                 "step_ms_median": round(statistics.median(step_dev), 3),
+                "step_ms_max": round(max(step_dev), 3),
+                "host_step_ms_median": round(statistics.median(step_host), 3),
+                "host_step_ms_max": round(max(step_host), 3),
                 "how": "every step: every gradient copied host->device from pinned memory (one copy of the "
                        "flat gradient buffer, issued once the previous step has read its gradients and "
                        "overlapping that step's Newton-Schulz chain), muon_adamw_step, and the step's norm "
