@@ -579,6 +579,8 @@ def run_ours(args):
                 "next_copy_end_ms_median": round(statistics.median(copy_end), 3) if copy_end else None,
                 "step_ms_median": round(statistics.median(step_dev), 3),
                 "step_ms_max": round(max(step_dev), 3),
+                "step_max_index": int(max(range(len(step_dev)), key=lambda k: step_dev[k])),
+                "gradient_copy_ms_max": round(max(a.elapsed_time(b) for a, b in cev), 3),
                 "host_step_ms_median": round(statistics.median(step_host), 3),
                 "host_step_ms_max": round(max(step_host), 3),
                 "how": "every step: every gradient copied host->device from pinned memory (one copy of the "
