@@ -1,8 +1,9 @@
-"""The sharded step on one GPU: two handles act as ranks 0 and 1 of two, one
-after the other on the same stream (no kernel waits for another). Each has
-its own copy of the parameters and reads the same gradients; the host sums
-their local sums of squares (what an all-reduce does) and copies each rank's
-updated parts to the other (what the exchange does). Checked against the
+"""The sharded step on one GPU: two or three handles act as the ranks of a
+world of that size, one after the other on the same stream (no kernel waits
+for another). Each has its own copy of the parameters and reads the same
+gradients; the host sums their local sums of squares (what an all-reduce
+does) and copies each rank's updated parts to the others (what the exchange
+does). Checked against the
 fp64 oracle's whole step at the parity suite's tolerances: the norm, O of
 every Muon matrix, AdamW p, m and v (each rank's state holds its range), the
 bf16 shadows; each rank's local sum of squares against the fp64 sum over the
@@ -39,11 +40,11 @@ def _workload():
     return workloads.custom_workload("tiny_shard", t, policy="bf16_mixed", steps=2)
 
 
-def test_sharded_step_two_ranks_on_one_gpu(mx):
+@pytest.mark.parametrize("world", [2, 3])
+def test_sharded_step_ranks_on_one_gpu(mx, world):
     import torch
 
     w = _workload()
-    world = 2
     dev = torch.device("cuda")
     n = len(w.tensors)
     names = [t.name for t in w.tensors]
@@ -56,7 +57,7 @@ def test_sharded_step_two_ranks_on_one_gpu(mx):
                          precision=mx.MA_BF16_MIXED) for r in range(world)]
     try:
         ranges = opts[0].shard_ranges()
-        assert ranges == opts[1].shard_ranges()
+        assert all(o.shard_ranges() == ranges for o in opts[1:])
         groups = opts[0].groups
         orc = oracle.HybridOracle(names, shapes)
         assert orc.groups == groups
@@ -73,7 +74,7 @@ def test_sharded_step_two_ranks_on_one_gpu(mx):
             local = [torch.zeros(1, dtype=torch.float64, device=dev) for _ in range(world)]
             for r in range(world):
                 opts[r].step_begin(w.lr, local[r])
-            total = local[0] + local[1]
+            total = sum(local[1:], local[0].clone())
             norms = [opts[r].step_end(total, want_norm=True) for r in range(world)]
             m_prev = dict(orc.m)
             res = orc.step(orc_p, grads, w.lr)
@@ -100,7 +101,7 @@ def test_sharded_step_two_ranks_on_one_gpu(mx):
             coef = res["coef"]
             for i in range(n):
                 p_gpu = P[0][i].cpu().numpy()
-                assert np.array_equal(p_gpu, P[1][i].cpu().numpy())
+                assert all(np.array_equal(p_gpu, P[r][i].cpu().numpy()) for r in range(1, world))
                 assert np.array_equal(S[0][i].float().cpu().numpy(), workloads.bf16_round(p_gpu)), names[i]
                 if groups[i] == "muon":
                     m_, n_ = shapes[i]
