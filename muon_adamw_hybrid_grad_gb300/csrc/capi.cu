@@ -108,7 +108,8 @@ struct Bucket {
   uint16_t *X0 = nullptr, *X1 = nullptr, *A = nullptr, *B = nullptr;
   bool fused = false;   // small matrices: the whole Newton-Schulz in one launch (ns_small_kernel)
   bool narrow = false;  // short side < kNarrowMinS: fp32 Newton-Schulz (ns_narrow_kernel)
-  float* XF = nullptr;  // narrow: fp32 X of each slot (S x L floats per slot)
+  float* XF = nullptr;  // narrow: fp32 X of each slot (xf_stride floats per slot)
+  size_t xf_stride = 0;  // narrow: the bucket's largest m n, rounded up to 64 floats
 };
 
 struct ProfRec {
@@ -181,8 +182,7 @@ struct muon_adamw {
   std::vector<SmallLaunch> small;      // one per fused bucket
   std::vector<double> small_units;     // their symmetric flops per step
   double unit_fused = 0;               // symmetric flops per step of all fused buckets
-  std::vector<NarrowLaunch> narrow;    // one per narrow bucket
-  std::vector<double> narrow_units;    // their symmetric flops per step
+  std::vector<NarrowLaunch> narrow;    // one launch over every narrow bucket (or none)
   double unit_narrow = 0;              // symmetric flops per step of all narrow buckets
   std::vector<std::vector<NsProblem>> simt[3];
   double unit_gram = 0, unit_poly = 0, unit_update = 0;  // symmetric flops per iteration (all buckets)
@@ -304,7 +304,7 @@ ma_status build_plan(muon_adamw* h) {
     if (p.group == MA_GROUP_MUON) h->muon_params.push_back(i);
     if (p.group == MA_GROUP_ADAMW) h->adam_params.push_back(i);
   }
-  // --- buckets (by padded canonical shape and narrowness, first-seen order) ---
+  // --- buckets (by padded canonical shape and narrowness, first-seen order; narrow ones moved first below) ---
   std::map<std::pair<std::pair<int, int>, bool>, int> bidx;
   h->buckets.clear();
   for (int pi : h->muon_params) {
@@ -328,6 +328,19 @@ ma_status build_plan(muon_adamw* h) {
   for (Bucket& B : h->buckets)
     B.fused = c.ns_kernel == MA_NS_TCGEN05 && !(c.reserved[0] & 8) && !B.narrow && B.S == 128 &&
               B.L <= kSmallMaxL;
+  // narrow buckets first, the costliest (S^2 L) first: their matrices are then
+  // one contiguous, largest-first run of the matrix table, which a single
+  // ns_narrow_kernel launch takes (the other buckets keep their order)
+  std::stable_sort(h->buckets.begin(), h->buckets.end(), [](const Bucket& a, const Bucket& b) {
+    if (a.narrow != b.narrow) return a.narrow;
+    return a.narrow && (double)a.S * a.S * a.L > (double)b.S * b.S * b.L;
+  });
+  for (Bucket& B : h->buckets) {
+    if (!B.narrow) continue;
+    int64_t mx = 0;
+    for (int pi : B.params) mx = std::max(mx, h->params[pi].numel);
+    B.xf_stride = (size_t)((mx + 63) / 64 * 64);
+  }
   // --- sizes ---
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
@@ -352,7 +365,7 @@ ma_status build_plan(muon_adamw* h) {
     const Bucket& B = h->buckets[b];
     const size_t nb = B.params.size();
     const size_t xs = al(nb * (size_t)B.S * B.L * 2), as = al(nb * (size_t)B.S * B.S * 2);
-    const size_t sizes[4] = {xs, B.narrow ? al(nb * (size_t)B.S * B.L * 4) : xs, B.narrow ? 0 : as,
+    const size_t sizes[4] = {xs, B.narrow ? al(nb * B.xf_stride * 4) : xs, B.narrow ? 0 : as,
                              B.narrow ? 0 : as};
     for (int q = 0; q < 4; ++q) {
       ws_off[4 * b + q] = off;
@@ -510,7 +523,6 @@ ma_status build_plan(muon_adamw* h) {
   int mat_index = 0;
   h->unit_gram = h->unit_poly = h->unit_update = h->dense_flops = h->unit_fused = h->unit_narrow = 0;
   h->small_units.clear();
-  h->narrow_units.clear();
   for (size_t b = 0; b < h->buckets.size(); ++b) {
     Bucket& B = h->buckets[b];
     B.mat0 = mat_index;
@@ -537,7 +549,7 @@ ma_status build_plan(muon_adamw* h) {
                (reinterpret_cast<uintptr_t>(p.shadow) % 16 == 0);
       M.lr_mult = (float)(p.lr_scale * c.muon_lr_scale * c.moonlight_coef * sqrt((double)M.l));
       M.group = p.og;
-      M.xf = B.narrow ? B.XF + slot * (size_t)B.S * B.L : nullptr;
+      M.xf = B.narrow ? B.XF + slot * B.xf_stride : nullptr;
       pmaps.resize(2 * (size_t)(mat_index + 1));
       M.tma = (c.ns_kernel == MA_NS_TCGEN05 && !(c.reserved[0] & 4) &&
                tc_encode_param_maps(&pmaps[2 * (size_t)mat_index], M))
@@ -566,7 +578,6 @@ ma_status build_plan(muon_adamw* h) {
       h->small_units.push_back(bucket_units);
       h->unit_fused += bucket_units;
     } else if (B.narrow) {
-      h->narrow_units.push_back(bucket_units);
       h->unit_narrow += bucket_units;
     }
   }
@@ -678,27 +689,33 @@ ma_status build_plan(muon_adamw* h) {
     }
   }
   h->narrow.clear();
-  for (Bucket& B : h->buckets) {
-    if (!B.narrow) continue;
-    NarrowLaunch nl;
-    memset(&nl, 0, sizeof nl);
-    nl.mats = h->d_mats + B.mat0;
-    nl.sc = h->d_scalars;
-    nl.sp = h->d_step;
-    nl.nmat = (int)B.params.size();
-    nl.steps = c.ns_steps;
-    nl.nesterov = c.muon_nesterov;
-    nl.mu = (float)c.muon_momentum;
-    nl.gscale = c.muon_momentum_form == MA_MOMENTUM_EMA ? (float)(1.0 - c.muon_momentum) : 1.0f;
-    nl.eps = (float)c.ns_eps;
-    for (int it = 0; it < c.ns_steps; ++it) {
-      NsEpiArgs e{};
-      set_epi_coefficients(e, c, it);
-      nl.coef[it][0] = e.a;
-      nl.coef[it][1] = e.b;
-      nl.coef[it][2] = e.c;
+  {
+    // every narrow bucket in one launch: they lead the bucket list, so their
+    // matrices are the table's first entries
+    int n_narrow = 0;
+    for (const Bucket& B : h->buckets)
+      if (B.narrow) n_narrow += (int)B.params.size();
+    if (n_narrow > 0) {
+      NarrowLaunch nl;
+      memset(&nl, 0, sizeof nl);
+      nl.mats = h->d_mats + h->buckets.front().mat0;
+      nl.sc = h->d_scalars;
+      nl.sp = h->d_step;
+      nl.nmat = n_narrow;
+      nl.steps = c.ns_steps;
+      nl.nesterov = c.muon_nesterov;
+      nl.mu = (float)c.muon_momentum;
+      nl.gscale = c.muon_momentum_form == MA_MOMENTUM_EMA ? (float)(1.0 - c.muon_momentum) : 1.0f;
+      nl.eps = (float)c.ns_eps;
+      for (int it = 0; it < c.ns_steps; ++it) {
+        NsEpiArgs e{};
+        set_epi_coefficients(e, c, it);
+        nl.coef[it][0] = e.a;
+        nl.coef[it][1] = e.b;
+        nl.coef[it][2] = e.c;
+      }
+      h->narrow.push_back(nl);
     }
-    h->narrow.push_back(nl);
   }
   h->small.clear();
   for (Bucket& B : h->buckets) {
@@ -880,9 +897,9 @@ static ma_status enqueue_newton_schulz(muon_adamw* h) {
   if (h->n_mats == 0) return MA_OK;
   timed(h, MA_K_NS_PREP, h->s0, (double)h->n_tiles * 4,
         [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, (float)c.ns_eps, h->d_rscale, h->s0); });
-  // narrow matrices: fp32 Newton-Schulz on the CUDA cores, one launch per bucket
+  // narrow matrices: fp32 Newton-Schulz on the CUDA cores, one launch for all
   for (size_t i = 0; i < h->narrow.size(); ++i)
-    timed(h, MA_K_NS_NARROW, h->s0, h->narrow_units[i], [&] { launch_ns_narrow(h->narrow[i], h->num_sms, h->s0); });
+    timed(h, MA_K_NS_NARROW, h->s0, h->unit_narrow, [&] { launch_ns_narrow(h->narrow[i], h->num_sms, h->s0); });
   // buckets of small matrices: every iteration and the update in one launch each
   for (size_t i = 0; i < h->small.size(); ++i) {
     SmallLaunch& sl = h->small[i];

@@ -222,7 +222,7 @@ cudaError_t launch_ns_small(const SmallLaunch& L, int num_sms, cudaStream_t st);
 // Newton-Schulz of narrow matrices (short side < kNarrowMinS) in fp32 on the
 // CUDA cores (ns_narrow.cu): one CTA per matrix recomputes the update from the
 // momentum buffer and the gradient, runs every iteration and the parameter
-// update. `mats` are the matrices of one narrow bucket, each with its xf.
+// update. `mats` are every narrow matrix (largest first), each with its xf.
 struct NarrowLaunch {
   const MuonMat* mats;
   const StepScalars* sc;     // clip coefficient
@@ -233,7 +233,7 @@ struct NarrowLaunch {
   float eps;                 // of the Frobenius normalisation
   float coef[64][3];         // (a, b, c) of each iteration
 };
-cudaError_t launch_ns_narrow(const NarrowLaunch& L, int num_sms, cudaStream_t st);  // grid: min(nmat, 4 SMs)
+cudaError_t launch_ns_narrow(const NarrowLaunch& L, int num_sms, cudaStream_t st);  // grid: min(nmat, 3 SMs)
 
 // Partition of the trainable parameters over `world` ranks (host; shard.cu).
 // group/numel/rows/cols per parameter (rows, cols used for Muon matrices).

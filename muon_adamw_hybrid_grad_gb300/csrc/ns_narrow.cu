@@ -16,14 +16,27 @@
 // a 40 x 2000 matrix costs about 2e8 flops per step.
 //
 // One CTA (256 threads) per matrix, over the matrix list in a grid-stride
-// loop. X lives in the matrix's fp32 workspace in the parameter's own layout
-// (m x n, row-major): for m <= n the canonical X is that array, for m > n it
-// is its transpose, which only changes the index arithmetic (A = U^T U and
-// U' = U B for a tall U, since B is symmetric). A and B (s x s, padded to
-// 64 x 64) are in shared memory; 64-column chunks of X pass through shared
-// memory for each product, and X' = B X is written back in place chunk by
-// chunk (a chunk of X' needs only the same chunk of X). Each thread holds a
-// 4 x 4 block of every 64 x 64 result.
+// loop; the host orders the list largest first. X lives in the matrix's fp32
+// workspace in the parameter's own layout (m x n, row-major): for m <= n the
+// canonical X is that array, for m > n it is its transpose, which only
+// changes the index arithmetic (A = U^T U and U' = U B for a tall U, since B
+// is symmetric). A and B (s x s, padded to 64 x 64) are in shared memory;
+// 64-column chunks of X pass through shared memory for each product, and
+// X' = B X is written back in place chunk by chunk (a chunk of X' needs only
+// the same chunk of X).
+//
+// Latency: every chunk is fetched into registers (four 16-byte loads per
+// thread where the layout allows) one chunk ahead, so the global loads of
+// chunk c + 1 are in flight while chunk c is multiplied out of shared memory.
+//
+// Work split: thread (ty, tx) of the 16 x 16 grid holds rows ty + 16 p
+// (p < 4) of each 64-row result. Rows interleave so that a short side s < 64
+// leaves every warp with ceil((s - row) / 16) live row groups, the same count
+// on all four schedulers; a warp skips the groups that lie wholly in the zero
+// padding, and the Gram product also skips the column groups tx + 16 q >= s
+// (the same for every thread). To read the four rows of a thread as one
+// 16-byte word, the Gram chunk and B are stored with row i at position
+// 4 (i mod 16) + i / 16.
 //
 // The update G is recomputed from the momentum buffer that the momentum pass
 // has just written and the gradient, with the same fp32 operations that pass
@@ -40,9 +53,11 @@ namespace ma {
 namespace {
 
 constexpr int kNarrowThreads = 256;
-constexpr int SP = 64;       // padded short side
-constexpr int CW = 64;       // columns of the long side per chunk
-constexpr int LD = SP + 4;   // shared row pitch in floats (16-byte rows, fewer bank conflicts)
+constexpr int SP = 64;                                 // padded short side
+constexpr int CW = 64;                                 // columns of the long side per chunk
+constexpr int LD = SP + 4;                             // shared row pitch in floats (16-byte rows)
+constexpr int QPT = SP * CW / 4 / kNarrowThreads;      // 4-float words of a chunk per thread
+constexpr int UB = 8;                                  // elements in flight per thread forming G
 
 __device__ __forceinline__ float narrow_grad(const MuonMat& M, int64_t idx) {
   return M.gdtype == DT_BF16 ? __uint_as_float(((uint32_t) static_cast<const uint16_t*>(M.g)[idx]) << 16)
@@ -54,27 +69,120 @@ __device__ __forceinline__ int64_t canon_index(const MuonMat& M, int i, int j) {
   return M.transposed ? (int64_t)j * M.n + i : (int64_t)i * M.n + j;
 }
 
-// Chunk [j0, j0 + CW) of X into shared memory, zero outside the matrix.
-// KMAJOR: T[jj][i] (for the Gram product); otherwise T[i][jj] (for B X).
-// The global reads run along the parameter's rows in both cases.
-template <bool KMAJOR>
-__device__ __forceinline__ void load_chunk(const MuonMat& M, const float* X, int j0, float (*T)[LD]) {
+// Shared position of row i in the interleaved layouts.
+__device__ __forceinline__ int perm_row(int i) { return 4 * (i & 15) + (i >> 4); }
+
+// Word k of the thread's share of chunk [j0, j0 + CW): the 4 floats at
+// (hi, lo..lo+3) of the chunk in memory order, where (hi, lo) is (i, jj) for a
+// wide matrix (parameter rows are rows of X) and (jj, i) for a tall one
+// (parameter rows are columns of X). Zero outside the matrix.
+__device__ __forceinline__ void word_coords(int k, int& hi, int& lo) {
+  const int q = threadIdx.x + k * kNarrowThreads;
+  hi = q >> 4;
+  lo = 4 * (q & 15);
+}
+
+__device__ __forceinline__ void fetch_chunk(const MuonMat& M, const float* X, int j0, float4 (&v)[QPT]) {
   const int s = M.s, l = M.l;
-  for (int e = threadIdx.x; e < SP * CW; e += kNarrowThreads) {
-    int i, jj;
-    if (M.transposed) {  // parameter row = j: consecutive threads take consecutive i
-      i = e % SP;
-      jj = e / SP;
-    } else {  // parameter row = i: consecutive threads take consecutive j
-      jj = e % CW;
-      i = e / CW;
+  // X starts 16-byte aligned (the host pads every slot); rows of X in memory
+  // are l floats long for a wide matrix, s for a tall one
+  const bool vec = M.transposed ? (s % 4 == 0) : (l % 4 == 0);
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    int hi, lo;
+    word_coords(k, hi, lo);
+    const int i0 = M.transposed ? lo : hi, j = M.transposed ? j0 + hi : j0 + lo;
+    float f[4];
+    if (M.transposed) {
+      const float* src = X + (int64_t)j * s + i0;
+      if (vec && j < l && i0 + 3 < s) {
+        v[k] = *reinterpret_cast<const float4*>(src);
+        continue;
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) f[t] = (j < l && i0 + t < s) ? src[t] : 0.f;
+    } else {
+      const float* src = X + (int64_t)i0 * l + j;
+      if (vec && i0 < s && j + 3 < l) {
+        v[k] = *reinterpret_cast<const float4*>(src);
+        continue;
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) f[t] = (i0 < s && j + t < l) ? src[t] : 0.f;
     }
-    const int j = j0 + jj;
-    const float v = (i < s && j < l) ? X[canon_index(M, i, j)] : 0.f;
-    if (KMAJOR)
-      T[jj][i] = v;
-    else
-      T[i][jj] = v;
+    v[k] = make_float4(f[0], f[1], f[2], f[3]);
+  }
+}
+
+// The fetched chunk into shared memory. GRAM: T[jj][perm_row(i)] (the
+// reduction index jj outer, rows interleaved); otherwise T[i][jj] (B X reduces
+// over i).
+template <bool GRAM>
+__device__ __forceinline__ void store_chunk(const MuonMat& M, const float4 (&v)[QPT], float (*T)[LD]) {
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    int hi, lo;
+    word_coords(k, hi, lo);
+    const float f[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+    if (M.transposed) {  // (jj = hi, i = lo + t)
+      if (GRAM) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) T[hi][perm_row(lo + t)] = f[t];
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) T[lo + t][hi] = f[t];
+      }
+    } else {  // (i = hi, jj = lo + t)
+      if (GRAM) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) T[lo + t][perm_row(hi)] = f[t];
+      } else {
+        *reinterpret_cast<float4*>(&T[hi][lo]) = v[k];
+      }
+    }
+  }
+}
+
+// acc[p][q] += sum over the chunk's columns of X[ty + 16 p][.] X[tx + 16 q][.]
+// for p < NP, q < NQ.
+template <int NP, int NQ>
+__device__ __forceinline__ void gram_chunk(const float (*T)[LD], int ty, int tx, float (&acc)[4][4]) {
+#pragma unroll 4
+  for (int jj = 0; jj < CW; ++jj) {
+    const float4 a = *reinterpret_cast<const float4*>(&T[jj][4 * ty]);
+    const float4 b = *reinterpret_cast<const float4*>(&T[jj][4 * tx]);
+    const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) acc[p][q] = fmaf(av[p], bv[q], acc[p][q]);
+  }
+}
+
+template <int NP>
+__device__ __forceinline__ void gram_chunk_q(const float (*T)[LD], int nq, int ty, int tx, float (&acc)[4][4]) {
+  switch (nq) {
+    case 1: gram_chunk<NP, 1>(T, ty, tx, acc); break;
+    case 2: gram_chunk<NP, 2>(T, ty, tx, acc); break;
+    case 3: gram_chunk<NP, 3>(T, ty, tx, acc); break;
+    default: gram_chunk<NP, 4>(T, ty, tx, acc); break;
+  }
+}
+
+// o[p][q] += sum_{k < kmax} B[ty + 16 p][k] X[k][4 tx + q] for p < NP, with
+// Bp[k][perm_row(i)] = B[i][k] and T[k][jj] the chunk of X.
+template <int NP>
+__device__ __forceinline__ void bx_chunk(const float (*Bp)[LD], const float (*T)[LD], int kmax, int ty, int tx,
+                                         float (&o)[4][4]) {
+#pragma unroll 4
+  for (int k = 0; k < kmax; ++k) {
+    const float4 b = *reinterpret_cast<const float4*>(&Bp[k][4 * ty]);
+    const float4 x = *reinterpret_cast<const float4*>(&T[k][4 * tx]);
+    const float bv[4] = {b.x, b.y, b.z, b.w}, xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) o[p][q] = fmaf(bv[p], xv[q], o[p][q]);
   }
 }
 
@@ -90,11 +198,11 @@ __device__ __forceinline__ double narrow_block_sum(double v, double* sh) {
   return r;
 }
 
-__global__ void __launch_bounds__(kNarrowThreads) ns_narrow_kernel(const __grid_constant__ NarrowLaunch L) {
+__global__ void __launch_bounds__(kNarrowThreads, 3) ns_narrow_kernel(const __grid_constant__ NarrowLaunch L) {
   __shared__ __align__(16) float s0[SP][LD];  // A; the chunk of B X
-  __shared__ __align__(16) float s1[SP][LD];  // the chunk of X X^T; B
+  __shared__ __align__(16) float s1[SP][LD];  // the chunk of X X^T; B (rows interleaved)
   __shared__ double red[kNarrowThreads / 32];
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 4 x 4 block (rows 4 ty.., cols 4 tx..)
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const float coef = L.sc->coef * L.gscale;
   const float mu = L.mu;
   for (int mi = blockIdx.x; mi < L.nmat; mi += gridDim.x) {
@@ -102,90 +210,119 @@ __global__ void __launch_bounds__(kNarrowThreads) ns_narrow_kernel(const __grid_
     float* const X = M.xf;
     const int s = M.s, l = M.l;
     const int64_t numel = (int64_t)M.m * M.n;
+    // live row groups of this warp (rows ty + 16 p of its lower ty), column
+    // groups of the Gram product, and the reduction length of A A and B X
+    const int ty0 = ty & ~1;
+    const int np = min(4, max(0, (s - ty0 + 15) / 16));
+    const int nq = min(4, (s + 15) / 16);
+    const int kmax = (s + 3) & ~3;
+    const int nch = (l + CW - 1) / CW;
     // ---- the update G (as the momentum pass forms it) and ||G||_F ----
     double sq = 0.0;
-    for (int64_t e = threadIdx.x; e < numel; e += kNarrowThreads) {
-      const float gh = coef * narrow_grad(M, e);
-      const float b = M.buf[e];
-      const float u = L.nesterov ? fmaf(mu, b, gh) : b;
-      X[e] = u;
-      sq += (double)u * (double)u;
+    for (int64_t e0 = threadIdx.x; e0 < numel; e0 += (int64_t)UB * kNarrowThreads) {
+      float gv[UB], bv[UB];
+#pragma unroll
+      for (int k = 0; k < UB; ++k) {
+        const int64_t e = e0 + (int64_t)k * kNarrowThreads;
+        gv[k] = e < numel ? narrow_grad(M, e) : 0.f;
+        bv[k] = e < numel ? M.buf[e] : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < UB; ++k) {
+        const int64_t e = e0 + (int64_t)k * kNarrowThreads;
+        if (e < numel) {
+          const float u = L.nesterov ? fmaf(mu, bv[k], coef * gv[k]) : bv[k];
+          X[e] = u;
+          sq += (double)u * (double)u;
+        }
+      }
     }
     const double tot = narrow_block_sum(sq, red);  // also orders the writes of X before the reads below
     const float r = (float)(1.0 / (sqrt(tot) + (double)L.eps));
+    float4 stage[QPT];
+    fetch_chunk(M, X, 0, stage);
     for (int it = 0; it < L.steps; ++it) {
       const bool first = it == 0, last = it == L.steps - 1;
       const float ca = L.coef[it][0], cb = L.coef[it][1], cc = L.coef[it][2];
       // ---- A = X X^T (r^2 X X^T in the first iteration) ----
       float acc[4][4] = {};
-      for (int j0 = 0; j0 < l; j0 += CW) {
-        load_chunk<true>(M, X, j0, s1);
+      for (int c = 0; c < nch; ++c) {
+        store_chunk<true>(M, stage, s1);
         __syncthreads();
+        if (c + 1 < nch) fetch_chunk(M, X, (c + 1) * CW, stage);
+        switch (np) {
+          case 0: break;
+          case 1: gram_chunk_q<1>(s1, nq, ty, tx, acc); break;
+          case 2: gram_chunk_q<2>(s1, nq, ty, tx, acc); break;
+          case 3: gram_chunk_q<3>(s1, nq, ty, tx, acc); break;
+          default: gram_chunk_q<4>(s1, nq, ty, tx, acc); break;
+        }
+        __syncthreads();  // the chunk buffer is refilled next
+      }
+      fetch_chunk(M, X, 0, stage);  // the first chunk of B X, in flight during A A
+      const float sa = first ? r * r : 1.f;
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) s0[ty + 16 * p][tx + 16 * q] = acc[p][q] * sa;
+      __syncthreads();
+      // ---- B = a I + b A + c A A (A is symmetric: A[i][k] = A[k][i]); thread
+      // (ty, tx) forms rows 4 ty.. and columns 4 tx.. of it ----
+      float aa[4][4] = {};
+      if (4 * ty < s) {
 #pragma unroll 4
-        for (int jj = 0; jj < CW; ++jj) {
-          const float4 a = *reinterpret_cast<const float4*>(&s1[jj][4 * ty]);
-          const float4 b = *reinterpret_cast<const float4*>(&s1[jj][4 * tx]);
+        for (int k = 0; k < kmax; ++k) {
+          const float4 a = *reinterpret_cast<const float4*>(&s0[k][4 * ty]);
+          const float4 b = *reinterpret_cast<const float4*>(&s0[k][4 * tx]);
           const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
           for (int p = 0; p < 4; ++p)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(av[p], bv[q], acc[p][q]);
+            for (int q = 0; q < 4; ++q) aa[p][q] = fmaf(av[p], bv[q], aa[p][q]);
         }
-        __syncthreads();
-      }
-      const float sa = first ? r * r : 1.f;
-#pragma unroll
-      for (int p = 0; p < 4; ++p)
-        *reinterpret_cast<float4*>(&s0[4 * ty + p][4 * tx]) =
-            make_float4(acc[p][0] * sa, acc[p][1] * sa, acc[p][2] * sa, acc[p][3] * sa);
-      __syncthreads();
-      // ---- B = a I + b A + c A A (A is symmetric: A[i][k] = A[k][i]) ----
-      float aa[4][4] = {};
-#pragma unroll 4
-      for (int k = 0; k < SP; ++k) {
-        const float4 a = *reinterpret_cast<const float4*>(&s0[k][4 * ty]);
-        const float4 b = *reinterpret_cast<const float4*>(&s0[k][4 * tx]);
-        const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) aa[p][q] = fmaf(av[p], bv[q], aa[p][q]);
       }
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
-        float o[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int i = 4 * ty + p, k = 4 * tx + q;
           const float lin = fmaf(cb, s0[i][k], i == k ? ca : 0.f);
-          o[q] = (i < s && k < s) ? fmaf(cc, aa[p][q], lin) : 0.f;
+          s1[k][perm_row(i)] = (i < s && k < s) ? fmaf(cc, aa[p][q], lin) : 0.f;
         }
-        *reinterpret_cast<float4*>(&s1[4 * ty + p][4 * tx]) = make_float4(o[0], o[1], o[2], o[3]);
       }
-      __syncthreads();
+      __syncthreads();  // B complete; A no longer read (s0 takes the chunks of X)
       // ---- X' = B X (r B X in the first iteration), chunk by chunk in place;
       // the last iteration applies it to the parameter instead ----
       const float sx = first ? r : 1.f;
       const float lrm = L.sp->ns_lr * M.lr_mult;
       const float dec = L.sp->ns_decay[M.group];
-      for (int j0 = 0; j0 < l; j0 += CW) {
-        load_chunk<false>(M, X, j0, s0);
+      for (int c = 0; c < nch; ++c) {
+        const int j0 = c * CW;
+        store_chunk<false>(M, stage, s0);
         __syncthreads();
-        float o[4][4] = {};
-#pragma unroll 4
-        for (int k = 0; k < SP; ++k) {
-          const float4 b = *reinterpret_cast<const float4*>(&s1[k][4 * ty]);  // B[4 ty + p][k]
-          const float4 x = *reinterpret_cast<const float4*>(&s0[k][4 * tx]);  // X[k][j0 + 4 tx + q]
-          const float bv[4] = {b.x, b.y, b.z, b.w}, xv[4] = {x.x, x.y, x.z, x.w};
+        if (c + 1 < nch) fetch_chunk(M, X, j0 + CW, stage);
+        float pv[4][4];
+        if (last) {  // the parameter's values, loaded while the product runs
 #pragma unroll
           for (int p = 0; p < 4; ++p)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) o[p][q] = fmaf(bv[p], xv[q], o[p][q]);
+            for (int q = 0; q < 4; ++q) {
+              const int i = ty + 16 * p, j = j0 + 4 * tx + q;
+              pv[p][q] = (p < np && i < s && j < l) ? M.p[canon_index(M, i, j)] : 0.f;
+            }
+        }
+        float o[4][4] = {};
+        switch (np) {
+          case 0: break;
+          case 1: bx_chunk<1>(s1, s0, kmax, ty, tx, o); break;
+          case 2: bx_chunk<2>(s1, s0, kmax, ty, tx, o); break;
+          case 3: bx_chunk<3>(s1, s0, kmax, ty, tx, o); break;
+          default: bx_chunk<4>(s1, s0, kmax, ty, tx, o); break;
         }
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-          const int i = 4 * ty + p;
-          if (i >= s) continue;
+          const int i = ty + 16 * p;
+          if (p >= np || i >= s) continue;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int j = j0 + 4 * tx + q;
@@ -195,7 +332,7 @@ __global__ void __launch_bounds__(kNarrowThreads) ns_narrow_kernel(const __grid_
             if (!last) {
               X[idx] = v;
             } else {
-              const float pn = fmaf(M.p[idx], dec, -lrm * v);
+              const float pn = fmaf(pv[p][q], dec, -lrm * v);
               M.p[idx] = pn;
               if (M.shadow) M.shadow[idx] = ns_f2bf(pn);
             }
@@ -203,6 +340,7 @@ __global__ void __launch_bounds__(kNarrowThreads) ns_narrow_kernel(const __grid_
         }
         __syncthreads();  // the chunk buffer is refilled next; X' is visible to the next Gram
       }
+      if (!last) fetch_chunk(M, X, 0, stage);  // the next iteration's first Gram chunk
     }
   }
 }
@@ -210,7 +348,7 @@ __global__ void __launch_bounds__(kNarrowThreads) ns_narrow_kernel(const __grid_
 }  // namespace
 
 cudaError_t launch_ns_narrow(const NarrowLaunch& L, int num_sms, cudaStream_t st) {
-  const int grid = L.nmat < 4 * num_sms ? L.nmat : 4 * num_sms;
+  const int grid = L.nmat < 3 * num_sms ? L.nmat : 3 * num_sms;
   if (grid <= 0) return cudaSuccess;
   ns_narrow_kernel<<<grid, kNarrowThreads, 0, st>>>(L);
   return cudaGetLastError();

@@ -20,6 +20,9 @@ Workloads (all synthetic; no dataset is involved):
 ``many_small``  512 Muon matrices 128x512 and 256 of 512x128, plus 4096 1-D
                 AdamW tensors with lengths drawn from
                 ``default_rng(0).integers(128, 4097, 4096)``; 10 steps.
+``narrow``      320 Muon matrices with a short side of 40 (128 of 1000x40,
+                128 of 40x1000, 64 of 2000x40; rank-8 + noise gradients), which
+                take the fp32 Newton-Schulz path, plus 8 norm vectors; 10 steps.
 ``full_vla``    Muon group of h2048 plus a 1.69 G-element AdamW backbone
                 (28 layers of hidden 2048 with GQA k/v 1024x2048, MLP 6144,
                 two norms; 67 vision stand-in blocks 2048x2048) and a frozen
@@ -153,6 +156,16 @@ def _many_small() -> Workload:
     return Workload("many_small", tuple(t), policy="fp32_mixed", grad_dtype="bf16", steps=10, lr=BASE_LR)
 
 
+def _narrow() -> Workload:
+    t: List[TensorSpec] = []
+    shapes = [(1000, 40)] * 128 + [(40, 1000)] * 128 + [(2000, 40)] * 64
+    for k, sh in enumerate(shapes):
+        t.append(TensorSpec(f"model.action_expert.layers.{k}.mlp.w_narrow.weight", sh, rank8=True))
+    for k in range(8):
+        t.append(TensorSpec(f"model.action_expert.layers.{k}.input_layernorm.weight", (1000,)))
+    return Workload("narrow", tuple(t), policy="bf16_mixed", grad_dtype="bf16", steps=10, lr=BASE_LR)
+
+
 FULL_VLA_VISION_BLOCKS = 67
 
 
@@ -183,6 +196,7 @@ _BUILDERS = {
     "h2048": _h2048,
     "h2048_fp32grad": lambda: _h2048("fp32"),
     "many_small": _many_small,
+    "narrow": _narrow,
     "full_vla": _full_vla,
 }
 
