@@ -108,8 +108,9 @@ struct Bucket {
   uint16_t *X0 = nullptr, *X1 = nullptr, *A = nullptr, *B = nullptr;
   bool fused = false;   // small matrices: the whole Newton-Schulz in one launch (ns_small_kernel)
   bool narrow = false;  // short side < kNarrowMinS: fp32 Newton-Schulz (ns_narrow_kernel)
-  float* XF = nullptr;  // narrow: fp32 X of each slot (xf_stride floats per slot)
+  float* XF = nullptr;  // narrow, streamed: fp32 X of each slot (xf_stride floats per slot)
   size_t xf_stride = 0;  // narrow: the bucket's largest m n, rounded up to 64 floats
+  bool narrow_stream = false;  // narrow: some matrix too long for a resident cluster (needs XF)
 };
 
 struct ProfRec {
@@ -182,7 +183,11 @@ struct muon_adamw {
   std::vector<SmallLaunch> small;      // one per fused bucket
   std::vector<double> small_units;     // their symmetric flops per step
   double unit_fused = 0;               // symmetric flops per step of all fused buckets
-  std::vector<NarrowLaunch> narrow;    // one launch over every narrow bucket (or none)
+  std::vector<NarrowLaunch> narrow;    // narrow matrices: one launch per cluster size, then the streamed ones
+  std::vector<size_t> narrow_smem;     // their dynamic shared memory
+  std::vector<double> narrow_units;    // their symmetric flops per step
+  int narrow_per_sm = 1;               // resident CTAs per SM of the streaming kernel
+  int32_t* d_narrow_idx = nullptr;     // the launches' matrix indices
   double unit_narrow = 0;              // symmetric flops per step of all narrow buckets
   std::vector<std::vector<NsProblem>> simt[3];
   double unit_gram = 0, unit_poly = 0, unit_update = 0;  // symmetric flops per iteration (all buckets)
@@ -335,11 +340,18 @@ ma_status build_plan(muon_adamw* h) {
     if (a.narrow != b.narrow) return a.narrow;
     return a.narrow && (double)a.S * a.S * a.L > (double)b.S * b.S * b.L;
   });
+  int n_narrow = 0;
   for (Bucket& B : h->buckets) {
     if (!B.narrow) continue;
     int64_t mx = 0;
-    for (int pi : B.params) mx = std::max(mx, h->params[pi].numel);
+    for (int pi : B.params) {
+      const Param& p = h->params[pi];
+      mx = std::max(mx, p.numel);
+      const int s = (int)std::min(p.shape[0], p.shape[1]), l = (int)std::max(p.shape[0], p.shape[1]);
+      if (narrow_cluster_for(s, l) == 0) B.narrow_stream = true;
+    }
     B.xf_stride = (size_t)((mx + 63) / 64 * 64);
+    n_narrow += (int)B.params.size();
   }
   // --- sizes ---
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -365,7 +377,7 @@ ma_status build_plan(muon_adamw* h) {
     const Bucket& B = h->buckets[b];
     const size_t nb = B.params.size();
     const size_t xs = al(nb * (size_t)B.S * B.L * 2), as = al(nb * (size_t)B.S * B.S * 2);
-    const size_t sizes[4] = {xs, B.narrow ? al(nb * B.xf_stride * 4) : xs, B.narrow ? 0 : as,
+    const size_t sizes[4] = {xs, B.narrow ? (B.narrow_stream ? al(nb * B.xf_stride * 4) : 0) : xs, B.narrow ? 0 : as,
                              B.narrow ? 0 : as};
     for (int q = 0; q < 4; ++q) {
       ws_off[4 * b + q] = off;
@@ -412,6 +424,8 @@ ma_status build_plan(muon_adamw* h) {
   off += al(sizeof(StepParams));
   const size_t off_err = off;
   off += al(sizeof(int));
+  const size_t off_nidx = off;
+  off += al((size_t)n_narrow * sizeof(int32_t));
   h->arena_bytes = off;
 
   // --- allocate and zero (state starts at zero; workspace padding stays zero) ---
@@ -427,7 +441,7 @@ ma_status build_plan(muon_adamw* h) {
     Bucket& B = h->buckets[b];
     B.X0 = reinterpret_cast<uint16_t*>(base + ws_off[4 * b + 0]);
     if (B.narrow) {
-      B.XF = reinterpret_cast<float*>(base + ws_off[4 * b + 1]);
+      B.XF = B.narrow_stream ? reinterpret_cast<float*>(base + ws_off[4 * b + 1]) : nullptr;
       B.X1 = B.A = B.B = nullptr;
     } else {
       B.XF = nullptr;
@@ -449,6 +463,7 @@ ma_status build_plan(muon_adamw* h) {
   h->d_scalars = reinterpret_cast<StepScalars*>(base + off_scalars);
   h->d_step = reinterpret_cast<StepParams*>(base + off_step);
   h->d_err = reinterpret_cast<int*>(base + off_err);
+  h->d_narrow_idx = reinterpret_cast<int32_t*>(base + off_nidx);
 
   // --- host tables with device pointers ---
   std::vector<GradChunk> norm_chunks;
@@ -549,7 +564,7 @@ ma_status build_plan(muon_adamw* h) {
                (reinterpret_cast<uintptr_t>(p.shadow) % 16 == 0);
       M.lr_mult = (float)(p.lr_scale * c.muon_lr_scale * c.moonlight_coef * sqrt((double)M.l));
       M.group = p.og;
-      M.xf = B.narrow ? B.XF + slot * B.xf_stride : nullptr;
+      M.xf = B.XF ? B.XF + slot * B.xf_stride : nullptr;
       pmaps.resize(2 * (size_t)(mat_index + 1));
       M.tma = (c.ns_kernel == MA_NS_TCGEN05 && !(c.reserved[0] & 4) &&
                tc_encode_param_maps(&pmaps[2 * (size_t)mat_index], M))
@@ -689,33 +704,55 @@ ma_status build_plan(muon_adamw* h) {
     }
   }
   h->narrow.clear();
-  {
-    // every narrow bucket in one launch: they lead the bucket list, so their
-    // matrices are the table's first entries
-    int n_narrow = 0;
-    for (const Bucket& B : h->buckets)
-      if (B.narrow) n_narrow += (int)B.params.size();
-    if (n_narrow > 0) {
-      NarrowLaunch nl;
-      memset(&nl, 0, sizeof nl);
-      nl.mats = h->d_mats + h->buckets.front().mat0;
-      nl.sc = h->d_scalars;
-      nl.sp = h->d_step;
-      nl.nmat = n_narrow;
-      nl.steps = c.ns_steps;
-      nl.nesterov = c.muon_nesterov;
-      nl.mu = (float)c.muon_momentum;
-      nl.gscale = c.muon_momentum_form == MA_MOMENTUM_EMA ? (float)(1.0 - c.muon_momentum) : 1.0f;
-      nl.eps = (float)c.ns_eps;
-      for (int it = 0; it < c.ns_steps; ++it) {
-        NsEpiArgs e{};
-        set_epi_coefficients(e, c, it);
-        nl.coef[it][0] = e.a;
-        nl.coef[it][1] = e.b;
-        nl.coef[it][2] = e.c;
-      }
-      h->narrow.push_back(nl);
+  h->narrow_smem.clear();
+  h->narrow_units.clear();
+  if (n_narrow > 0) {
+    // the narrow matrices lead the matrix table (their buckets come first,
+    // costliest first); one launch per cluster size, each over its matrices
+    // in table order, then the streamed ones
+    NarrowLaunch base;
+    memset(&base, 0, sizeof base);
+    base.mats = h->d_mats;
+    base.sc = h->d_scalars;
+    base.sp = h->d_step;
+    base.steps = c.ns_steps;
+    base.nesterov = c.muon_nesterov;
+    base.mu = (float)c.muon_momentum;
+    base.gscale = c.muon_momentum_form == MA_MOMENTUM_EMA ? (float)(1.0 - c.muon_momentum) : 1.0f;
+    base.eps = (float)c.ns_eps;
+    for (int it = 0; it < c.ns_steps; ++it) {
+      NsEpiArgs e{};
+      set_epi_coefficients(e, c, it);
+      base.coef[it][0] = e.a;
+      base.coef[it][1] = e.b;
+      base.coef[it][2] = e.c;
     }
+    std::vector<int32_t> idx;
+    size_t max_smem = 0;
+    for (int cl : {8, 4, 2, 1, 0}) {
+      const size_t first = idx.size();
+      size_t smem = 0;
+      double units = 0;
+      for (int mi = 0; mi < n_narrow; ++mi) {
+        const MuonMat& M = mats[mi];
+        if (narrow_cluster_for(M.s, M.l) != cl) continue;
+        idx.push_back(mi);
+        if (cl > 0) smem = std::max(smem, narrow_resident_smem(M.s, M.l, cl));
+        const double sd = M.s, ld = M.l;
+        units += (double)c.ns_steps * (sd * (sd + 1) * ld + sd * (sd + 1) * sd + 2 * sd * sd * ld);
+      }
+      if (idx.size() == first) continue;
+      NarrowLaunch nl = base;
+      nl.idx = h->d_narrow_idx + first;
+      nl.nmat = (int)(idx.size() - first);
+      nl.cluster = cl;
+      h->narrow.push_back(nl);
+      h->narrow_smem.push_back(smem);
+      h->narrow_units.push_back(units);
+      max_smem = std::max(max_smem, smem);
+    }
+    CUDA_TRY(cudaMemcpy(h->d_narrow_idx, idx.data(), idx.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+    CUDA_TRY(ns_narrow_prepare(max_smem, &h->narrow_per_sm));
   }
   h->small.clear();
   for (Bucket& B : h->buckets) {
@@ -897,9 +934,11 @@ static ma_status enqueue_newton_schulz(muon_adamw* h) {
   if (h->n_mats == 0) return MA_OK;
   timed(h, MA_K_NS_PREP, h->s0, (double)h->n_tiles * 4,
         [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, (float)c.ns_eps, h->d_rscale, h->s0); });
-  // narrow matrices: fp32 Newton-Schulz on the CUDA cores, one launch for all
+  // narrow matrices: fp32 Newton-Schulz on the CUDA cores
   for (size_t i = 0; i < h->narrow.size(); ++i)
-    timed(h, MA_K_NS_NARROW, h->s0, h->unit_narrow, [&] { launch_ns_narrow(h->narrow[i], h->num_sms, h->s0); });
+    timed(h, MA_K_NS_NARROW, h->s0, h->narrow_units[i], [&] {
+      launch_ns_narrow(h->narrow[i], h->narrow_smem[i], h->num_sms, h->narrow_per_sm, h->s0);
+    });
   // buckets of small matrices: every iteration and the update in one launch each
   for (size_t i = 0; i < h->small.size(); ++i) {
     SmallLaunch& sl = h->small[i];

@@ -220,20 +220,62 @@ bool tc_encode_small(SmallLaunch& sl, const uint16_t* X, int nmat, int L, char* 
 cudaError_t launch_ns_small(const SmallLaunch& L, int num_sms, cudaStream_t st);  // grid: min(nmat, num_sms)
 
 // Newton-Schulz of narrow matrices (short side < kNarrowMinS) in fp32 on the
-// CUDA cores (ns_narrow.cu): one CTA per matrix recomputes the update from the
-// momentum buffer and the gradient, runs every iteration and the parameter
-// update. `mats` are every narrow matrix (largest first), each with its xf.
+// CUDA cores (ns_narrow.cu), from the update (recomputed from the momentum
+// buffer and the gradient) through the parameter update, in one launch per
+// group of matrices:
+//   resident (cluster >= 1): a cluster of `cluster` CTAs per matrix, each CTA
+//     holding a slice of the long side of X in shared memory for the whole
+//     chain; the partial Gram matrices are summed through distributed shared
+//     memory;
+//   streaming (cluster == 0): one CTA per matrix, X in the matrix's fp32
+//     workspace (xf), streamed through shared memory in 64-column chunks (for
+//     matrices whose slices would not fit in 8 CTAs' shared memory).
 struct NarrowLaunch {
   const MuonMat* mats;
+  const int32_t* idx;        // the launch's matrices (indices into mats), largest first
   const StepScalars* sc;     // clip coefficient
   const StepParams* sp;      // lr and decays of the update
   int32_t nmat, steps;
   int32_t nesterov;
+  int32_t cluster;           // CTAs per matrix (resident), 0 = streaming
   float mu, gscale;          // momentum coefficient, weight of the clipped gradient
   float eps;                 // of the Frobenius normalisation
   float coef[64][3];         // (a, b, c) of each iteration
 };
-cudaError_t launch_ns_narrow(const NarrowLaunch& L, int num_sms, cudaStream_t st);  // grid: min(nmat, 3 SMs)
+
+// Shape plan of the resident kernel, shared by the host planner and the
+// kernel: target columns of the long side per CTA, rows of the X slice held
+// in shared memory (row s, read by some warps of the last live row group, is
+// zero), columns per CTA (a multiple of 4; the last CTA may have fewer or
+// none), and the row pitch in floats (a multiple of 64, plus 4).
+constexpr int kNarrowColsPerCta = 256;
+constexpr int kNarrowMaxCluster = 8;
+constexpr size_t kNarrowMaxSmem = 227 * 1024;
+constexpr int kNarrowFixedFloats = 2 * 64 * 68 + 32;  // two A / B tiles and 16 doubles
+__host__ __device__ inline int narrow_rows(int s) {
+  const int r = (s + 16) / 16 * 16;
+  return r > 64 ? 64 : r;
+}
+__host__ __device__ inline int narrow_cols(int l, int cluster) { return ((l + cluster - 1) / cluster + 3) & ~3; }
+__host__ __device__ inline int narrow_pitch(int lc) { return (lc + 63) / 64 * 64 + 4; }
+inline size_t narrow_resident_smem(int s, int l, int cluster) {
+  return ((size_t)kNarrowFixedFloats + (size_t)narrow_rows(s) * narrow_pitch(narrow_cols(l, cluster))) * 4;
+}
+// Cluster size for a narrow s x l matrix (canonical s <= l): the smallest
+// power of two giving at most kNarrowColsPerCta columns per CTA, capped at
+// kNarrowMaxCluster; 0 if its slices then exceed kNarrowMaxSmem (streaming).
+inline int narrow_cluster_for(int s, int l) {
+  int c = 1;
+  while (c < kNarrowMaxCluster && (l + c - 1) / c > kNarrowColsPerCta) c *= 2;
+  return narrow_resident_smem(s, l, c) <= kNarrowMaxSmem ? c : 0;
+}
+
+// Sets the kernels' shared-memory attributes (the resident kernel's to
+// resident_smem bytes); returns the streaming kernel's resident CTAs per SM.
+cudaError_t ns_narrow_prepare(size_t resident_smem, int* stream_blocks_per_sm);
+// Resident: grid nmat x cluster CTAs, `smem` bytes each. Streaming: grid
+// min(nmat, blocks_per_sm x num_sms), a grid-stride loop over the matrices.
+cudaError_t launch_ns_narrow(const NarrowLaunch& L, size_t smem, int num_sms, int blocks_per_sm, cudaStream_t st);
 
 // Partition of the trainable parameters over `world` ranks (host; shard.cu).
 // group/numel/rows/cols per parameter (rows, cols used for Muon matrices).
