@@ -63,6 +63,7 @@ constexpr int CW = 64;                             // columns of the long side p
 constexpr int LD = SP + 4;                         // shared row pitch in floats (16-byte rows)
 constexpr int QPT = SP * CW / 4 / kNarrowThreads;  // 4-float words of a chunk per thread
 constexpr int UB = 8;                              // elements in flight per thread forming G
+constexpr int UBV = 4;                             // 16-byte words of them, where aligned
 constexpr int kTile = SP * LD;                     // floats per shared tile
 constexpr size_t kNarrowSmem = 3 * kTile * sizeof(float) + (kNarrowThreads / 32) * sizeof(double);
 
@@ -500,11 +501,17 @@ __global__ void __launch_bounds__(kNarrowThreads, 2) ns_narrow_stream_kernel(con
 // iteration's cluster barrier, which every CTA reaches only once it has read
 // all partials of this one; the other tile is free locally from this
 // iteration's barrier on (its partials were read before it). The Frobenius
-// norm's sum of squares is exchanged the same way. All CTAs of a cluster take
+// norm's sum of squares is exchanged the same way, its barrier split around
+// the first Gram product. All CTAs of a cluster take
 // the same path (the same matrix and iteration count), so each cluster
 // barrier is reached by all of them; a final cluster barrier keeps every CTA's
 // shared memory alive until the last remote read of it.
 // ---------------------------------------------------------------------------
+
+// The two halves of a cluster barrier (every thread of every CTA of the
+// cluster executes both, in this order, between two full barriers).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // Shared-memory offset and global index of element e of this CTA's slice, in
 // the order of the parameter's rows (e < s ncol < 2^31).
@@ -551,7 +558,50 @@ __device__ void resident_matrix(const NarrowLaunch& L, const MuonMat& M, int C, 
     const float* const buf = M.buf;
     const int cnt = s * ncol;
     double sq = 0.0;
-    for (int e0 = threadIdx.x; e0 < cnt; e0 += UB * kNarrowThreads) {
+    // 16-byte words of 4 consecutive elements of a parameter row where the
+    // rows hold whole words (then every CTA's slice starts on one)
+    const bool uvec = (TALL ? (s % 4 == 0) : (l % 4 == 0)) &&
+                      reinterpret_cast<uintptr_t>(g) % (gbf ? 8 : 16) == 0 && reinterpret_cast<uintptr_t>(buf) % 16 == 0;
+    const int words = uvec ? cnt / 4 : 0;
+    for (int w0 = threadIdx.x; w0 < words; w0 += UBV * kNarrowThreads) {
+      float4 gv[UBV], bv[UBV];
+      int xo[UBV];
+#pragma unroll
+      for (int k = 0; k < UBV; ++k) {
+        const int w = w0 + k * kNarrowThreads;
+        xo[k] = -1;
+        if (w < words) {
+          int64_t gi;
+          slice_coords<TALL>(4 * w, s, l, c0, ncol, P, xo[k], gi);
+          bv[k] = *reinterpret_cast<const float4*>(buf + gi);
+          if (gbf) {
+            const uint2 h = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(g) + gi);
+            gv[k] = make_float4(__uint_as_float(h.x << 16), __uint_as_float(h.x & 0xffff0000u),
+                                __uint_as_float(h.y << 16), __uint_as_float(h.y & 0xffff0000u));
+          } else {
+            gv[k] = *reinterpret_cast<const float4*>(static_cast<const float*>(g) + gi);
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < UBV; ++k) {
+        if (xo[k] < 0) continue;
+        float4 u = bv[k];
+        if (L.nesterov)
+          u = make_float4(fmaf(mu, bv[k].x, coef * gv[k].x), fmaf(mu, bv[k].y, coef * gv[k].y),
+                          fmaf(mu, bv[k].z, coef * gv[k].z), fmaf(mu, bv[k].w, coef * gv[k].w));
+        if (!TALL) {
+          *reinterpret_cast<float4*>(XS + xo[k]) = u;  // X[i][j..j+3]
+        } else {
+          XS[xo[k]] = u.x;  // X[i..i+3][j]
+          XS[xo[k] + P] = u.y;
+          XS[xo[k] + 2 * P] = u.z;
+          XS[xo[k] + 3 * P] = u.w;
+        }
+        sq += (double)u.x * u.x + (double)u.y * u.y + (double)u.z * u.z + (double)u.w * u.w;
+      }
+    }
+    for (int e0 = 4 * words + threadIdx.x; e0 < cnt; e0 += UB * kNarrowThreads) {
       float gv[UB], bv[UB];
       int xo[UB];
 #pragma unroll
@@ -577,15 +627,16 @@ __device__ void resident_matrix(const NarrowLaunch& L, const MuonMat& M, int C, 
         }
       }
     }
-    double tot = narrow_block_sum(sq, red);  // also orders the writes of XS before the reads below
+    const double tot = narrow_block_sum(sq, red);  // also orders the writes of XS before the reads below
     if (C > 1) {
-      cg::cluster_group cl = cg::this_cluster();
+      // every CTA's sum of squares is read after the first Gram product, which
+      // does not need it (r enters as the factor r^2 of that A)
       if (threadIdx.x == 0) xch[0] = tot;
-      cl.sync();
-      tot = 0.0;
-      for (int q = 0; q < C; ++q) tot += *cl.map_shared_rank(xch, q);  // rank order: the same in every CTA
+      cluster_arrive();
+      r = 0.f;
+    } else {
+      r = (float)(1.0 / (sqrt(tot) + (double)L.eps));
     }
-    r = (float)(1.0 / (sqrt(tot) + (double)L.eps));
   }
   for (int it = 0; it < L.steps; ++it) {
     const bool first = it == 0;
@@ -596,6 +647,12 @@ __device__ void resident_matrix(const NarrowLaunch& L, const MuonMat& M, int C, 
     {
       float acc[4][4] = {};
       gram_chunk<false>(XS, P, lc, np, nq, ty, tx, acc);
+      if (first && C > 1) {
+        cluster_wait();
+        double tot = 0.0;
+        for (int q = 0; q < C; ++q) tot += *cg::this_cluster().map_shared_rank(xch, q);  // rank order everywhere
+        r = (float)(1.0 / (sqrt(tot) + (double)L.eps));
+      }
 #pragma unroll
       for (int p = 0; p < 4; ++p)
         reinterpret_cast<float4*>(PT)[p * kNarrowThreads + threadIdx.x] =
