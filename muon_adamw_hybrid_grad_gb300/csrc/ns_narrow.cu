@@ -662,12 +662,14 @@ __device__ void resident_matrix(const NarrowLaunch& L, const MuonMat& M, int C, 
     if (C > 1) {
       cg::cluster_group cl = cg::this_cluster();
       cl.sync();  // every partial written; the other tile's partials all read
-#pragma unroll 2
+      // row groups p >= np are zero in every partial: not read
+#pragma unroll 4
       for (int rk = 0; rk < C; ++rk) {
         const float4* rp = reinterpret_cast<const float4*>(cl.map_shared_rank(PT, rk));
         float4 w[4];
 #pragma unroll
-        for (int p = 0; p < 4; ++p) w[p] = rp[p * kNarrowThreads + threadIdx.x];
+        for (int p = 0; p < 4; ++p)
+          w[p] = p < np ? rp[p * kNarrowThreads + threadIdx.x] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
           sum[p][0] += w[p].x;
