@@ -507,7 +507,14 @@ def run_ours(args):
             d["frac_bf16_peak"] = round(d["tflops"] / tc_peak, 3)
             d["frac_bf16_burst"] = round(d["tflops"] / peaks["bf16_tflops"], 3)
         elif k == "ns_narrow":
+            # fp32 on the CUDA cores: "alu"-bound, against SMs x 128 fp32 lanes x 2 flops x the
+            # maximum SM clock (nvidia-smi's clocks.max.sm, else the part's nominal 2070 MHz)
             d["tflops_fp32"] = round(e["units"] / (e["ms"] / 1e3) / 1e12, 2)
+            mhz = clk.get("sm_max_mhz") or 2070.0
+            peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+            d["fp32_peak_tflops"] = round(peak, 1)
+            d["frac_fp32_peak"] = round(d["tflops_fp32"] / peak, 3)
+            d["bound"] = "alu"
         elif k in STREAM_KINDS:
             d["gbs"] = round(e["units"] / (e["ms"] / 1e3) / 1e9, 1)
             d["frac_hbm"] = round(d["gbs"] / peaks["hbm_gbs"], 3)
