@@ -1056,13 +1056,20 @@ __device__ __forceinline__ void small_get_row(const uint8_t* panels, int r, int 
 // row0 + l.
 __device__ __forceinline__ void small_apply_block(const MuonMat& M, float lrm, float dec, float rs, int row0,
                                                   int col0, uint32_t taddr, float (*t)[33], int lane) {
+  // the matrix's fields in registers: the stores below go through generic
+  // pointers that could otherwise alias the descriptor and force its reloads
+  float* const P = M.p;
+  uint16_t* const SH = M.shadow;
+  const size_t n = (size_t)M.n;
+  const int s = M.s, l = M.l;
+  const bool tr = M.transposed != 0;
   uint32_t v[32];
   tmem_ld_32x32b_x32(taddr, v);
   tmem_ld_wait();
   float o[32];
   int gc, nr;      // this lane's parameter column; rows of the block inside the parameter
   size_t base;     // parameter offset of the block's first row at this lane's column
-  if (!M.transposed) {
+  if (!tr) {
 #pragma unroll
     for (int e = 0; e < 32; ++e) t[lane][e] = __uint_as_float(v[e]) * rs;
     __syncwarp();
@@ -1070,27 +1077,27 @@ __device__ __forceinline__ void small_apply_block(const MuonMat& M, float lrm, f
     for (int r = 0; r < 32; ++r) o[r] = t[r][lane];
     __syncwarp();
     gc = col0 + lane;
-    nr = M.s - row0;
-    base = (size_t)row0 * M.n + gc;
-    if (gc >= M.l) nr = 0;
+    nr = s - row0;
+    base = (size_t)row0 * n + gc;
+    if (gc >= l) nr = 0;
   } else {
 #pragma unroll
     for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * rs;
     gc = row0 + lane;
-    nr = M.l - col0;
-    base = (size_t)col0 * M.n + gc;
-    if (gc >= M.s) nr = 0;
+    nr = l - col0;
+    base = (size_t)col0 * n + gc;
+    if (gc >= s) nr = 0;
   }
   if (nr > 32) nr = 32;
   float pv[32];
 #pragma unroll
-  for (int r = 0; r < 32; ++r) pv[r] = r < nr ? M.p[base + (size_t)r * M.n] : 0.f;
+  for (int r = 0; r < 32; ++r) pv[r] = r < nr ? P[base + (size_t)r * n] : 0.f;
 #pragma unroll
   for (int r = 0; r < 32; ++r) {
     if (r < nr) {
       const float q = fmaf(pv[r], dec, -lrm * o[r]);
-      M.p[base + (size_t)r * M.n] = q;
-      if (M.shadow) M.shadow[base + (size_t)r * M.n] = ns_f2bf(q);
+      P[base + (size_t)r * n] = q;
+      if (SH) SH[base + (size_t)r * n] = ns_f2bf(q);
     }
   }
 }
