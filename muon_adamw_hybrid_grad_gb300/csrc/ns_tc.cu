@@ -527,18 +527,28 @@ __device__ __forceinline__ void apply_block_direct(const MuonMat& M, const NsEpi
   uint32_t r[32];
   tmem_ld_32x32b_x32(taddr, r);
   tmem_ld_wait();
+  // the descriptor's fields in registers (the stores below could otherwise
+  // alias it), and every load issued before the first store
+  float* const P = M.p;
+  uint16_t* const SH = M.shadow;
+  const size_t n = (size_t)M.n;
+  const bool tr = M.transposed != 0;
   const int gi = row0 + lane;
   const int cnt = M.l - col0 < 32 ? M.l - col0 : 32;
   if (gi >= M.s || cnt <= 0) return;
   const float lrm = ep.sp->ns_lr * M.lr_mult;
   const float dec = ep.sp->ns_decay[M.group];
+  float pv[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    pv[e] = e < cnt ? P[tr ? (size_t)(col0 + e) * n + gi : (size_t)gi * n + col0 + e] : 0.f;
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     if (e < cnt) {
-      const size_t po = M.transposed ? (size_t)(col0 + e) * M.n + gi : (size_t)gi * M.n + col0 + e;
-      const float q = fmaf(M.p[po], dec, -lrm * (__uint_as_float(r[e]) * rs));
-      M.p[po] = q;
-      if (M.shadow) M.shadow[po] = ns_f2bf(q);
+      const size_t po = tr ? (size_t)(col0 + e) * n + gi : (size_t)gi * n + col0 + e;
+      const float q = fmaf(pv[e], dec, -lrm * (__uint_as_float(r[e]) * rs));
+      P[po] = q;
+      if (SH) SH[po] = ns_f2bf(q);
     }
   }
 }
@@ -1057,10 +1067,11 @@ __device__ __forceinline__ void small_get_row(const uint8_t* panels, int r, int 
 __device__ __forceinline__ void small_apply_block(const MuonMat& M, float lrm, float dec, float rs, int row0,
                                                   int col0, uint32_t taddr, float (*t)[33], int lane) {
   // the matrix's fields in registers: the stores below go through generic
-  // pointers that could otherwise alias the descriptor and force its reloads
+  // pointers that could otherwise alias the descriptor and force its reloads;
+  // offsets in 32 bits (a small matrix has at most 128 x 512 elements)
   float* const P = M.p;
   uint16_t* const SH = M.shadow;
-  const size_t n = (size_t)M.n;
+  const int n = M.n;
   const int s = M.s, l = M.l;
   const bool tr = M.transposed != 0;
   uint32_t v[32];
@@ -1068,7 +1079,7 @@ __device__ __forceinline__ void small_apply_block(const MuonMat& M, float lrm, f
   tmem_ld_wait();
   float o[32];
   int gc, nr;      // this lane's parameter column; rows of the block inside the parameter
-  size_t base;     // parameter offset of the block's first row at this lane's column
+  int base;        // parameter offset of the block's first row at this lane's column
   if (!tr) {
 #pragma unroll
     for (int e = 0; e < 32; ++e) t[lane][e] = __uint_as_float(v[e]) * rs;
@@ -1078,26 +1089,26 @@ __device__ __forceinline__ void small_apply_block(const MuonMat& M, float lrm, f
     __syncwarp();
     gc = col0 + lane;
     nr = s - row0;
-    base = (size_t)row0 * n + gc;
+    base = row0 * n + gc;
     if (gc >= l) nr = 0;
   } else {
 #pragma unroll
     for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * rs;
     gc = row0 + lane;
     nr = l - col0;
-    base = (size_t)col0 * n + gc;
+    base = col0 * n + gc;
     if (gc >= s) nr = 0;
   }
   if (nr > 32) nr = 32;
   float pv[32];
 #pragma unroll
-  for (int r = 0; r < 32; ++r) pv[r] = r < nr ? P[base + (size_t)r * n] : 0.f;
+  for (int r = 0; r < 32; ++r) pv[r] = r < nr ? P[base + r * n] : 0.f;
 #pragma unroll
   for (int r = 0; r < 32; ++r) {
     if (r < nr) {
       const float q = fmaf(pv[r], dec, -lrm * o[r]);
-      P[base + (size_t)r * n] = q;
-      if (SH) SH[base + (size_t)r * n] = ns_f2bf(q);
+      P[base + r * n] = q;
+      if (SH) SH[base + r * n] = ns_f2bf(q);
     }
   }
 }
