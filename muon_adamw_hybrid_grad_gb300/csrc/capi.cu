@@ -21,6 +21,7 @@
 #include <map>
 #include <new>
 #include <string>
+#include <type_traits>
 #include <utility>
 #include <vector>
 
@@ -215,18 +216,26 @@ cudaEvent_t take_event(muon_adamw* h) {
   return e;
 }
 
-// Launch helper: records a profiling event pair around `fn` when enabled.
+// Launch helper: records a profiling event pair around `fn` when enabled, and
+// returns the launch status `fn` returns (cudaSuccess for launchers that leave
+// a failure to the step's final cudaGetLastError).
 template <class F>
-void timed(muon_adamw* h, int kind, cudaStream_t st, double units, F&& fn) {
-  if (!h->profiling) {
-    fn();
-    return;
-  }
+cudaError_t timed(muon_adamw* h, int kind, cudaStream_t st, double units, F&& fn) {
+  auto call = [&]() -> cudaError_t {
+    if constexpr (std::is_same_v<decltype(fn()), void>) {
+      fn();
+      return cudaSuccess;
+    } else {
+      return fn();
+    }
+  };
+  if (!h->profiling) return call();
   ProfRec r{kind, take_event(h), take_event(h), units};
   if (r.a) cudaEventRecord(r.a, st);
-  fn();
+  const cudaError_t e = call();
   if (r.b) cudaEventRecord(r.b, st);
   if (r.a && r.b) h->prof_pending.push_back(r);
+  return e;
 }
 
 ma_status fold_profile(muon_adamw* h) {
@@ -936,15 +945,15 @@ static ma_status enqueue_newton_schulz(muon_adamw* h) {
         [&] { launch_ns_prep(h->d_mats, h->n_mats, h->d_tile_partials, (float)c.ns_eps, h->d_rscale, h->s0); });
   // narrow matrices: fp32 Newton-Schulz on the CUDA cores
   for (size_t i = 0; i < h->narrow.size(); ++i)
-    timed(h, MA_K_NS_NARROW, h->s0, h->narrow_units[i], [&] {
-      launch_ns_narrow(h->narrow[i], h->narrow_smem[i], h->num_sms, h->narrow_per_sm, h->s0);
-    });
+    CUDA_TRY(timed(h, MA_K_NS_NARROW, h->s0, h->narrow_units[i], [&] {
+      return launch_ns_narrow(h->narrow[i], h->narrow_smem[i], h->num_sms, h->narrow_per_sm, h->s0);
+    }));
   // buckets of small matrices: every iteration and the update in one launch each
   for (size_t i = 0; i < h->small.size(); ++i) {
     SmallLaunch& sl = h->small[i];
     sl.stall_test = h->stall_test ? 1 : 0;
     h->stall_test = false;  // one launch only
-    timed(h, MA_K_NS_FUSED, h->s0, h->small_units[i], [&] { launch_ns_small(sl, h->num_sms, h->s0); });
+    CUDA_TRY(timed(h, MA_K_NS_FUSED, h->s0, h->small_units[i], [&] { return launch_ns_small(sl, h->num_sms, h->s0); }));
   }
   NsEpiArgs epi;
   epi.sp = h->d_step;
@@ -958,7 +967,7 @@ static ma_status enqueue_newton_schulz(muon_adamw* h) {
           L.stall_test = h->stall_test ? 1 : 0;
           h->stall_test = false;  // one launch only
           const int pk = (kind == NS_UPDATE && it == c.ns_steps - 1) ? MA_K_NS_APPLY : MA_K_NS_GRAM + kind;
-          timed(h, pk, h->s0, units[kind] / h->tc[kind][it].size(), [&] { launch_ns_tc(L, h->s0); });
+          CUDA_TRY(timed(h, pk, h->s0, units[kind] / h->tc[kind][it].size(), [&] { return launch_ns_tc(L, h->s0); }));
         }
       } else {
         const int pk = (kind == NS_UPDATE && it == c.ns_steps - 1) ? MA_K_NS_APPLY : MA_K_NS_GRAM + kind;
