@@ -11,36 +11,40 @@
 // 4, and the rounding of X there is amplified to 2.3-2.7e-2 in Frobenius
 // norm. A matrix whose short side s is small and whose update is noise-like
 // has all its singular values near 1 / sqrt(s), which is that range for s of
-// about 25 to 55. Matrices with s < 64 therefore take this kernel, which keeps
+// about 25 to 55. Matrices with s < 64 therefore take this path, which keeps
 // X, A and B in fp32 throughout (an error near 1e-6). They are few and cheap:
 // a 40 x 2000 matrix costs about 2e8 flops per step.
 //
-// One CTA (256 threads) per matrix, over the matrix list in a grid-stride
-// loop; the host orders the list largest first. X lives in the matrix's fp32
-// workspace in the parameter's own layout (m x n, row-major). For a wide
-// matrix (m <= n) the canonical s x l X is that array; for a tall one it is
-// its transpose. A and B (s x s, padded to 64 x 64) are in shared memory;
-// 64-column chunks of X pass through shared memory for each product, and
-// X' = B X is written back in place chunk by chunk (a chunk of X' needs only
-// the same chunk of X).
+// Two kernels, both of 256-thread CTAs:
+//   ns_narrow_resident_kernel (below, after the shared helpers): a cluster of
+//     1 to 8 CTAs per matrix, each holding a slice of X's long side in shared
+//     memory for the whole chain; the partial Gram matrices are summed through
+//     distributed shared memory.
+//   ns_narrow_stream_kernel: one CTA per matrix, for matrices whose slices
+//     would not fit in 8 CTAs' shared memory. X lives in the matrix's fp32
+//     workspace in the parameter's own layout (m x n, row-major; for a wide
+//     matrix, m <= n, the canonical s x l X is that array, for a tall one its
+//     transpose). A and B (s x s, padded to 64 x 64) are in shared memory;
+//     64-column chunks of X pass through shared memory for each product, and
+//     X' = B X is written back in place chunk by chunk (a chunk of X' needs
+//     only the same chunk of X). Every chunk is fetched into registers one
+//     chunk ahead (four 16-byte words per thread), so the global loads of
+//     chunk c + 1 are in flight while chunk c is multiplied out of shared
+//     memory; each word goes to shared memory as one 16-byte store, in a
+//     layout chosen per orientation:
+//       wide:  the chunk as T[i][jj] for both products (rows of X);
+//       tall:  T[jj][4 (i mod 16) + i / 16] for X X^T (rows of the parameter,
+//              entries interleaved by the fetch), T[jj][i] for B X, which is
+//              computed as (B X)^T = X^T B and staged through a third tile
+//              so that it leaves along the parameter's rows.
 //
-// Latency: every chunk is fetched into registers one chunk ahead (four
-// 16-byte words per thread), so the global loads of chunk c + 1 are in flight
-// while chunk c is multiplied out of shared memory; each word goes to shared
-// memory as one 16-byte store, in a layout chosen per orientation:
-//   wide:  the chunk as T[i][jj] for both products (rows of X);
-//   tall:  T[jj][4 (i mod 16) + i / 16] for X X^T (rows of the parameter,
-//          entries interleaved by the fetch), T[jj][i] for B X, which is
-//          computed as (B X)^T = X^T B and staged through a third tile so
-//          that it leaves along the parameter's rows.
-//
-// Work split: thread (ty, tx) of the 16 x 16 grid holds rows ty + 16 p
-// (p < 4) of each 64-row result. Rows interleave so that a short side s < 64
-// leaves every warp with ceil((s - row) / 16) live row groups, the same count
-// on all four schedulers; a warp skips the groups that lie wholly in the zero
-// padding, the Gram product skips the column groups tx + 16 q >= s (the same
-// for every thread), and A A and B X stop their reductions at s rounded up
-// to 4.
+// Work split (both kernels): thread (ty, tx) of the 16 x 16 grid holds rows
+// ty + 16 p (p < 4) of each 64-row result. Rows interleave so that a short
+// side s < 64 leaves every warp with ceil((s - row) / 16) live row groups, the
+// same count on all four schedulers; a warp skips the groups that lie wholly
+// in the zero padding, the Gram product skips the column groups tx + 16 q >= s
+// (the same for every thread), and A A and B X stop their reductions at s
+// rounded up to 4.
 //
 // The update G is recomputed from the momentum buffer that the momentum pass
 // has just written and the gradient, with the same fp32 operations that pass
