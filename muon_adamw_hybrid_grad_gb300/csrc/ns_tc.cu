@@ -1113,6 +1113,17 @@ __device__ __forceinline__ void small_apply_block(const MuonMat& M, float lrm, f
   }
 }
 
+// L1 prefetch of a 32 x 32 parameter block of a small matrix (the layout of
+// small_apply_block): lane r takes the 128 bytes of the block's r-th
+// parameter row, so the block's loads find it close when they come.
+__device__ __forceinline__ void small_prefetch_block(const MuonMat& M, int row0, int col0, int lane) {
+  const bool tr = M.transposed != 0;
+  const int pr = tr ? col0 + lane : row0 + lane;  // parameter row of this lane
+  const int pc = tr ? row0 : col0;                // first parameter column of the block
+  if (pr < M.m && pc < M.n)
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(M.p + (size_t)pr * M.n + pc) : "memory");
+}
+
 // Every thread waits for phase `parity` of `bar`; false on the CTA when any
 // thread's bounded wait ran out (the error is recorded), so all leave together.
 __device__ __forceinline__ bool small_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
@@ -1267,6 +1278,8 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) ns_small_kernel(const __grid
       fence_proxy_async_smem();
       tc_fence_before();
       __syncthreads();
+      // the last iteration's update starts with this warp's first parameter block
+      if (last && warp >= 1) small_prefetch_block(M, 32 * quarter, 32 * half, lane);
       // ---- X' = B X (columns 0..L-1) ----
       if (threadIdx.x == 0) {
         tc_fence_after();
@@ -1324,8 +1337,10 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) ns_small_kernel(const __grid
           const float rs = first ? r : 1.f;
           const float lrm = L.sp->ns_lr * M.lr_mult;
           const float dec = L.sp->ns_decay[M.group];
-          for (int c0 = 32 * half; c0 < l; c0 += 64)
+          for (int c0 = 32 * half; c0 < l; c0 += 64) {
+            if (c0 + 64 < l) small_prefetch_block(M, 32 * quarter, c0 + 64, lane);  // the next block
             small_apply_block(M, lrm, dec, rs, 32 * quarter, c0, tq + (uint32_t)c0, t, lane);
+          }
         }
       }
       tc_fence_before();
