@@ -737,7 +737,6 @@ ma_status build_plan(muon_adamw* h) {
       base.coef[it][2] = e.c;
     }
     std::vector<int32_t> idx;
-    size_t max_smem = 0;
     for (int cl : {8, 4, 2, 1, 0}) {
       const size_t first = idx.size();
       size_t smem = 0;
@@ -758,10 +757,12 @@ ma_status build_plan(muon_adamw* h) {
       h->narrow.push_back(nl);
       h->narrow_smem.push_back(smem);
       h->narrow_units.push_back(units);
-      max_smem = std::max(max_smem, smem);
     }
     CUDA_TRY(cudaMemcpy(h->d_narrow_idx, idx.data(), idx.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
-    CUDA_TRY(ns_narrow_prepare(max_smem, &h->narrow_per_sm));
+    // the resident kernel's shared-memory ceiling at the largest any plan uses:
+    // the attribute is per device, and another handle's plan may need more
+    // than this one's (it allows, and reserves nothing)
+    CUDA_TRY(ns_narrow_prepare(kNarrowMaxSmem, &h->narrow_per_sm));
   }
   h->small.clear();
   for (Bucket& B : h->buckets) {

@@ -209,6 +209,42 @@ def test_narrow_matrices_fp32_newton_schulz(mx, ns_kernel):
         gpu.close()
 
 
+def test_narrow_plans_of_two_handles_share_the_device(mx):
+    """The resident narrow kernel's shared-memory ceiling is a per-device
+    attribute: a handle whose narrow matrices need less (1000 x 40, 85 KB per
+    CTA) must not lower it under another's (40 x 8000 in clusters of 8 at
+    227 KB per CTA). The big handle, stepped around the small one's plan and
+    step, matches bit for bit the same steps on a handle of its own."""
+    big = workloads.custom_workload(
+        "narrow_big", [TensorSpec("model.action_expert.layers.0.mlp.w_big.weight", (40, 8000), rank8=True)],
+        policy="bf16_mixed", steps=2)
+    small = workloads.custom_workload(
+        "narrow_small", [TensorSpec("model.action_expert.layers.0.mlp.w_small.weight", (1000, 40), rank8=True)],
+        policy="bf16_mixed", steps=1)
+
+    def run(interleave):
+        g = GpuSide(big, workloads.master_weights(big))
+        try:
+            g.load_grads(workloads.gradients(big, 1))
+            g.step(big.lr)
+            if interleave:
+                o = GpuSide(small, workloads.master_weights(small))
+                try:
+                    o.load_grads(workloads.gradients(small, 1))
+                    o.step(small.lr)
+                finally:
+                    o.close()
+            g.load_grads(workloads.gradients(big, 2))
+            g.step(big.lr)
+            return g.param(0)
+        finally:
+            g.close()
+
+    alone, shared = run(False), run(True)
+    assert not np.array_equal(alone, workloads.master_weights(big)[0])
+    assert np.array_equal(alone, shared)
+
+
 def test_fp32_gradients(mx):
     w = workloads.get_workload("tiny")
     w = workloads.custom_workload("tiny_fp32g", w.tensors, grad_dtype="fp32", policy="fp32_mixed", steps=2)
