@@ -246,6 +246,49 @@ def test_narrow_plans_of_two_handles_share_the_device(mx):
     assert np.array_equal(alone, shared)
 
 
+def test_gpu_orthogonalised_update_singular_values_in_band(mx):
+    """OpenDM article, Muon 的工作原理: the quintic X <- a X + (b A + c A A) X
+    maps each singular value x of the normalised update to phi(x) = a x +
+    b x^3 + c x^5 and keeps the singular vectors, so five steps give
+    phi^5(x). On x in [0.003, 1] phi^5 lies in a band near 1 (computed here
+    on a fine grid); the GPU's O, recovered from the fp32 parameter update,
+    keeps its singular values inside that band up to the 2e-2 that bf16
+    storage allows, for inputs whose smallest normalised singular value is
+    at least 0.003 (rectangular matrices, both orientations, on the
+    tensor-core, small-matrix and narrow paths)."""
+    import torch  # noqa: F401  (GpuSide holds torch tensors)
+
+    a, b, c = 3.4445, -4.7750, 2.0315
+    x = np.concatenate([np.linspace(0.003, 0.05, 20001), np.linspace(0.05, 1.0, 20001)])
+    y = x.copy()
+    for _ in range(5):
+        y = a * y + b * y ** 3 + c * y ** 5
+    lo, hi = float(y.min()), float(y.max())
+    assert 0.6 < lo < 0.75 and 1.1 < hi < 1.3
+    shapes = [(1024, 256), (256, 1024), (640, 384), (128, 512), (512, 128), (1000, 40)]
+    t = [TensorSpec(f"model.action_expert.layers.{k}.mlp.w{k}.weight", sh) for k, sh in enumerate(shapes)]
+    w = workloads.custom_workload("band", t, policy="fp32_mixed", steps=1)
+    masters = workloads.master_weights(w)
+    gpu = GpuSide(w, masters)
+    try:
+        grads = workloads.gradients(w, 1)
+        gpu.load_grads(grads)
+        gpu.step(w.lr)
+        cfg = gpu.opt.cfg
+        f32 = np.float32
+        for i, (m_, n_) in enumerate(shapes):
+            g = grads[i].astype(np.float64)
+            sg = np.linalg.svd(g, compute_uv=False)
+            assert sg.min() / np.linalg.norm(g) >= 0.003, shapes[i]  # the band's premise
+            decay = float(f32(1.0 - w.lr * cfg.muon_weight_decay))
+            lr_mult = float(f32(cfg.muon_lr_scale * cfg.moonlight_coef * math.sqrt(max(m_, n_))))
+            O = (masters[i].astype(np.float64) * decay - gpu.param(i)) / (float(f32(w.lr)) * lr_mult)
+            so = np.linalg.svd(O, compute_uv=False)
+            assert lo - 2e-2 <= so.min() and so.max() <= hi + 2e-2, (shapes[i], so.min(), so.max(), lo, hi)
+    finally:
+        gpu.close()
+
+
 def test_fp32_gradients(mx):
     w = workloads.get_workload("tiny")
     w = workloads.custom_workload("tiny_fp32g", w.tensors, grad_dtype="fp32", policy="fp32_mixed", steps=2)
