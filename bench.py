@@ -93,6 +93,25 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def blas_threads() -> dict:
+    """Threads of the BLAS behind the oracle's matrix products: from
+    threadpoolctl where it is installed, else the thread-count environment
+    variables, else the library's default of one thread per available core."""
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return {"blas_threads": int(max(n)), "blas_threads_source": "threadpoolctl"}
+    except Exception:
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(k)
+        if v and v.isdigit():
+            return {"blas_threads": int(v), "blas_threads_source": k}
+    return {"blas_threads": host_cores(), "blas_threads_source": "default: one per available core"}
+
+
 # ---------------------------------------------------------------------------
 # multi-rank plumbing (replicas only)
 # ---------------------------------------------------------------------------
@@ -603,7 +622,7 @@ def run_ours(args):
         smp = OracleSample(w)
         runs = [smp.run() for _ in range(args.cpu_repeats)]
         full = statistics.median(r[1] for r in runs)
-        out["cpu_baseline"] = {"value": round(1.0 / full, 6), "unit": "steps/s", "cores": host_cores(),
+        out["cpu_baseline"] = {"value": round(1.0 / full, 6), "unit": "steps/s", "cores": host_cores(), **blas_threads(),
                                "kind": "oracle", "extrapolated": not smp.whole,
                                "sample": f"{smp.desc}; median of {len(runs)} passes, each "
                                          f"{statistics.median(r[0] for r in runs):.2f} s of oracle work"}
@@ -650,7 +669,7 @@ def run_reference(args):
                    "full_step_s_estimated": round(full / args.steps, 4), "wall_s_timed_region": round(t_wall, 3),
                    "how": "each timed step runs the sample once (ms_per_step is its time); value is the "
                           "estimated rate of whole optimizer steps"},
-        "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": host_cores(), "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": host_cores(), **blas_threads(), "kind": "oracle",
                          "extrapolated": not smp.whole, "sample": smp.desc},
         "e2e": {"value": round(value, 6), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
