@@ -93,6 +93,43 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def pinned_host_buffer(numel: int, dtype):
+    """Host buffer of the end-to-end leg's per-step gradient copy: anonymous
+    memory advised to transparent huge pages (where the kernel grants them)
+    and page-locked with cudaHostRegister, which keeps the host->device copy's
+    address translation to a few large pages; plain pinned memory
+    (cudaHostAlloc) where that fails. Returns (tensor, kind, release)."""
+    import mmap
+
+    import torch
+
+    esz = torch.tensor([], dtype=dtype).element_size()
+    numel = max(int(numel), 1)
+    size = numel * esz
+    try:
+        mm = mmap.mmap(-1, size, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        advised = False
+        if hasattr(mmap, "MADV_HUGEPAGE"):
+            try:
+                mm.madvise(mmap.MADV_HUGEPAGE)
+                advised = True
+            except OSError:
+                pass
+        t = torch.frombuffer(mm, dtype=dtype, count=numel)
+        t.zero_()  # every page present before it is locked
+        cudart = torch.cuda.cudart()
+        if int(cudart.cudaHostRegister(t.data_ptr(), size, 0)) != 0:
+            raise RuntimeError("cudaHostRegister failed")
+        kind = ("anonymous memory advised to huge pages" if advised else "anonymous memory") + ", cudaHostRegister"
+
+        def release(t=t, mm=mm):
+            cudart.cudaHostUnregister(t.data_ptr())
+
+        return t, kind, release
+    except Exception:
+        return torch.zeros(numel, dtype=dtype).pin_memory(), "pinned (cudaHostAlloc)", lambda: None
+
+
 def blas_threads() -> dict:
     """Threads of the BLAS behind the oracle's matrix products: from
     threadpoolctl where it is installed, else the thread-count environment
@@ -381,7 +418,7 @@ def run_ours(args):
         if not t.frozen:
             total += (t.numel + align - 1) // align * align
     gflat = torch.zeros(max(total, 1), dtype=gdt, device=dev)
-    hflat = torch.zeros(max(total, 1), dtype=gdt).pin_memory()
+    hflat, host_kind, host_release = pinned_host_buffer(total, gdt)
     n = len(w.tensors)
     P, G, S, entries = [None] * n, [None] * n, [None] * n, [None] * n
     for batch in _batches(range(n)):
@@ -609,6 +646,7 @@ def run_ours(args):
                 "gradient_copy_ms_max": round(max(a.elapsed_time(b) for a, b in cev), 3),
                 "host_step_ms_median": round(statistics.median(step_host), 3),
                 "host_step_ms_max": round(max(step_host), 3),
+                "host_buffer": host_kind,
                 "how": "every step: every gradient copied host->device from pinned memory (one copy of the "
                        "flat gradient buffer, issued once the previous step has read its gradients and "
                        "overlapping that step's Newton-Schulz chain), muon_adamw_step, and the step's norm "
@@ -618,6 +656,7 @@ def run_ours(args):
     }
     opt.close()
     del opt
+    host_release()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleSample(w)
         runs = [smp.run() for _ in range(args.cpu_repeats)]
