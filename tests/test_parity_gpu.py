@@ -289,6 +289,48 @@ def test_gpu_orthogonalised_update_singular_values_in_band(mx):
         gpu.close()
 
 
+def test_large_matrices_norm_and_band(mx):
+    """Larger than any configuration: Muon matrices of 4096 x 16384 and
+    16384 x 4096 (67 M elements each; 16 x 16 output units of the symmetric
+    products, K up to 16384), where the fp64 oracle's Newton-Schulz would
+    take minutes. Checked by what holds at any size: the step's norm against
+    the fp64 sum over the gradients, and every singular value of the
+    orthogonalised update (recovered from the fp32 parameter update; SVD on
+    the GPU in fp32) inside phi^5([0.003, 1]) with the 2e-2 bf16 slack
+    (OpenDM article, Muon 的工作原理; the inputs' smallest normalised singular
+    value is about 0.008)."""
+    import torch
+
+    a, b, c = 3.4445, -4.7750, 2.0315
+    x = np.concatenate([np.linspace(0.003, 0.05, 20001), np.linspace(0.05, 1.0, 20001)])
+    y = x.copy()
+    for _ in range(5):
+        y = a * y + b * y ** 3 + c * y ** 5
+    lo, hi = float(y.min()), float(y.max())
+    shapes = [(4096, 16384), (16384, 4096)]
+    t = [TensorSpec(f"model.action_expert.layers.{k}.mlp.w{k}.weight", sh) for k, sh in enumerate(shapes)]
+    w = workloads.custom_workload("large", t, policy="fp32_mixed", steps=1)
+    masters = workloads.master_weights(w)
+    gpu = GpuSide(w, masters)
+    try:
+        grads = workloads.gradients(w, 1)
+        gpu.load_grads(grads)
+        norm = gpu.step(w.lr)
+        want = math.sqrt(sum(float(np.sum(np.square(g.astype(np.float64)))) for g in grads))
+        assert math.isclose(norm, want, rel_tol=1e-5)
+        cfg = gpu.opt.cfg
+        f32 = np.float32
+        for i, (m_, n_) in enumerate(shapes):
+            decay = float(f32(1.0 - w.lr * cfg.muon_weight_decay))
+            lr_mult = float(f32(cfg.muon_lr_scale * cfg.moonlight_coef * math.sqrt(max(m_, n_))))
+            p0 = torch.from_numpy(masters[i]).to("cuda", torch.float64)
+            O = (p0 * decay - gpu.P[i].to(torch.float64)) / (float(f32(w.lr)) * lr_mult)
+            so = torch.linalg.svdvals(O.to(torch.float32)).cpu().numpy()
+            assert lo - 2e-2 <= so.min() and so.max() <= hi + 2e-2, (shapes[i], so.min(), so.max())
+    finally:
+        gpu.close()
+
+
 def test_fp32_gradients(mx):
     w = workloads.get_workload("tiny")
     w = workloads.custom_workload("tiny_fp32g", w.tensors, grad_dtype="fp32", policy="fp32_mixed", steps=2)
