@@ -715,6 +715,86 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_shard_projection(args):
+    """Per-rank compute of the sharded step, projected on one GPU (not a
+    multi-GPU measurement): the ranks of a world run one after another on one
+    GPU, sharing the parameter tensors (each writes only what it owns), none
+    waiting on another. Each rank's step_begin + step_end is timed with CUDA
+    events (median of `--steps` steps after `--warmup`); the collectives are
+    not included. Prints one JSON line."""
+    import statistics
+
+    import torch
+
+    import muon_adamw_hybrid_grad_gb300 as mx
+    import workloads
+
+    mx.load_library()
+    w = workloads.get_workload(args.workload)
+    lr = w.lr
+    if w.schedule is not None:
+        step_, total_, warm_, min_rate = w.schedule
+        lr = w.lr * mx.muon_adamw_cosine_with_min_lr(step_, total_, warm_, min_rate)
+    dev = torch.device("cuda")
+    gdt = torch.bfloat16 if w.grad_dtype == "bf16" else torch.float32
+    n = len(w.tensors)
+    entries = [None] * n
+    for batch in _batches(range(n)):
+        ms = workloads.master_weights(w, batch)
+        gs = workloads.gradients(w, 1, batch)
+        for i, m, g in zip(batch, ms, gs):
+            t = w.tensors[i]
+            p = torch.from_numpy(m).to(dev)
+            gt = None if t.frozen else torch.from_numpy(g).to(gdt).to(dev)
+            sh = torch.empty(t.shape, dtype=torch.bfloat16, device=dev) if (w.policy == "bf16_mixed" and not t.frozen) else None
+            entries[i] = (t.name, p, gt, sh, mx.MA_GROUP_FROZEN if t.frozen else None)
+        del ms, gs
+    prec = mx.MA_BF16_MIXED if w.policy == "bf16_mixed" else mx.MA_FP32_MIXED
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    out = {"shard_projection": {"workload": args.workload, "steps": args.steps, "warmup": args.warmup,
+                                "how": run_shard_projection.__doc__.split("\n\n")[0].replace("\n", " ")}}
+    opt = mx.MuonAdamW(entries, precision=prec, stream=stream)
+    ts = []
+    for k in range(args.warmup + args.steps):
+        a, b = ev(), ev()
+        a.record(stream)
+        opt.step(lr)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            ts.append(a.elapsed_time(b))
+    opt.close()
+    out["shard_projection"]["world1_ms"] = round(statistics.median(ts), 3)
+    for world in (2, 4, 8):
+        opts = [mx.MuonAdamW(entries, precision=prec, stream=stream, shard=(r, world)) for r in range(world)]
+        loc = [torch.zeros(1, dtype=torch.float64, device=dev) for _ in range(world)]
+        per = [[] for _ in range(world)]
+        for k in range(args.warmup + args.steps):
+            eb = [(ev(), ev()) for _ in range(world)]
+            ee = [(ev(), ev()) for _ in range(world)]
+            for r in range(world):
+                eb[r][0].record(stream)
+                opts[r].step_begin(lr, loc[r])
+                eb[r][1].record(stream)
+            tot = sum(loc[1:], loc[0].clone())  # what the all-reduce returns
+            for r in range(world):
+                ee[r][0].record(stream)
+                opts[r].step_end(tot)
+                ee[r][1].record(stream)
+            torch.cuda.synchronize()
+            if k >= args.warmup:
+                for r in range(world):
+                    per[r].append(eb[r][0].elapsed_time(eb[r][1]) + ee[r][0].elapsed_time(ee[r][1]))
+        for o in opts:
+            o.close()
+        med = [statistics.median(x) for x in per]
+        out["shard_projection"][f"world{world}"] = {
+            "rank_ms": [round(x, 3) for x in med], "max_ms": round(max(med), 3),
+            "mean_ms": round(sum(med) / world, 3), "max_over_mean": round(max(med) / (sum(med) / world), 3)}
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -724,6 +804,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-repeats", type=int, default=2, help="passes of the oracle sample for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shard-projection", action="store_true",
+                    help="instead of the benchmark: per-rank compute of the sharded step for worlds of 2, 4 "
+                         "and 8, projected on one GPU (ranks run one after another)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -732,7 +815,11 @@ def main(argv=None):
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE is {world}: launch one process per GPU, e.g. "
                  f"python -m torch.distributed.run --nnodes=1 --nproc-per-node {args.gpus} --master-addr 127.0.0.1 "
                  f"bench.py --gpus {args.gpus}")
-    if args.impl == "reference":
+    if args.shard_projection:
+        if world != 1:
+            ap.error("--shard-projection runs on one GPU")
+        run_shard_projection(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
