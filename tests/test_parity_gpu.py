@@ -43,6 +43,20 @@ def test_tiny_three_steps(mx, ns_kernel, policy):
     assert r["worst_o"] <= O_TOL
 
 
+def test_twenty_steps_every_path(mx):
+    """Twenty steps of the tiny workload plus a small and a narrow matrix (the
+    tensor-core, small-matrix and narrow paths), against the oracle at every
+    step: each step's rounding is carried into the next by the recurrences,
+    and the state bounds carry it the same way, so a drift that a few steps
+    would not show fails here."""
+    tiny = workloads.get_workload("tiny")
+    extra = [TensorSpec("model.action_expert.layers.2.mlp.w_small.weight", (128, 512), rank8=True),
+             TensorSpec("model.action_expert.layers.2.mlp.w_narrow.weight", (1000, 40), rank8=True)]
+    w = workloads.custom_workload("tiny20", list(tiny.tensors) + extra, policy="bf16_mixed", steps=20)
+    r = run_parity(w)
+    assert r["worst_o"] <= O_TOL
+
+
 def _many_small_reduced():
     lens = workloads.many_small_lengths()[:256]
     t = [TensorSpec(f"model.action_expert.layers.{k}.w_a.weight", (128, 512)) for k in range(64)]
