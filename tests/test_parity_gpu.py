@@ -686,6 +686,21 @@ SCHEDULE = [(3.4445, -4.7750, 2.0315)] * 3 + [(3.0, -3.2, 1.2), (1.875, -1.25, 0
 
 
 @pytest.mark.parametrize("ns_kernel", KERNELS, ids=lambda k: KNAMES[k])
+def test_plain_momentum_without_nesterov(mx, ns_kernel):
+    """muon_nesterov off (OpenDM article, 关键超参默认值 names the switch):
+    the update is the momentum buffer itself, u = mu buf + g; through the
+    momentum pass, the fused small-matrix kernel and the narrow kernel (which
+    recompute u from buf), against the oracle over three steps."""
+    tiny = workloads.get_workload("tiny")
+    extra = [TensorSpec("model.action_expert.layers.2.mlp.w_small.weight", (128, 512), rank8=True),
+             TensorSpec("model.action_expert.layers.2.mlp.w_narrow.weight", (1000, 40), rank8=True)]
+    w = workloads.custom_workload("tiny_plain", list(tiny.tensors) + extra, policy="bf16_mixed", steps=3)
+    r = run_parity(w, config={"ns_kernel": ns_kernel, "muon_nesterov": 0},
+                   oracle_overrides={"muon_nesterov": False})
+    assert r["worst_o"] <= O_TOL
+
+
+@pytest.mark.parametrize("ns_kernel", KERNELS, ids=lambda k: KNAMES[k])
 def test_ema_momentum_and_coefficient_schedule(mx, ns_kernel):
     w = workloads.get_workload("tiny")
     w = workloads.custom_workload("tiny", w.tensors, policy="bf16_mixed", steps=3)
