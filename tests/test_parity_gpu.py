@@ -686,6 +686,30 @@ SCHEDULE = [(3.4445, -4.7750, 2.0315)] * 3 + [(3.0, -3.2, 1.2), (1.875, -1.25, 0
 
 
 @pytest.mark.parametrize("ns_kernel", KERNELS, ids=lambda k: KNAMES[k])
+def test_every_hyperparameter_off_its_default(mx, ns_kernel):
+    """Every numeric hyperparameter of the configuration away from its
+    default at once (momentum, the 0.2 coefficient, muon_lr_scale, both
+    weight decays, both betas, both epsilons, the clip threshold and the
+    quintic's coefficients), on every Newton-Schulz path, against the oracle
+    given the same values: no kernel holds a default of its own."""
+    tiny = workloads.get_workload("tiny")
+    extra = [TensorSpec("model.action_expert.layers.2.mlp.w_small.weight", (128, 512), rank8=True),
+             TensorSpec("model.action_expert.layers.2.mlp.w_narrow.weight", (1000, 40), rank8=True)]
+    w = workloads.custom_workload("tiny_hp", list(tiny.tensors) + extra, policy="bf16_mixed", steps=3)
+    abc = (3.0, -3.2, 1.2)
+    config = {"ns_kernel": ns_kernel, "muon_momentum": 0.9, "moonlight_coef": 0.3, "muon_lr_scale": 1.5,
+              "muon_weight_decay": 0.05, "adam_beta1": 0.85, "adam_beta2": 0.99, "adam_eps": 1e-6,
+              "adam_weight_decay": 0.02, "ns_eps": 1e-6, "max_grad_norm": 0.5,
+              "ns_a": abc[0], "ns_b": abc[1], "ns_c": abc[2]}
+    overrides = {"muon_momentum": 0.9, "muon_moonlight_coefficient": 0.3, "muon_lr_scale": 1.5,
+                 "muon_weight_decay": 0.05, "adam_betas": (0.85, 0.99), "adam_eps": 1e-6, "weight_decay": 0.02,
+                 "ns_eps": 1e-6, "max_grad_norm": 0.5, "ns_coefficients": abc}
+    r = run_parity(w, config=config, oracle_overrides=overrides, grad_scale=50.0, lr=2e-3)
+    assert r["worst_o"] <= O_TOL
+    assert r["o_errors"][len(w.tensors) - 1] <= 1e-4  # the narrow matrix: fp32 throughout (either setting)
+
+
+@pytest.mark.parametrize("ns_kernel", KERNELS, ids=lambda k: KNAMES[k])
 def test_plain_momentum_without_nesterov(mx, ns_kernel):
     """muon_nesterov off (OpenDM article, 关键超参默认值 names the switch):
     the update is the momentum buffer itself, u = mu buf + g; through the
