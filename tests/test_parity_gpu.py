@@ -745,6 +745,23 @@ def _options_workload():
     return workloads.custom_workload("options", t, policy="bf16_mixed", steps=3)
 
 
+def test_param_options_on_small_and_narrow_matrices(mx):
+    """Per-parameter (lr_scale, weight_decay_scale) on matrices of the fused
+    small-matrix kernel and of the narrow kernel (clusters of 4 and of 2),
+    which apply the update in their own epilogues, against the oracle given
+    the same options; the narrow ones within 1e-4 (fp32 throughout)."""
+    t = [TensorSpec("model.action_expert.layers.0.mlp.w_small.weight", (128, 512), rank8=True),
+         TensorSpec("model.action_expert.layers.0.mlp.w_narrow.weight", (1000, 40), rank8=True),
+         TensorSpec("model.action_expert.layers.0.mlp.w_narrow2.weight", (40, 300), rank8=True),
+         TensorSpec("model.action_expert.layers.0.self_attn.q_proj.weight", (256, 256)),
+         TensorSpec("model.action_expert.layers.0.input_layernorm.weight", (256,))]
+    w = workloads.custom_workload("options_small", t, policy="bf16_mixed", steps=3)
+    opts = {0: (2.0, 0.0), 1: (0.5, 3.0), 2: (1.5, 2.0), 3: (0.25, 1.0)}
+    r = run_parity(w, param_options=opts, lr=2e-3)
+    assert r["worst_o"] <= O_TOL
+    assert r["o_errors"][1] <= 1e-4 and r["o_errors"][2] <= 1e-4, r["o_errors"]
+
+
 def test_param_options_and_decay_exemption(mx):
     """Per-parameter (lr_scale, weight_decay_scale) on Muon and AdamW
     parameters, the bias/norm exemption rule, and an explicit option that
