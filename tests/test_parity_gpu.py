@@ -724,6 +724,29 @@ def test_plain_momentum_without_nesterov(mx, ns_kernel):
     assert r["worst_o"] <= O_TOL
 
 
+@pytest.mark.parametrize("variant", ["ema_schedule", "one_step", "three_steps"])
+def test_narrow_kernels_variants(mx, variant):
+    """The narrow kernels (resident, in clusters of 4 and 2, and streaming)
+    with the exponential-average momentum and a per-iteration coefficient
+    schedule, and with one and three iterations (one: the first iteration's
+    scale and the parameter update in the same pass), against the oracle
+    within 1e-4."""
+    t = [TensorSpec("model.action_expert.layers.0.mlp.w_a.weight", (1000, 40), rank8=True),
+         TensorSpec("model.action_expert.layers.0.mlp.w_b.weight", (40, 300), rank8=True),
+         TensorSpec("model.action_expert.layers.0.mlp.w_c.weight", (9000, 40), rank8=True),
+         TensorSpec("model.action_expert.layers.0.input_layernorm.weight", (40,))]
+    w = workloads.custom_workload("narrow_variants", t, policy="bf16_mixed", steps=3)
+    if variant == "ema_schedule":
+        config = {"muon_momentum_form": "ema", "ns_schedule": SCHEDULE}
+        overrides = {"muon_momentum_form": "ema", "ns_schedule": SCHEDULE}
+    else:
+        k = 1 if variant == "one_step" else 3
+        config, overrides = {"ns_steps": k}, {"muon_ns_steps": k}
+    r = run_parity(w, config=config, oracle_overrides=overrides, lr=2e-3)
+    for i in range(3):
+        assert r["o_errors"][i] <= 1e-4, (variant, t[i].shape, r["o_errors"][i])
+
+
 @pytest.mark.parametrize("ns_kernel", KERNELS, ids=lambda k: KNAMES[k])
 def test_ema_momentum_and_coefficient_schedule(mx, ns_kernel):
     w = workloads.get_workload("tiny")
