@@ -351,6 +351,25 @@ def test_fp32_gradients(mx):
     run_parity(w)
 
 
+def test_fp32_gradients_small_and_narrow(mx):
+    """fp32 gradients into the fused small-matrix kernel's momentum pass and
+    into the narrow kernels, which read the gradient themselves: 16-byte
+    words where the rows allow (1000 x 40, 37 x 300), single elements where
+    they do not (300 x 37), and the streaming kernel (9000 x 40); the narrow
+    ones within 1e-4."""
+    t = [TensorSpec("model.action_expert.layers.0.mlp.w_s.weight", (128, 512), rank8=True),
+         TensorSpec("model.action_expert.layers.0.mlp.w_a.weight", (1000, 40), rank8=True),
+         TensorSpec("model.action_expert.layers.0.mlp.w_b.weight", (37, 300), rank8=True),
+         TensorSpec("model.action_expert.layers.0.mlp.w_c.weight", (300, 37), rank8=True),
+         TensorSpec("model.action_expert.layers.0.mlp.w_d.weight", (9000, 40), rank8=True),
+         TensorSpec("model.action_expert.layers.0.input_layernorm.weight", (40,))]
+    w = workloads.custom_workload("small_narrow_fp32g", t, grad_dtype="fp32", policy="bf16_mixed", steps=2)
+    r = run_parity(w, lr=2e-3)
+    assert r["worst_o"] <= O_TOL
+    for i in range(1, 5):
+        assert r["o_errors"][i] <= 1e-4, (t[i].shape, r["o_errors"][i])
+
+
 def test_h1024_full_size_sampled(mx):
     """The benchmark workload at full size (16 layers, 268 M Muon elements):
     every momentum and AdamW element checked; O checked on layers 0, 8, 15
