@@ -1,6 +1,7 @@
 """The sharded step on one GPU: two or three handles act as the ranks of a
 world of that size, one after the other on the same stream (no kernel waits
-for another). Each has its own copy of the parameters and reads the same
+for another). The matrices take every Newton-Schulz path: tensor-core,
+fused small-matrix (128 x 512) and narrow (1000 x 40). Each has its own copy of the parameters and reads the same
 gradients; the host sums their local sums of squares (what an all-reduce
 does) and copies each rank's updated parts to the others (what the exchange
 does). Checked against the
@@ -36,6 +37,8 @@ def mx():
 def _workload():
     base = workloads.get_workload("tiny")
     t = list(base.tensors) + [TensorSpec("model.action_expert.layers.2.wq.weight", (384, 640), rank8=True),
+                              TensorSpec("model.action_expert.layers.2.w_small.weight", (128, 512), rank8=True),
+                              TensorSpec("model.action_expert.layers.2.w_narrow.weight", (1000, 40), rank8=True),
                               TensorSpec("model.vlm.v.weight", (100003,)), TensorSpec("model.vlm.b.bias", (77,))]
     return workloads.custom_workload("tiny_shard", t, policy="bf16_mixed", steps=2)
 
