@@ -521,8 +521,27 @@ def test_inf_gradient_zero_clip(mx):
         gpu.close()
 
 
+def _all_paths_workload():
+    """Small matrices of both orientations, tensor-core matrices (single CTAs
+    and CTA pairs), narrow matrices in clusters of 4 and 8 and one for the
+    streaming kernel, and AdamW vectors."""
+    lens = workloads.many_small_lengths()[:64]
+    t = [TensorSpec(f"model.action_expert.layers.{k}.w_a.weight", (128, 512)) for k in range(8)]
+    t += [TensorSpec(f"model.action_expert.layers.{8 + k}.w_b.weight", (512, 128)) for k in range(4)]
+    t += [TensorSpec("model.action_expert.layers.20.wq.weight", (384, 640), rank8=True),
+          TensorSpec("model.action_expert.layers.20.wk.weight", (512, 1024), rank8=True),
+          TensorSpec("model.action_expert.layers.20.w_n1.weight", (1000, 40), rank8=True),
+          TensorSpec("model.action_expert.layers.20.w_n2.weight", (40, 2000), rank8=True),
+          TensorSpec("model.action_expert.layers.20.w_n3.weight", (9000, 40), rank8=True)]
+    t += [TensorSpec(f"model.vlm.layers.{k}.ln.weight", (int(n),)) for k, n in enumerate(lens)]
+    return workloads.custom_workload("all_paths", t, policy="bf16_mixed", steps=2)
+
+
 def test_deterministic(mx):
-    w = _many_small_reduced()
+    """Two runs of the same steps give bitwise-identical parameters on every
+    Newton-Schulz path (no atomics; the narrow clusters add their partial
+    Gram tiles in rank order)."""
+    w = _all_paths_workload()
     outs = []
     for _ in range(2):
         masters = workloads.master_weights(w)
@@ -593,10 +612,10 @@ def test_tma_writeback_matches_register_writeback(mx, policy):
 
 def test_checkpoint_roundtrip_bitwise(mx):
     """get_state/set_state/set_step resume: a restored optimizer continues
-    bit for bit like the original."""
+    bit for bit like the original, on every Newton-Schulz path."""
     import torch
 
-    w = _many_small_reduced()
+    w = _all_paths_workload()
     masters = workloads.master_weights(w)
     a = GpuSide(w, masters)
     try:
