@@ -896,14 +896,15 @@ def test_grads_consumed_event_allows_overwriting_gradients(mx):
         gpu.close()
 
 
-@pytest.mark.parametrize("which", ["options", "small"])
+@pytest.mark.parametrize("which", ["options", "small", "all_paths"])
 def test_graph_mode_matches_direct_launches(mx, which):
     """Steps replayed from the captured CUDA graph (the default) and steps
     launched one kernel at a time give bitwise-identical parameters and
     shadows, with a different lr every step (the step's scalars are read from
     HBM) and with profiling (which forces direct launches) on for one step;
-    for per-product launches and for the fused small-matrix kernel."""
-    w = _options_workload() if which == "options" else _small_workload()
+    for per-product launches, the fused small-matrix kernel and the narrow
+    kernels' cluster launches."""
+    w = {"options": _options_workload, "small": _small_workload, "all_paths": _all_paths_workload}[which]()
     masters = workloads.master_weights(w)
     lrs = (w.lr, 0.5 * w.lr, 2.0 * w.lr)
     outs = []
