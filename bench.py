@@ -576,12 +576,11 @@ def run_ours(args):
             d["frac_hbm"] = round(d["gbs"] / peaks["hbm_gbs"], 3)
             d["frac_8tbs"] = round(d["gbs"] / 8000.0, 3)
             if k == "adamw":
-                d["note"] = ("second stream, beside the momentum pass and the Newton-Schulz chain: the event "
-                             "time includes sharing HBM and waiting for SMs (adamw_standalone times it alone)")
+                d["note"] = ("second stream, beside the momentum pass (the Newton-Schulz chain waits for it when "
+                             "it moves more bytes than that pass): the event time includes sharing HBM and SMs "
+                             "(adamw_standalone times it alone)")
             elif k == "momentum" and prof["adamw"]["launches"]:
                 d["note"] = "runs beside AdamW (second stream): both share HBM bandwidth"
-        elif k == "ns_prep" and prof["adamw"]["launches"]:
-            d["note"] = "its event time includes waiting for AdamW's blocks to leave the SMs"
         kernels[k] = d
     launches = sum(prof[k]["launches"] for k in KINDS)
     adam_alone = adamw_standalone(mx, torch, entries, w, lr, stream, peaks)

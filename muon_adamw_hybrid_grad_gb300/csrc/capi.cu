@@ -136,7 +136,7 @@ struct muon_adamw {
   cudaStream_t s0 = nullptr;  // caller's stream
   cudaStream_t s1 = nullptr;  // AdamW stream (library-owned)
   cudaStream_t s2 = nullptr;  // joins the gradient readers for muon_adamw_record_grads_consumed
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_fork = nullptr;
   cudaEvent_t ev_g0 = nullptr, ev_g1 = nullptr;  // last gradient reader of the latest step on s0 / s1
   bool g1_valid = false;                          // the latest step read gradients on s1
   StepParams* d_step = nullptr;                   // this step's scalars (arena)
@@ -1063,7 +1063,6 @@ ma_status muon_adamw_create(const muon_adamw_config* cfg, void* cuda_stream, muo
   cudaError_t e = cudaStreamCreateWithFlags(&h->s1, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->s2, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_g0, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_g1, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_slot[0], cudaEventDisableTiming);
@@ -1151,11 +1150,20 @@ static ma_status begin_step(muon_adamw* h, double lr) {
 
 // Finish a step once the clip coefficient is in h->d_scalars: the update
 // passes, the Newton-Schulz chain (one graph launch, or its launches one by
-// one) and the join of the AdamW stream; with grad_norm_out, wait and read.
+// one) and the join of the AdamW stream, before the chain or after it; with
+// grad_norm_out, wait and read.
 static ma_status finish_step(muon_adamw* h, float* grad_norm_out) {
   const muon_adamw_config& c = h->cfg;
   ma_status st = enqueue_update_passes(h);
   if (st != MA_OK) return st;
+  // Where AdamW moves more bytes than the momentum pass, the chain starts
+  // once AdamW is done: its long-running blocks hold every SM until they run
+  // out of work, so a chain launched earlier would only wait for them inside
+  // its first launch. Where AdamW is the smaller stream, its blocks retire
+  // one by one and the chain's first CTAs take their SMs as they do, so the
+  // join comes at the end of the step instead.
+  const bool join_first = h->g1_valid && h->bytes_adam > h->bytes_mom;
+  if (join_first) CUDA_TRY(cudaStreamWaitEvent(h->s0, h->ev_g1, 0));
   const bool graph = h->graph_mode && !h->graph_broken && !h->profiling && !h->stall_test &&
                      c.ns_kernel == MA_NS_TCGEN05 && h->n_mats > 0;
   if (graph && !h->gexec) capture_newton_schulz_graph(h);
@@ -1165,10 +1173,7 @@ static ma_status finish_step(muon_adamw* h, float* grad_norm_out) {
     st = enqueue_newton_schulz(h);
     if (st != MA_OK) return st;
   }
-  if (h->g1_valid) {
-    CUDA_TRY(cudaEventRecord(h->ev_join, h->s1));
-    CUDA_TRY(cudaStreamWaitEvent(h->s0, h->ev_join, 0));
-  }
+  if (h->g1_valid && !join_first) CUDA_TRY(cudaStreamWaitEvent(h->s0, h->ev_g1, 0));
   CUDA_TRY(cudaGetLastError());
   if (h->profiling) h->prof.steps += 1;
   if (grad_norm_out) {
@@ -1520,7 +1525,6 @@ ma_status muon_adamw_destroy(muon_adamw_t* h) {
   for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
   if (h->arena) cudaFree(h->arena);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
-  if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->ev_g0) cudaEventDestroy(h->ev_g0);
   if (h->ev_g1) cudaEventDestroy(h->ev_g1);
   if (h->gexec) cudaGraphExecDestroy(h->gexec);
