@@ -1016,12 +1016,16 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
 // operands: the rows coincide) and of B in B X, and as the MN-major right-hand
 // operand of B X (panels 16 KiB apart). Products accumulate in TMEM: A at
 // columns 0..127, A A at 128..255, X' = B X over columns 0..L-1 once those are
-// read. The epilogues (two warps per TMEM lane quarter) round to bf16 into the
-// panels; the last one updates the parameters from registers. The next
-// matrix's X is loaded by TMA as soon as the last B X has read X.
+// read. The CTA's 8 warps all run the epilogues (two warps per TMEM lane
+// quarter), which round to bf16 into the panels; the last one updates the
+// parameters from registers. Thread 0 also issues the copies and the MMAs:
+// the phases follow each other, every thread waiting at each product's
+// barrier, so no warp is set aside for issuing and a thread may hold up to
+// 255 registers. The next matrix's X is loaded by TMA as soon as the last
+// B X has read X.
 // ---------------------------------------------------------------------------
 constexpr int SMALL_EPI_WARPS = 8;
-constexpr int SMALL_THREADS = 32 * (1 + SMALL_EPI_WARPS);
+constexpr int SMALL_THREADS = 32 * SMALL_EPI_WARPS;
 constexpr int SMALL_PANEL = 128 * 64 * 2;  // 16 KiB
 
 struct SmallSmem {
@@ -1058,28 +1062,42 @@ __device__ __forceinline__ void small_get_row(const uint8_t* panels, int r, int 
   for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(row + (((q0 + j) ^ (r & 7)) << 4));
 }
 
-// Last-iteration update of one 32 x 32 block of a small matrix's parameter,
-// with the lanes along parameter rows (coalesced) and all 32 loads of p issued
-// before any store. Wide parameters (canonical row = parameter row) pass the
-// block through the warp's padded fp32 tile `t` to get there; for tall ones
-// (canonical row = parameter column) lane l already holds parameter column
-// row0 + l.
-__device__ __forceinline__ void small_apply_block(const MuonMat& M, float lrm, float dec, float rs, int row0,
-                                                  int col0, uint32_t taddr, float (*t)[33], int lane) {
-  // the matrix's fields in registers: the stores below go through generic
-  // pointers that could otherwise alias the descriptor and force its reloads;
-  // offsets in 32 bits (a small matrix has at most 128 x 512 elements)
-  float* const P = M.p;
-  uint16_t* const SH = M.shadow;
-  const int n = M.n;
-  const int s = M.s, l = M.l;
-  const bool tr = M.transposed != 0;
+// Last-iteration update of a small matrix's parameter in 32 x 32 blocks, with
+// the lanes along parameter rows (coalesced). Wide parameters (canonical row =
+// parameter row) pass a block through the warp's padded fp32 tile `t` to get
+// there; for tall ones (canonical row = parameter column) lane l already holds
+// parameter column row0 + l. A lane's part of a block: `nr` parameter rows
+// from offset `base` (one element per row, a row apart).
+struct SmallBlk {
+  int base, nr;
+};
+
+__device__ __forceinline__ SmallBlk small_block_at(int n, int s, int l, bool tr, int row0, int col0, int lane) {
+  SmallBlk b;
+  if (!tr) {
+    const int gc = col0 + lane;
+    b.base = row0 * n + gc;
+    b.nr = gc < l ? s - row0 : 0;
+  } else {
+    const int gc = row0 + lane;
+    b.base = col0 * n + gc;
+    b.nr = gc < s ? l - col0 : 0;
+  }
+  if (b.nr > 32) b.nr = 32;
+  return b;
+}
+
+__device__ __forceinline__ void small_load_block(const float* P, int n, SmallBlk b, float (&pv)[32]) {
+#pragma unroll
+  for (int r = 0; r < 32; ++r) pv[r] = r < b.nr ? P[b.base + r * n] : 0.f;
+}
+
+// The block's update direction for this lane's parameter column, from TMEM.
+__device__ __forceinline__ void small_block_dir(uint32_t taddr, float rs, bool tr, float (*t)[33], int lane,
+                                                float (&o)[32]) {
   uint32_t v[32];
   tmem_ld_32x32b_x32(taddr, v);
   tmem_ld_wait();
-  float o[32];
-  int gc, nr;      // this lane's parameter column; rows of the block inside the parameter
-  int base;        // parameter offset of the block's first row at this lane's column
   if (!tr) {
 #pragma unroll
     for (int e = 0; e < 32; ++e) t[lane][e] = __uint_as_float(v[e]) * rs;
@@ -1087,34 +1105,26 @@ __device__ __forceinline__ void small_apply_block(const MuonMat& M, float lrm, f
 #pragma unroll
     for (int r = 0; r < 32; ++r) o[r] = t[r][lane];
     __syncwarp();
-    gc = col0 + lane;
-    nr = s - row0;
-    base = row0 * n + gc;
-    if (gc >= l) nr = 0;
   } else {
 #pragma unroll
     for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * rs;
-    gc = row0 + lane;
-    nr = l - col0;
-    base = col0 * n + gc;
-    if (gc >= s) nr = 0;
   }
-  if (nr > 32) nr = 32;
-  float pv[32];
-#pragma unroll
-  for (int r = 0; r < 32; ++r) pv[r] = r < nr ? P[base + r * n] : 0.f;
+}
+
+__device__ __forceinline__ void small_store_block(float* P, uint16_t* SH, int n, SmallBlk b, float dec, float lrm,
+                                                  const float (&pv)[32], const float (&o)[32]) {
 #pragma unroll
   for (int r = 0; r < 32; ++r) {
-    if (r < nr) {
+    if (r < b.nr) {
       const float q = fmaf(pv[r], dec, -lrm * o[r]);
-      P[base + r * n] = q;
-      if (SH) SH[base + r * n] = ns_f2bf(q);
+      P[b.base + r * n] = q;
+      if (SH) SH[b.base + r * n] = ns_f2bf(q);
     }
   }
 }
 
 // L1 prefetch of a 32 x 32 parameter block of a small matrix (the layout of
-// small_apply_block): lane r takes the 128 bytes of the block's r-th
+// small_block_at): lane r takes the 128 bytes of the block's r-th
 // parameter row, so the block's loads find it close when they come.
 __device__ __forceinline__ void small_prefetch_block(const MuonMat& M, int row0, int col0, int lane) {
   const bool tr = M.transposed != 0;
@@ -1164,7 +1174,7 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) ns_small_kernel(const __grid
   };
   // epilogue geometry: TMEM lane quarter (rows) and alternate 32-column blocks
   const int quarter = warp & 3;
-  const int half = (warp - 1) >> 2;
+  const int half = warp >> 2;
   const int row = 32 * quarter + lane;  // this lane's canonical row
   const uint32_t tq = tmem + ((uint32_t)(32 * quarter) << 16);
 
@@ -1212,7 +1222,7 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) ns_small_kernel(const __grid
       mma_ph ^= 1u;
       mma_out = false;
       tc_fence_after();
-      if (warp >= 1) {
+      {
         const float sc = first ? r * r : 1.f;
         for (int c0 = 32 * half; c0 < 128; c0 += 64) {
           uint32_t v[32];
@@ -1249,7 +1259,7 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) ns_small_kernel(const __grid
       mma_ph ^= 1u;
       mma_out = false;
       tc_fence_after();
-      if (warp >= 1) {
+      {
         for (int c0 = 32 * half; c0 < 128; c0 += 64) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tq + 128u + (uint32_t)c0, v);
@@ -1279,7 +1289,10 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) ns_small_kernel(const __grid
       tc_fence_before();
       __syncthreads();
       // the last iteration's update starts with this warp's first parameter block
-      if (last && warp >= 1) small_prefetch_block(M, 32 * quarter, 32 * half, lane);
+      if (last) {
+        small_prefetch_block(M, 32 * quarter, 32 * half, lane);
+        small_prefetch_block(M, 32 * quarter, 32 * half + 64, lane);
+      }
       // ---- X' = B X (columns 0..L-1) ----
       if (threadIdx.x == 0) {
         tc_fence_after();
@@ -1301,7 +1314,7 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) ns_small_kernel(const __grid
       mma_out = false;
       tc_fence_after();
       if (!last) {
-        if (warp >= 1) {
+        {
           const float sc = first ? r : 1.f;
           // two blocks per TMEM wait (L is a multiple of 128: blocks c0 and c0 + 64 both exist)
           for (int c0 = 32 * half; c0 < L.L; c0 += 128) {
@@ -1331,15 +1344,34 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) ns_small_kernel(const __grid
           load_x(mat + gridDim.x);
           pending = true;
         }
-        if (warp >= 1) {
+        {
           // A and B are free now: a padded 32 x 33 fp32 tile per epilogue warp
-          float(*t)[33] = reinterpret_cast<float(*)[33]>(Ap + (size_t)(warp - 1) * 32 * 33 * 4);
+          float(*t)[33] = reinterpret_cast<float(*)[33]>(Ap + (size_t)warp * 32 * 33 * 4);
           const float rs = first ? r : 1.f;
           const float lrm = L.sp->ns_lr * M.lr_mult;
           const float dec = L.sp->ns_decay[M.group];
-          for (int c0 = 32 * half; c0 < l; c0 += 64) {
-            if (c0 + 64 < l) small_prefetch_block(M, 32 * quarter, c0 + 64, lane);  // the next block
-            small_apply_block(M, lrm, dec, rs, 32 * quarter, c0, tq + (uint32_t)c0, t, lane);
+          // the matrix's fields in registers: the stores below go through
+          // generic pointers that could otherwise alias the descriptor
+          float* const P = M.p;
+          uint16_t* const SH = M.shadow;
+          const int n = M.n, row0 = 32 * quarter;
+          const bool tr = M.transposed != 0;
+          // each block's loads are issued before the previous block's stores
+          int c0 = 32 * half;
+          SmallBlk b = small_block_at(n, s, l, tr, row0, c0, lane);
+          float pv[32];
+          small_load_block(P, n, b, pv);
+          for (; c0 < l; c0 += 64) {
+            if (c0 + 128 < l) small_prefetch_block(M, row0, c0 + 128, lane);
+            const SmallBlk bn = c0 + 64 < l ? small_block_at(n, s, l, tr, row0, c0 + 64, lane) : SmallBlk{0, 0};
+            float pn[32];
+            small_load_block(P, n, bn, pn);
+            float o[32];
+            small_block_dir(tq + (uint32_t)c0, rs, tr, t, lane, o);
+            small_store_block(P, SH, n, b, dec, lrm, pv, o);
+#pragma unroll
+            for (int r = 0; r < 32; ++r) pv[r] = pn[r];
+            b = bn;
           }
         }
       }
